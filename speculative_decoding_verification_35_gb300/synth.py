@@ -1,0 +1,170 @@
+"""Seeded synthetic logit batches shaped like the verify-step workloads.
+
+This module is the one piece shared by the CUDA path's tests/bench and the CPU oracle. It holds none
+of the verify step's arithmetic: it draws logits (Gaussian noise plus a Zipf log-prior over the
+vocabulary index), rounds them once to the kernel dtype, and draws the draft tokens from the draft
+distribution with the Gumbel-max trick (argmax of l/T + Gumbel noise), which samples softmax(l/T)
+exactly by a different route than the verify step's inverse CDF. Greedy workloads take the draft's
+argmax as its token. All randomness comes from numpy's PCG64 with per-workload seeds.
+
+No dataset is used: the pages measure nothing on the verify step itself, and these synthetic batches
+stand in for the decode batches the pages describe (draft model proposes gamma tokens, target scores
+gamma + 1 positions; "Accelerating Sonar through speculation", §"Speculative decoding" steps 2-4).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+F32, BF16 = "f32", "bf16"
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    V: int
+    dtype: str
+    temperature: float
+    gamma: int | None            # fixed gamma, or None for the ragged U{gamma_lo..gamma_hi} draw
+    target_sigma: float
+    zipf_s: float                # 0: no prior
+    draft_scale: float           # draft = draft_scale * target + N(0, draft_sigma^2)
+    draft_sigmas: tuple          # per-sequence sigma cycle (b mod len)
+    gamma_lo: int = 1
+    gamma_hi: int = 8
+    seed: int = 0
+    tags: tuple = field(default_factory=tuple)
+
+    @property
+    def greedy(self) -> bool:
+        return self.temperature == 0.0
+
+
+# Workloads named by what they are. The seeds only make each workload's draw distinct.
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("b1_g4_v1024_f32", 1, 1024, F32, 1.0, 4, 2.0, 0.0, 1.0, (0.5,), seed=1000),
+        Workload("b8_g4_v32000_t0.7", 8, 32000, BF16, 0.7, 4, 3.0, 1.1, 0.9, (1.0,), seed=2000),
+        Workload("b8_g4_v32000_greedy", 8, 32000, BF16, 0.0, 4, 3.0, 1.1, 0.9, (1.0,), seed=2000),
+        Workload("b64_g5_v128256", 64, 128256, BF16, 1.0, 5, 2.5, 1.1, 1.0, (0.3, 1.0, 2.0), seed=3000),
+        Workload("b256_g3_v152064_t0.8", 256, 152064, BF16, 0.8, 3, 2.0, 1.05, 1.0, (0.8,), seed=4000),
+        Workload("ragged_b128_v129280", 128, 129280, BF16, 1.0, None, 2.0, 1.1, 1.0, (1.0,), seed=5000),
+    ]
+}
+
+# The workload the headline throughput is quoted on.
+HEADLINE = "b64_g5_v128256"
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round to bfloat16 (round to nearest even, via float32) and return the raw 16-bit codes."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclass
+class Batch:
+    workload: Workload
+    target: np.ndarray           # [R_t, V] float32, or uint16 raw bf16 codes
+    draft: np.ndarray | None     # [R_d, V], same dtype as target (None only when R_d == 0)
+    draft_tokens: np.ndarray     # [R_d] int32
+    seq_offsets: np.ndarray      # [B+1] int32, prefix sum of gammas over draft rows
+    gammas: np.ndarray           # [B] int32
+
+    @property
+    def B(self):
+        return len(self.gammas)
+
+    @property
+    def V(self):
+        return int(self.target.shape[1])
+
+    @property
+    def R_t(self):
+        return int(self.seq_offsets[-1]) + self.B
+
+    @property
+    def R_d(self):
+        return int(self.seq_offsets[-1])
+
+    @property
+    def temperature(self):
+        return self.workload.temperature
+
+    @property
+    def elem_bytes(self):
+        return 2 if self.workload.dtype == BF16 else 4
+
+    def logits_f32(self, which: str) -> np.ndarray:
+        a = self.target if which == "target" else self.draft
+        return bf16_bits_to_f32(a) if self.workload.dtype == BF16 else a
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes the verify step must move at least: every logit it needs read once, plus the
+        small index arrays and outputs."""
+        rows = self.R_t if self.workload.greedy else self.R_t + self.R_d
+        return (rows * self.V * self.elem_bytes + 4 * self.R_d + 4 * (self.B + 1) + 4 * self.B
+                + 4 * self.R_t + 4 * self.B)
+
+    def verified_rows(self) -> int:
+        return self.R_t if self.workload.greedy else self.R_t + self.R_d
+
+
+def _rows(rng, n, V, sigma, zipf_s):
+    prior = -zipf_s * np.log(np.arange(1, V + 1, dtype=np.float64)) if zipf_s else 0.0
+    return rng.normal(0.0, sigma, size=(n, V)) + prior
+
+
+def make_batch(name_or_w, B: int | None = None, V: int | None = None, gammas=None,
+               seed_offset: int = 0) -> Batch:
+    """Draw one batch. ``B``/``V``/``gammas`` override the workload's sizes (smaller parity cases
+    with the same value distributions); ``seed_offset`` selects another independent draw."""
+    w = WORKLOADS[name_or_w] if isinstance(name_or_w, str) else name_or_w
+    B = w.B if B is None else B
+    V = w.V if V is None else V
+    rng = np.random.Generator(np.random.PCG64(w.seed + seed_offset))
+    if gammas is None:
+        if w.gamma is None:
+            gammas = rng.integers(w.gamma_lo, w.gamma_hi + 1, size=B)
+        else:
+            gammas = np.full(B, w.gamma)
+    gammas = np.asarray(gammas, dtype=np.int32)
+    offs = np.zeros(B + 1, dtype=np.int32)
+    offs[1:] = np.cumsum(gammas)
+    R_d = int(offs[-1])
+    R_t = R_d + B
+    out_dtype = np.uint16 if w.dtype == BF16 else np.float32
+    target = np.empty((R_t, V), dtype=out_dtype)
+    draft = np.empty((R_d, V), dtype=out_dtype)
+    tokens = np.zeros(R_d, dtype=np.int32)
+    tok_rng = np.random.Generator(np.random.PCG64(w.seed + seed_offset + 7))
+    for b in range(B):
+        g = int(gammas[b])
+        d0 = int(offs[b])
+        t0 = d0 + b
+        t64 = _rows(rng, g + 1, V, w.target_sigma, w.zipf_s)
+        sig = w.draft_sigmas[b % len(w.draft_sigmas)]
+        d64 = w.draft_scale * t64[:g] + rng.normal(0.0, sig, size=(g, V))
+        if w.dtype == BF16:
+            target[t0:t0 + g + 1] = to_bf16_bits(t64)
+            draft[d0:d0 + g] = to_bf16_bits(d64)
+            dl = bf16_bits_to_f32(draft[d0:d0 + g]).astype(np.float64)
+        else:
+            target[t0:t0 + g + 1] = t64.astype(np.float32)
+            draft[d0:d0 + g] = d64.astype(np.float32)
+            dl = draft[d0:d0 + g].astype(np.float64)
+        if g:
+            if w.greedy:
+                tokens[d0:d0 + g] = np.argmax(dl, axis=1)
+            else:
+                gum = -np.log(-np.log(tok_rng.random(size=(g, V)) + 1e-300) + 1e-300)
+                tokens[d0:d0 + g] = np.argmax(dl / w.temperature + gum, axis=1)
+    return Batch(w, target, draft if R_d else None, tokens, offs, gammas)
