@@ -1,0 +1,130 @@
+/*
+ * libspecverify: the speculative-sampling verify step on one GB300 (sm_103a).
+ *
+ * The operation (velog article "6-1편. Speculative Decoding", §2 "4-step algorithm" steps 3-4,
+ * §2-1 accept/reject rule, §2-2 corrected distribution and sampling; greedy variant from
+ * "All About Transformer Inference", Appendix D "Speculative Sampling", steps 1-3; the bonus token
+ * from "Accelerating Sonar through speculation", §"Speculative decoding"):
+ *
+ *   for every sequence b of a CSR-packed batch, with gamma_b drafted tokens x_0..x_{gamma_b - 1}:
+ *     p_i = softmax(target_logits[row t0 + i] / T)   for i = 0..gamma_b      (gamma_b + 1 rows)
+ *     q_i = softmax(draft_logits[row d0 + i] / T)    for i = 0..gamma_b - 1  (gamma_b rows)
+ *     accept x_i while u_i * q_i(x_i) < p_i(x_i)  (probability min(1, p/q)), in slot order;
+ *     at the first rejected slot n draw a token from norm(max(0, p_n - q_n));
+ *     if all gamma_b drafts are accepted (n = gamma_b) draw a bonus token from p_gamma.
+ *   Draws use the inverse CDF in vocabulary index order: the smallest k whose running weight sum
+ *   exceeds u' * (total weight); if rounding leaves none, the last k with positive weight.
+ *   Greedy (T == 0): accept x_i while it equals argmax(target row t0 + i) (lowest index on ties);
+ *   emit that argmax at the first mismatch, or argmax(target row t0 + gamma_b) when all match.
+ *   Uniforms: u = (Philox4x32-10(ctr, key).word0 >> 8) * 2^-24 with key = (seed lo32, seed hi32) and
+ *   ctr = (step lo32, step hi32, b, (slot << 8) | purpose), purpose 0 for the accept test of slot
+ *   i and 1 for the draw at the emitting slot; b is the global sequence index.
+ *
+ * Layout (all row-major, row stride V elements, no padding):
+ *   seq_offsets  int32[B + 1], seq_offsets[0] = 0, seq_offsets[b+1] - seq_offsets[b] = gammas[b].
+ *   draft rows of b: seq_offsets[b] .. seq_offsets[b+1] - 1           (R_d = seq_offsets[B] rows)
+ *   target rows of b: seq_offsets[b] + b .. seq_offsets[b+1] + b        (R_t = R_d + B rows)
+ *   draft_tokens int32[R_d], aligned with the draft rows.
+ *   out_tokens   int32[R_t], aligned with the target rows: slot j of b at seq_offsets[b] + b + j holds
+ *                x_j for j < n, the drawn token at j = n, and -1 for n < j <= gamma_b.
+ *   out_num_accepted int32[B]: n for every sequence, -1 for a sequence that failed a device check.
+ *
+ * Ownership and errors: every array argument is a DEVICE pointer owned by the caller; the library
+ * never frees or retains them. Host-side argument errors return SV_ERR_INVALID_ARG (or
+ * SV_ERR_WORKSPACE) before anything is launched. Data errors found on the device set bit
+ * (1u << code) of the device status word. Inconsistent CSR offsets (seq_offsets[0] != 0, a gap
+ * that differs from gammas[b], a negative gamma or one above max_gamma) fail the whole batch before
+ * any logit row is read: every out_num_accepted is -1 and out_tokens is not written. A draft token
+ * outside [0, V), a NaN or +inf logit, or a row whose logits are all -inf (-inf entries are
+ * otherwise allowed and mean p = 0) fail only their sequence: its out_num_accepted is -1 and its
+ * out_tokens slots are -1. No device check traps.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1, /* bad scalar, NULL pointer, misaligned pointer, unsupported size */
+    SV_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
+    SV_ERR_BAD_TOKEN = 3,   /* device: draft token outside [0, V) */
+    SV_ERR_BAD_OFFSETS = 4, /* device: seq_offsets / gammas inconsistent or gamma > max_gamma */
+    SV_ERR_NONFINITE = 5,   /* device: NaN or +inf logit in a row the step reads */
+    SV_ERR_EMPTY_ROW = 6,   /* device: a row whose logits are all -inf */
+    SV_ERR_TIMEOUT = 7,     /* device: a bounded wait gave up (reserved; no path waits today) */
+    SV_ERR_WORKSPACE = 8    /* workspace NULL or smaller than spec_verify_workspace_size() */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Largest gamma_b one call accepts: the accept decisions of a sequence are one warp's lanes. */
+#define SV_MAX_GAMMA 31
+
+/*
+ * Optional intermediate values (every field a nullable DEVICE pointer). Rows are numbered target
+ * rows first (0 .. R_t - 1) then draft rows (R_t .. R_t + R_d - 1).
+ *   row_lse    double[R_t + R_d]: log sum_k exp(l_k / T) of each row (sampling mode only).
+ *   row_argmax int32[R_t]: argmax of each target row, lowest index on ties (greedy mode only).
+ *   p_x, q_x   double[R_d]: p_i(x_i) and q_i(x_i) of every draft slot (sampling mode only).
+ *   seq_mass   double[B]: total weight S of the sequence's draw relative to p (1 - beta at a
+ *              rejected slot; about 1 for a bonus draw) (sampling mode only).
+ */
+typedef struct {
+    double* row_lse;
+    int32_t* row_argmax;
+    double* p_x;
+    double* q_x;
+    double* seq_mass;
+} sv_debug;
+
+/*
+ * The plain form: bf16 logits, the legacy default stream, blocking. It allocates its own
+ * workspace and device status word, waits for the step to finish and returns SV_OK or the first
+ * device error code (priority BAD_OFFSETS, BAD_TOKEN, NONFINITE, EMPTY_ROW, TIMEOUT). Host sizes
+ * are read from gammas (copied to the host once) to size the workspace. temperature == 0 selects
+ * greedy, in which case draft_logits may be NULL and is never read.
+ */
+int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V,
+                float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                int32_t* out_num_accepted);
+
+/* Bytes of device workspace spec_verify_ex needs for B sequences of gamma_b <= max_gamma over a
+ * vocabulary of V. Returns 0 for invalid sizes. */
+size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t max_gamma);
+
+/*
+ * The full form: asynchronous on `cuda_stream` (a cudaStream_t; NULL = legacy default stream), no
+ * allocation and no host synchronisation. Requirements checked on the host: B >= 0, V >= 1,
+ * 0 <= max_gamma <= SV_MAX_GAMMA, temperature finite and >= 0 with log2(e) / temperature finite in
+ * float32 when positive, non-NULL target_logits / seq_offsets / gammas / draft_tokens / outputs,
+ * non-NULL draft_logits when temperature > 0, workspace of at least
+ * spec_verify_workspace_size(B, V, max_gamma) bytes aligned to 256 bytes. Rows may be at any
+ * element alignment; 16-byte-aligned rows take the vectorised path. device_status (nullable) is a
+ * device uint32 that the call ORs error bits into; the caller clears it. The workspace must not be
+ * shared by calls that may overlap on the GPU. Returns SV_OK once the work is enqueued.
+ */
+int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                   const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                   int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
+                   uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                   uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                   const sv_debug* debug, void* cuda_stream);
+
+/* Map a device status word (OR of 1u << code) to one status code, by the priority above. */
+int spec_verify_status_from_bits(uint32_t bits);
+
+/* Static, human-readable name of a status code. */
+const char* spec_verify_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

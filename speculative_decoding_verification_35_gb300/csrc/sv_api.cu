@@ -1,0 +1,139 @@
+// C ABI of libspecverify (declared in include/specverify.h): host-side validation, workspace layout
+// and the launch of the verify step on the caller's stream.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+#include "sv_internal.h"
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t max_gamma) {
+    if (B < 0 || V < 1 || max_gamma < 0 || max_gamma > SV_MAX_GAMMA) return 0;
+    return workspace_layout(B, V, max_gamma).total;
+}
+
+int spec_verify_status_from_bits(uint32_t bits) {
+    static const int order[] = {SV_ERR_BAD_OFFSETS, SV_ERR_BAD_TOKEN, SV_ERR_NONFINITE, SV_ERR_EMPTY_ROW,
+                                SV_ERR_TIMEOUT};
+    for (int c : order)
+        if (bits & (1u << c)) return c;
+    for (int c = 1; c < 32; ++c)
+        if (bits & (1u << c)) return c;
+    return SV_OK;
+}
+
+const char* spec_verify_status_string(int status) {
+    switch (status) {
+        case SV_OK: return "SV_OK";
+        case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: bad scalar, NULL or misaligned pointer, or unsupported size";
+        case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA call or kernel launch failed";
+        case SV_ERR_BAD_TOKEN: return "SV_ERR_BAD_TOKEN: a draft token lies outside [0, V)";
+        case SV_ERR_BAD_OFFSETS: return "SV_ERR_BAD_OFFSETS: seq_offsets / gammas inconsistent or gamma above max_gamma";
+        case SV_ERR_NONFINITE: return "SV_ERR_NONFINITE: NaN or +inf logit";
+        case SV_ERR_EMPTY_ROW: return "SV_ERR_EMPTY_ROW: a row whose logits are all -inf";
+        case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded device wait gave up";
+        case SV_ERR_WORKSPACE: return "SV_ERR_WORKSPACE: workspace missing, too small or not 256-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                   const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                   int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
+                   uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                   uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                   const sv_debug* debug, void* cuda_stream) {
+    if (B < 0 || V < 1 || max_gamma < 0 || max_gamma > SV_MAX_GAMMA) return SV_ERR_INVALID_ARG;
+    if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+    if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.f;
+    const double K64 = greedy ? 0.0 : 1.4426950408889634074 / (double)temperature;
+    const float K_hi = (float)K64;
+    if (!greedy && !std::isfinite(K_hi)) return SV_ERR_INVALID_ARG;
+    if (!target_logits || !seq_offsets || !gammas || !out_tokens || !out_num_accepted) return SV_ERR_INVALID_ARG;
+    if (max_gamma > 0 && (!draft_tokens || (!greedy && !draft_logits))) return SV_ERR_INVALID_ARG;
+    const size_t esz = dtype == SV_BF16 ? 2 : 4;
+    if ((uintptr_t)target_logits % esz || (draft_logits && (uintptr_t)draft_logits % esz)) return SV_ERR_INVALID_ARG;
+    if ((uintptr_t)seq_offsets % 4 || (uintptr_t)gammas % 4 || (uintptr_t)out_tokens % 4 ||
+        (uintptr_t)out_num_accepted % 4 || (draft_tokens && (uintptr_t)draft_tokens % 4))
+        return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    const Layout L = workspace_layout(B, V, max_gamma);
+    if (!workspace || workspace_bytes < L.total || (uintptr_t)workspace % 256) return SV_ERR_WORKSPACE;
+
+    const bool uses_draft = !greedy && max_gamma > 0;
+    const bool vec = (uintptr_t)target_logits % 16 == 0 && (!uses_draft || (uintptr_t)draft_logits % 16 == 0) &&
+                     ((size_t)V * esz) % 16 == 0;
+    char* ws = (char*)workspace;
+    Params P{};
+    P.target = target_logits;
+    P.draft = draft_logits;
+    P.tokens = draft_tokens;
+    P.offs = seq_offsets;
+    P.gammas = gammas;
+    P.B = B;
+    P.V = V;
+    P.max_gamma = max_gamma;
+    P.nchunks = (V + kChunk - 1) / kChunk;
+    P.nsub = (V + kSub - 1) / kSub;
+    P.K_hi = K_hi;
+    P.K_lo = (float)(K64 - (double)K_hi);
+    P.K64 = K64;
+    P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;
+    P.seed = seed;
+    P.step = step;
+    P.out_tokens = out_tokens;
+    P.out_n = out_num_accepted;
+    P.status = device_status ? device_status : (uint32_t*)(ws + L.status);
+    if (debug) P.dbg = *debug;
+    P.partials = (Partial*)(ws + L.partials);
+    P.tasks = (SeqTask*)(ws + L.tasks);
+    P.subs = (SubSum*)(ws + L.subs);
+    P.batch_bad = (uint32_t*)(ws + L.batch_bad);
+    const cudaError_t e = launch_verify(P, (int)dtype, vec, greedy, (cudaStream_t)cuda_stream);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, float temperature,
+                uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted) {
+    if (B < 0 || !gammas) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    std::vector<int32_t> g((size_t)B);
+    if (cudaMemcpy(g.data(), gammas, sizeof(int32_t) * (size_t)B, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SV_ERR_CUDA;
+    int32_t max_gamma = 0;
+    for (int32_t v : g) {
+        if (v < 0 || v > SV_MAX_GAMMA) return SV_ERR_INVALID_ARG;
+        max_gamma = std::max(max_gamma, v);
+    }
+    const size_t need = spec_verify_workspace_size(B, V, max_gamma);
+    if (!need) return SV_ERR_INVALID_ARG;
+    void* ws = nullptr;
+    uint32_t* st = nullptr;
+    if (cudaMalloc(&ws, need) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaMalloc((void**)&st, sizeof(uint32_t)) != cudaSuccess) {
+        cudaFree(ws);
+        return SV_ERR_CUDA;
+    }
+    int rc = SV_OK;
+    uint32_t bits = 0;
+    if (cudaMemsetAsync(st, 0, sizeof(uint32_t), 0) != cudaSuccess) rc = SV_ERR_CUDA;
+    if (rc == SV_OK)
+        rc = spec_verify_ex(target_logits, draft_logits, SV_BF16, draft_tokens, seq_offsets, gammas, B, V,
+                            max_gamma, temperature, seed, step, out_tokens, out_num_accepted, st, ws, need,
+                            nullptr, nullptr);
+    if (rc == SV_OK && (cudaStreamSynchronize(0) != cudaSuccess ||
+                        cudaMemcpy(&bits, st, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess))
+        rc = SV_ERR_CUDA;
+    cudaFree(st);
+    cudaFree(ws);
+    if (rc != SV_OK) return rc;
+    return spec_verify_status_from_bits(bits);
+}
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+"""Python binding of libspecverify (argument marshalling only).
+
+Every function here forwards to the C ABI declared in ``include/specverify.h``; all of the verify step
+runs in the library's CUDA kernels. PyTorch supplies device memory and streams. If the compiled library
+is missing this module raises at import time: there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_CUDA, SV_ERR_BAD_TOKEN, SV_ERR_BAD_OFFSETS = 0, 1, 2, 3, 4
+SV_ERR_NONFINITE, SV_ERR_EMPTY_ROW, SV_ERR_TIMEOUT, SV_ERR_WORKSPACE = 5, 6, 7, 8
+SV_F32, SV_BF16 = 0, 1
+SV_MAX_GAMMA = 31
+
+# every exported symbol of the C ABI, in header order
+EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex",
+           "spec_verify_status_from_bits", "spec_verify_status_string")
+
+
+class SvDebug(ctypes.Structure):
+    _fields_ = [("row_lse", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p),
+                ("p_x", ctypes.c_void_p), ("q_x", ctypes.c_void_p), ("seq_mass", ctypes.c_void_p)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libspecverify.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, u64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t
+    L.spec_verify.argtypes = [vp, vp, vp, vp, vp, i32, i32, f32, u64, u64, vp, vp]
+    L.spec_verify.restype = ctypes.c_int
+    L.spec_verify_workspace_size.argtypes = [i32, i32, i32]
+    L.spec_verify_workspace_size.restype = sz
+    L.spec_verify_ex.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
+                                 vp, vp, sz, ctypes.POINTER(SvDebug), vp]
+    L.spec_verify_ex.restype = ctypes.c_int
+    L.spec_verify_status_from_bits.argtypes = [ctypes.c_uint32]
+    L.spec_verify_status_from_bits.restype = ctypes.c_int
+    L.spec_verify_status_string.argtypes = [ctypes.c_int]
+    L.spec_verify_status_string.restype = ctypes.c_char_p
+    return L
+
+
+lib = _load()
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, seq_offsets, gammas, B, V, temperature,
+                seed, step, out_tokens, out_num_accepted) -> int:
+    """Blocking bf16 form on the legacy default stream. Pointer arguments are device addresses (int)."""
+    return lib.spec_verify(target_logits, draft_logits, draft_tokens, seq_offsets, gammas, B, V,
+                           float(temperature), seed, step, out_tokens, out_num_accepted)
+
+
+def spec_verify_workspace_size(B, V, max_gamma) -> int:
+    return lib.spec_verify_workspace_size(B, V, max_gamma)
+
+
+def spec_verify_ex(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                   temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
+                   workspace_bytes, debug: SvDebug | None, cuda_stream) -> int:
+    """Asynchronous form. Pointer arguments are device addresses (int or None)."""
+    return lib.spec_verify_ex(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V,
+                              max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
+                              device_status, workspace, workspace_bytes,
+                              ctypes.byref(debug) if debug is not None else None, cuda_stream)
+
+
+def spec_verify_status_from_bits(bits: int) -> int:
+    return lib.spec_verify_status_from_bits(bits)
+
+
+def spec_verify_status_string(status: int) -> str:
+    return lib.spec_verify_status_string(status).decode()
+
+
+# ------------------------------------------------------------------------------------------------
+# torch marshalling helpers
+# ------------------------------------------------------------------------------------------------
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+class Call:
+    """Device buffers of one verify call, allocated once and reused (workspace, outputs, status).
+
+    ``run`` enqueues spec_verify_ex on the given stream and returns its host status code.
+    """
+
+    def __init__(self, B: int, V: int, max_gamma: int, R_t: int, R_d: int, device="cuda", debug=False):
+        import torch
+        self.B, self.V, self.max_gamma, self.R_t, self.R_d = B, V, max_gamma, R_t, R_d
+        self.ws_bytes = spec_verify_workspace_size(B, V, max_gamma)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.out_tokens = torch.empty(R_t, dtype=torch.int32, device=device)
+        self.out_n = torch.empty(B, dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.dbg = None
+        self.dbg_struct = None
+        if debug:
+            self.dbg = dict(row_lse=torch.full((R_t + R_d,), float("nan"), dtype=torch.float64, device=device),
+                            row_argmax=torch.full((R_t,), -7, dtype=torch.int32, device=device),
+                            p_x=torch.full((R_d,), float("nan"), dtype=torch.float64, device=device),
+                            q_x=torch.full((R_d,), float("nan"), dtype=torch.float64, device=device),
+                            seq_mass=torch.full((B,), float("nan"), dtype=torch.float64, device=device))
+            self.dbg_struct = SvDebug(*(self.dbg[k].data_ptr() for k in
+                                        ("row_lse", "row_argmax", "p_x", "q_x", "seq_mass")))
+
+    def run(self, target, draft, draft_tokens, seq_offsets, gammas, temperature, seed, step, stream=None,
+            clear_status=True) -> int:
+        import torch
+        if clear_status:
+            self.status.zero_()
+        st = stream if stream is not None else torch.cuda.current_stream()
+        return spec_verify_ex(_ptr(target), _ptr(draft), dtype_code(target), _ptr(draft_tokens),
+                              _ptr(seq_offsets), _ptr(gammas), self.B, self.V, self.max_gamma, temperature,
+                              seed, step, _ptr(self.out_tokens), _ptr(self.out_n), _ptr(self.status),
+                              _ptr(self.workspace), self.ws_bytes, self.dbg_struct, st.cuda_stream)
+
+    def status_bits(self) -> int:
+        return int(self.status.item()) & 0xFFFFFFFF

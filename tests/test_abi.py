@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports every symbol include/specverify.h declares (CPU).
+
+Only host-side argument checks are exercised here: they return before any CUDA call, so they run
+without a GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from speculative_decoding_verification_35_gb300 import _build
+    return _build.build()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ ]*[\s\*]+([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex",
+                          "spec_verify_status_from_bits", "spec_verify_status_string"}
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    out = subprocess.run(["nm", "-D", "--defined-only", libpath], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+    L = ctypes.CDLL(libpath)
+    for name in declared_functions():
+        assert hasattr(L, name)
+
+
+def test_binding_lists_every_export(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    assert set(sv.EXPORTS) == set(declared_functions())
+
+
+def test_header_compiles_as_c(tmp_path):
+    c = tmp_path / "t.c"
+    c.write_text('#include "specverify.h"\nint main(void){ sv_debug d = {0}; (void)d; return SV_OK; }\n')
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-c", str(c),
+                           "-o", str(tmp_path / "t.o")])
+
+
+def test_host_side_checks_without_gpu(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    assert sv.spec_verify_workspace_size(64, 128256, 5) > 0
+    assert sv.spec_verify_workspace_size(-1, 10, 1) == 0
+    assert sv.spec_verify_workspace_size(4, 10, 32) == 0
+    fake = 1 << 20  # never dereferenced: every call below fails its host checks first
+    args = dict(target_logits=fake, draft_logits=fake, dtype=sv.SV_BF16, draft_tokens=fake, seq_offsets=fake,
+                gammas=fake, B=4, V=100, max_gamma=4, temperature=1.0, seed=1, step=0, out_tokens=fake,
+                out_num_accepted=fake, device_status=None, workspace=fake, workspace_bytes=1 << 30, debug=None,
+                cuda_stream=None)
+
+    def call(**kw):
+        a = dict(args); a.update(kw)
+        return sv.spec_verify_ex(**a)
+
+    assert call(temperature=-1.0) == sv.SV_ERR_INVALID_ARG
+    assert call(temperature=float("nan")) == sv.SV_ERR_INVALID_ARG
+    assert call(temperature=float("inf")) == sv.SV_ERR_INVALID_ARG
+    assert call(temperature=1e-45) == sv.SV_ERR_INVALID_ARG
+    assert call(V=0) == sv.SV_ERR_INVALID_ARG
+    assert call(B=-1) == sv.SV_ERR_INVALID_ARG
+    assert call(max_gamma=32) == sv.SV_ERR_INVALID_ARG
+    assert call(dtype=7) == sv.SV_ERR_INVALID_ARG
+    assert call(target_logits=None) == sv.SV_ERR_INVALID_ARG
+    assert call(draft_logits=None) == sv.SV_ERR_INVALID_ARG
+    assert call(draft_tokens=None) == sv.SV_ERR_INVALID_ARG
+    assert call(target_logits=fake + 1) == sv.SV_ERR_INVALID_ARG
+    assert call(workspace=None) == sv.SV_ERR_WORKSPACE
+    assert call(workspace_bytes=16) == sv.SV_ERR_WORKSPACE
+    assert call(workspace=fake + 64) == sv.SV_ERR_WORKSPACE
+    assert call(B=0) == sv.SV_OK  # nothing to do, nothing launched
+
+
+def test_status_helpers(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    assert sv.spec_verify_status_from_bits(0) == sv.SV_OK
+    assert sv.spec_verify_status_from_bits((1 << 5) | (1 << 3)) == sv.SV_ERR_BAD_TOKEN
+    assert sv.spec_verify_status_from_bits((1 << 5) | (1 << 4)) == sv.SV_ERR_BAD_OFFSETS
+    assert sv.spec_verify_status_from_bits(1 << 6) == sv.SV_ERR_EMPTY_ROW
+    for code in range(9):
+        assert sv.spec_verify_status_string(code).startswith("SV_")
