@@ -78,8 +78,9 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
     P.B = B;
     P.V = V;
     P.max_gamma = max_gamma;
-    P.nchunks = (V + kChunk - 1) / kChunk;
+    P.nchA = (V + kAChunk - 1) / kAChunk;
     P.nsub = (V + kSub - 1) / kSub;
+    P.nS = (V + kSTask - 1) / kSTask;
     P.K_hi = K_hi;
     P.K_lo = (float)(K64 - (double)K_hi);
     P.K64 = K64;
@@ -92,9 +93,13 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
     if (debug) P.dbg = *debug;
     P.partials = (Partial*)(ws + L.partials);
     P.tasks = (SeqTask*)(ws + L.tasks);
-    P.subs = (SubSum*)(ws + L.subs);
-    P.batch_bad = (uint32_t*)(ws + L.batch_bad);
-    const cudaError_t e = launch_verify(P, (int)dtype, vec, greedy, (cudaStream_t)cuda_stream);
+    P.subs = (double2*)(ws + L.subs);
+    P.stot = (double2*)(ws + L.stot);
+    P.ctr = (Counters*)(ws + L.counters);
+    P.a_done = (uint32_t*)(ws + L.a_done);
+    P.s_done = (uint32_t*)(ws + L.s_done);
+    P.seq_ready = (uint32_t*)(ws + L.seq_ready);
+    const cudaError_t e = launch_verify(P, L, workspace, (int)dtype, vec, greedy, (cudaStream_t)cuda_stream);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -107,6 +107,80 @@ __device__ __forceinline__ ff exp2_ff(float d_hi, float d_lo, float K_hi, float 
 }
 
 // ------------------------------------------------------------------------------------------------
+// Packed forms: two independent float-float values per register pair, so every floating-point step
+// issues once for two columns (Blackwell's f32x2 add / mul / fma).
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+struct ff2 {
+    float2 hi, lo;
+};
+
+// Running sums of two independent float-float streams.
+struct ffacc2 {
+    float2 hi = make_float2(0.f, 0.f), lo = make_float2(0.f, 0.f);
+    __device__ __forceinline__ void add(float2 h, float2 l) {
+        const float2 s = add2(hi, h);
+        const float2 bb = sub2(s, hi);
+        const float2 e = add2(sub2(hi, sub2(s, bb)), sub2(h, bb));  // exact error of hi + h
+        hi = s;
+        lo = add2(lo, add2(e, l));
+    }
+    // sum of both streams as one float-float value (exact split of the two hi parts)
+    __device__ __forceinline__ ffacc fold() const {
+        ffacc r;
+        float s, e;
+        two_sum(hi.x, hi.y, s, e);
+        r.hi = s;
+        r.lo = __fadd_rn(__fadd_rn(lo.x, lo.y), e);
+        return r;
+    }
+};
+
+// 2^((l - m) K) for two columns, precise as exp2_ff: the subtraction split exactly (TwoSum), the
+// argument carried as float-float, Tang's table step and the e^y - 1 series on |y| <= ln2/128.
+// Columns whose argument is below -125.5 (including -inf logits) give exactly 0.
+__device__ __forceinline__ ff2 exp2_ff2(float2 l, float2 m, float K_hi, float K_lo, const float2* tab) {
+    const float2 Kh = f2(K_hi), Kl = f2(K_lo);
+    // d = l - m exactly as d_hi + d_lo
+    const float2 d_hi = sub2(l, m);
+    const float2 bb = sub2(d_hi, l);
+    const float2 d_lo = add2(sub2(l, sub2(d_hi, bb)), sub2(make_float2(-m.x, -m.y), bb));
+    // t = d * K as t_hi + t_lo
+    const float2 t_hi = mul2(d_hi, Kh);
+    float2 t_lo = fma2(d_hi, Kh, make_float2(-t_hi.x, -t_hi.y));
+    t_lo = fma2(d_hi, Kl, t_lo);
+    t_lo = fma2(d_lo, Kh, t_lo);
+    const bool ok0 = t_hi.x > -125.5f, ok1 = t_hi.y > -125.5f;  // false for -inf and NaN as well
+    // columns that are not ok run on a harmless argument and are zeroed at the end
+    const float2 tc = make_float2(ok0 ? t_hi.x : 0.f, ok1 ? t_hi.y : 0.f);
+    t_lo = make_float2(ok0 ? t_lo.x : 0.f, ok1 ? t_lo.y : 0.f);
+    // j = rint(64 t): adding 1.5 * 2^23 rounds to an integer held in the low mantissa bits
+    const float2 jm = fma2(tc, f2(64.f), f2(12582912.f));
+    const int j0 = __float_as_int(jm.x) - 0x4B400000, j1 = __float_as_int(jm.y) - 0x4B400000;
+    const float2 jf = sub2(jm, f2(12582912.f));
+    const float2 r = add2(fma2(jf, f2(-0.015625f), tc), t_lo);  // |r| <= 1/128 (+ rounding)
+    const float2 y = fma2(r, f2(0.693145751953125f), mul2(r, f2(1.42860682030941723212e-6f)));
+    float2 c = fma2(y, f2(1.0f / 24.0f), f2(1.0f / 6.0f));
+    c = fma2(c, y, f2(0.5f));
+    const float2 em1 = fma2(mul2(c, y), y, y);
+    const float2 T0 = tab[j0 & 63], T1 = tab[j1 & 63];
+    const float2 Tx = make_float2(T0.x, T1.x), Ty = make_float2(T0.y, T1.y);
+    const float2 p = mul2(Tx, em1);
+    const float2 pe = fma2(Tx, em1, make_float2(-p.x, -p.y));
+    const float2 h = add2(Tx, p);
+    float2 lo = sub2(p, sub2(h, Tx));
+    lo = add2(lo, add2(pe, fma2(Ty, em1, Ty)));
+    const float2 sc = make_float2(__int_as_float(((j0 >> 6) + 127) << 23), __int_as_float(((j1 >> 6) + 127) << 23));
+    const float2 vh = mul2(h, sc), vl = mul2(lo, sc);
+    return ff2{make_float2(ok0 ? vh.x : 0.f, ok1 ? vh.y : 0.f), make_float2(ok0 ? vl.x : 0.f, ok1 ? vl.y : 0.f)};
+}
+
+// ------------------------------------------------------------------------------------------------
 // Fast (MUFU) 2^x for the statistics pass: relative error about 2^-22, ex2(-inf) = 0.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -1,4 +1,4 @@
-// Internal interface between the C ABI (sv_api.cu) and the kernels (sv_kernels.cu).
+// Internal interface between the C ABI (sv_api.cu) and the verify kernel (sv_kernels.cu).
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -9,15 +9,18 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;       // threads per CTA of every kernel
-constexpr int kChunk = 8192;        // vocabulary elements per statistics work item
-constexpr int kSub = 512;           // vocabulary elements per sampler sub-chunk (one warp)
-constexpr int kSubPerLane = kSub / 32;
+constexpr int kThreads = 256;               // threads per CTA
+constexpr int kWarps = kThreads / 32;       // independent warp workers per CTA
+constexpr int kAChunk = 4096;               // vocabulary columns of one statistics task (one warp, one row)
+constexpr int kSub = 512;                   // sampler sub-chunk: the finest unit of the inverse-CDF search
+constexpr int kSubPerLane = kSub / 32;      // 16 consecutive columns per lane
+constexpr int kSTask = 2048;                // vocabulary columns of one sampler task (one warp)
+constexpr int kSubPerTask = kSTask / kSub;  // 4
 
 enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2 };
 
-// Partial statistics of one (row, chunk): raw-logit max, sum of 2^((l - m) * K) in fp32,
-// argmax (greedy) and error flags (bit code of sv_status).
+// Partial statistics of one (row, chunk): raw-logit max, sum of 2^((l - m) K) in fp32, first
+// argmax (greedy) and error flags (bit codes of sv_status).
 struct Partial {
     float m;
     float s;
@@ -25,22 +28,24 @@ struct Partial {
     uint32_t flags;
 };
 
-// What the sampler has to draw for one sequence, written by the decision kernel.
-struct SeqTask {
-    int32_t mode;   // kMode*
-    int32_t n;      // emitting slot
-    int32_t prow;   // target row of the draw
-    int32_t qrow;   // draft row of the draw (residual), -1 otherwise
-    float m_p, m_q; // raw-logit row maxima
-    float rho;      // approximate s_p / s_q: selects the tokens with p > q
-    int32_t out_pos;// index into out_tokens of the emitting slot
-    double u;       // uniform of the draw
+// What the sampler draws for one sequence, written by the decision step. 48 bytes, 16-byte
+// aligned: readers fetch it with 16-byte loads.
+struct alignas(16) SeqTask {
+    int32_t mode;    // kMode*
+    int32_t n;       // emitting slot
+    int32_t prow;    // target row of the draw
+    int32_t qrow;    // draft row of the draw (residual), -1 otherwise
+    float m_p, m_q;  // raw-logit row maxima
+    float rho;       // approximate s_p / s_q: selects the tokens with p > q
+    int32_t out_pos; // index into out_tokens of the emitting slot
+    double u;        // uniform of the draw
+    int32_t pad[2];
 };
 
-// Precise sums of one sampler sub-chunk, all relative to the row maxima:
-// a = sum_sel 2^{(l_p - m_p) K}, b = sum_sel 2^{(l_q - m_q) K}, p / q = the same over all tokens.
-struct SubSum {
-    double a, b, p, q;
+// Counters of one call (zeroed before the kernel by the launch sequence).
+struct Counters {
+    uint32_t claim;  // sampler tasks claimed, in sequence order
+    uint32_t pad[31];
 };
 
 struct Params {
@@ -50,7 +55,9 @@ struct Params {
     const int32_t* offs;
     const int32_t* gammas;
     int32_t B, V, max_gamma;
-    int32_t nchunks, nsub;
+    int32_t nchA;      // statistics chunks per row
+    int32_t nsub;      // sampler sub-chunks per row
+    int32_t nS;        // sampler tasks per sequence
     float K_hi, K_lo;  // log2(e) / T as float-float
     double K64;        // log2(e) / T
     double invT64;     // 1 / T
@@ -59,20 +66,28 @@ struct Params {
     int32_t* out_n;
     uint32_t* status;
     sv_debug dbg;
-    Partial* partials;
-    SeqTask* tasks;
-    SubSum* subs;
-    uint32_t* batch_bad;  // written by k_validate each call: nonzero when the CSR offsets are unusable
+    // workspace
+    Partial* partials;  // [B * (2 max_gamma + 1) * nchA]
+    SeqTask* tasks;     // [B]
+    double2* subs;      // [B * nsub]: (sum_sel 2^{(l_p-m_p)K}, sum_sel 2^{(l_q-m_q)K}) per sub-chunk
+    double2* stot;      // [B * nS]: (sum_all p-weight, sum_all q-weight) per sampler task
+    Counters* ctr;
+    uint32_t* a_done;   // [B] statistics tasks finished per sequence
+    uint32_t* s_done;   // [B] sampler tasks finished per sequence
+    uint32_t* seq_ready;  // [B] set (release) once a sequence's sampler task record is written
 };
 
 struct Layout {
-    size_t partials, tasks, subs, status, batch_bad, total;
+    size_t partials, tasks, subs, stot, counters, a_done, s_done, seq_ready, status;
+    size_t zero_begin, zero_end;  // byte range the launch sequence clears
+    size_t total;
 };
 
 Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma);
 
-// Enqueue the whole verify step on `stream`. dtype: SV_F32 / SV_BF16; vec: rows are 16-byte
-// aligned and V * elem_size is a multiple of 16; greedy: temperature == 0.
-cudaError_t launch_verify(const Params& P, int dtype, bool vec, bool greedy, cudaStream_t stream);
+// Enqueue the whole verify step on `stream`: one memset of the counters and one cooperative launch.
+// dtype: SV_F32 / SV_BF16; vec: rows 16-byte aligned and V * elem_size a multiple of 16.
+cudaError_t launch_verify(const Params& P, const Layout& L, void* workspace, int dtype, bool vec, bool greedy,
+                          cudaStream_t stream);
 
 }  // namespace sv

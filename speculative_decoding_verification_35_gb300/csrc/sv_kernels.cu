@@ -1,94 +1,77 @@
-// Kernels of the speculative-sampling verify step (sm_103a).
+// The verify step as one persistent kernel (sm_103a).
 //
-// The step, for each sequence of a CSR-packed batch (velog "6-1편. Speculative Decoding", §2 steps 3-4,
-// §2-1, §2-2; greedy: "All About Transformer Inference", App. D steps 1-3):
-//   k_stats        one pass over every logit the step needs: per (row, vocabulary chunk) the raw
-//                  maximum, sum of exp((l - max) / T) in fp32 and (greedy) the first argmax.
-//                  This pass moves almost all of the HBM traffic.
-//   k_decide       one warp per sequence: merge the chunk partials of each row, evaluate
-//                  u_i * q_i(x_i) < p_i(x_i) for every slot in fp64, find the first rejection with a
-//                  warp ballot, write the accepted tokens and the draw each sequence needs.
-//   k_sample_sums  the draw's weights in float-float precision (residual max(0, p - q) or p), summed
-//                  per 512-token sub-chunk. The rows were streamed moments before (L2-resident).
-//   k_sample_find  one warp per sequence: exact normalisers, inverse CDF over the sub-chunk sums,
-//                  then over the 512 tokens of the crossing sub-chunk, in fp64.
-// Precision: the accept test tolerates fp32 statistics (its decision moves with an error ~1e-7 of
-// p/q); the inverse CDF over ~1e5 tokens does not, so the sampler recomputes its row(s) with a
-// float-float exponential (relative error ~1e-9) and exact normalisers.
+// The method, per sequence of a CSR-packed batch (velog "6-1편. Speculative Decoding", §2 steps 3-4,
+// §2-1 accept/reject rule, §2-2 corrected distribution and sampling; greedy: "All About Transformer
+// Inference", App. D steps 1-3; bonus token: "Accelerating Sonar through speculation",
+// §"Speculative decoding"):
+//   p_i = softmax(l_target_i / T), q_i = softmax(l_draft_i / T); accept x_i while u_i q_i(x_i) < p_i(x_i);
+//   draw the first rejected slot from norm(max(0, p - q)), or a bonus token from p_gamma.
+//
+// Every warp of the grid is an independent worker that repeatedly takes one task:
+//   statistics task (row r, 4096-column chunk c), in sequence-major order, statically strided over the
+//     warps: one streaming pass over the logits (16 x 16-byte loads in flight per lane) computing the
+//     raw max, the fp32 sum of exp((l - max) / T) and, greedy, the first argmax. This pass moves almost
+//     all HBM traffic. The warp that finishes the last statistics task of a sequence runs its decision.
+//   decision (one warp, one sequence): merge the chunk partials of each row, evaluate
+//     u_i * q_i(x_i) < p_i(x_i) in fp64 for every slot, find the first rejection with a ballot, write
+//     the accepted tokens and publish the sequence's sampler work (a per-sequence ready flag).
+//   sampler task (sequence b, 2048 columns), claimed in sequence order in preference to statistics work:
+//     the draw's weights (max(0, p - q), or p for a bonus) in float-float precision, summed per
+//     512-column sub-chunk. The rows were streamed moments earlier, so these reads hit L2. The warp that
+//     finishes the last sampler task of a sequence runs its find.
+//   find (one warp, one sequence): exact normalisers, then the inverse CDF in fp64 over the sub-chunk
+//     sums and over the 512 columns of the crossing sub-chunk.
+// Precision: the accept test tolerates fp32 statistics (its decision moves by ~1e-7 of p/q); the
+// inverse CDF over ~1e5 tokens does not, hence the float-float sampler with exact normalisers.
+// Waits: a warp out of statistics work waits for published sampler work with a bounded spin; the launch
+// is cooperative, so every CTA is resident and every awaited task is held by a running warp.
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
+
+#include <cuda_bf16.h>
 
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
 namespace sv {
 
+constexpr uint32_t kSpinLimit = 1u << 22;  // ~0.5-1 s of short sleeps before a wait gives up
+
 // ------------------------------------------------------------------------------------------------
-// CSR structure checks. A sequence is read only when its own offsets are consistent with the
-// batch total, so no row index can leave [0, R) whatever the offsets hold.
+// Memory-model helpers for data written by other warps during this launch (never through L1's
+// non-coherent path).
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ bool batch_ok(const Params& P) {
-    const int32_t oB = __ldg(P.offs + P.B);
-    return __ldg(P.offs) == 0 && oB >= 0 && (long long)oB <= (long long)P.B * P.max_gamma;
+// Relaxed polling loads (no acquire on every poll: an acquire load discards the SM's L1 contents,
+// which the other warps' cached data and spills would then miss). A poll that succeeds is followed by
+// one fence before the published data is read.
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
-
-__device__ __forceinline__ bool seq_ok(const Params& P, int32_t b, int32_t& g, int32_t& o0) {
-    o0 = __ldg(P.offs + b);
-    const int32_t o1 = __ldg(P.offs + b + 1), oB = __ldg(P.offs + P.B);
-    g = __ldg(P.gammas + b);
-    return o0 >= 0 && o0 <= o1 && o1 <= oB && o1 - o0 == g && g <= P.max_gamma;
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-
-// Statistics rows of a sequence: gamma + 1 target rows, then (sampling) gamma draft rows.
-template <bool GREEDY>
-__device__ __forceinline__ int32_t stat_rows(int32_t g) { return GREEDY ? g + 1 : 2 * g + 1; }
-
-template <bool GREEDY>
-__device__ __forceinline__ int32_t stat_base(const Params& P, int32_t b) {
-    const int32_t o = __ldg(P.offs + b);
-    return GREEDY ? o + b : 2 * o + b;
+__device__ __forceinline__ Partial ld_partial(const Partial* p) {
+    const int4 v = __ldcg((const int4*)p);
+    return Partial{__int_as_float(v.x), __int_as_float(v.y), v.z, (uint32_t)v.w};
 }
-
-// Largest b with stat_base(b) <= r (terminates for any offsets).
-template <bool GREEDY>
-__device__ int32_t find_seq(const Params& P, int32_t r) {
-    int32_t lo = 0, hi = P.B - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (stat_base<GREEDY>(P, mid) <= r) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
+__device__ __forceinline__ SeqTask ld_task(const SeqTask* p) {
+    static_assert(sizeof(SeqTask) == 48 && alignof(SeqTask) == 16, "SeqTask layout");
+    const int4 a = __ldcg((const int4*)p);
+    const int4 c = __ldcg((const int4*)p + 1);
+    const double u = __ldcg((const double*)p + 4);
+    SeqTask t;
+    t.mode = a.x; t.n = a.y; t.prow = a.z; t.qrow = a.w;
+    t.m_p = __int_as_float(c.x); t.m_q = __int_as_float(c.y); t.rho = __int_as_float(c.z); t.out_pos = c.w;
+    t.u = u;
+    return t;
 }
 
 // ------------------------------------------------------------------------------------------------
-// k_validate: the whole CSR structure, before any row is read. One CTA; writes the batch flag every
-// call (no stale state). Inconsistent offsets make row ownership ambiguous, so they fail the batch.
+// Warp reductions
 // ------------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_validate(const Params P) {
-    __shared__ uint32_t s_bad;
-    if (threadIdx.x == 0) s_bad = __ldg(P.offs) != 0;
-    __syncthreads();
-    uint32_t bad = 0;
-    for (int32_t b = threadIdx.x; b < P.B; b += kThreads) {
-        const int32_t o0 = __ldg(P.offs + b), o1 = __ldg(P.offs + b + 1), g = __ldg(P.gammas + b);
-        bad |= !(g >= 0 && g <= P.max_gamma && o0 >= 0 && o1 - o0 == g);
-    }
-    if (bad) atomicOr(&s_bad, 1u);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        *P.batch_bad = s_bad;
-        if (s_bad) atomicOr(P.status, 1u << SV_ERR_BAD_OFFSETS);
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ float logit_at(const void* base, size_t idx) {
-    if (DT == SV_BF16) return __uint_as_float((uint32_t)__ldg((const unsigned short*)base + idx) << 16);
-    return __ldg((const float*)base + idx);
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -109,364 +92,30 @@ __device__ __forceinline__ uint32_t warp_or(uint32_t v) {
     for (int o = 16; o; o >>= 1) v |= __shfl_xor_sync(0xFFFFFFFFu, v, o);
     return v;
 }
-
-// Table of 2^(j/64), j = 0..63, as float-float, built from the fp64 exp2 of the CUDA math library.
-__device__ __forceinline__ void fill_exp2_table(float2* tab) {
-    if (threadIdx.x < 64) {
-        const double v = exp2((double)threadIdx.x * (1.0 / 64.0));
-        const float hi = (float)v;
-        tab[threadIdx.x] = make_float2(hi, (float)(v - (double)hi));
-    }
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
 }
-
-// ------------------------------------------------------------------------------------------------
-// k_stats: per (row, chunk) statistics. 32 elements per thread, 8192 per CTA item.
-// ------------------------------------------------------------------------------------------------
-template <int DT, bool VEC>
-struct Loader {
-    // elements per thread = 32; e(i) is the chunk offset of element i of thread t, increasing in i
-    static constexpr int kPerLoad = VEC ? (DT == SV_BF16 ? 8 : 4) : 1;
-    static constexpr int kLoads = 32 / kPerLoad;
-    __device__ static __forceinline__ int offset(int i, int t) {
-        return ((i / kPerLoad) * kThreads + t) * kPerLoad + (i % kPerLoad);
-    }
-    __device__ static __forceinline__ void load(const void* row, int len, int t, float (&x)[32]) {
-        if (VEC && DT == SV_BF16) {
-            const uint4* p = (const uint4*)row;
+__device__ __forceinline__ int warp_max_i(int v) {
 #pragma unroll
-            for (int q = 0; q < kLoads; ++q) {
-                const int e0 = (q * kThreads + t) * 8;
-                const uint4 v = e0 < len ? ldg_stream(p + q * kThreads + t)
-                                         : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-                x[q * 8 + 0] = bf16lo_to_f32(v.x); x[q * 8 + 1] = bf16hi_to_f32(v.x);
-                x[q * 8 + 2] = bf16lo_to_f32(v.y); x[q * 8 + 3] = bf16hi_to_f32(v.y);
-                x[q * 8 + 4] = bf16lo_to_f32(v.z); x[q * 8 + 5] = bf16hi_to_f32(v.z);
-                x[q * 8 + 6] = bf16lo_to_f32(v.w); x[q * 8 + 7] = bf16hi_to_f32(v.w);
-            }
-        } else if (VEC) {
-            const uint4* p = (const uint4*)row;
-#pragma unroll
-            for (int q = 0; q < kLoads; ++q) {
-                const int e0 = (q * kThreads + t) * 4;
-                const uint4 v = e0 < len ? ldg_stream(p + q * kThreads + t)
-                                         : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
-                x[q * 4 + 0] = __uint_as_float(v.x); x[q * 4 + 1] = __uint_as_float(v.y);
-                x[q * 4 + 2] = __uint_as_float(v.z); x[q * 4 + 3] = __uint_as_float(v.w);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int e = i * kThreads + t;
-                x[i] = e < len ? logit_at<DT>(row, (size_t)e) : -INFINITY;
-            }
-        }
-    }
-};
-
-template <int DT, bool VEC, bool GREEDY>
-__global__ void __launch_bounds__(kThreads) k_stats(const Params P) {
-    __shared__ float s_redf[kThreads / 32];
-    __shared__ int s_redi[kThreads / 32];
-    __shared__ uint32_t s_redu[kThreads / 32];
-    if (*P.batch_bad || !batch_ok(P)) return;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int32_t oB = __ldg(P.offs + P.B);
-    const int32_t total_rows = GREEDY ? oB + P.B : 2 * oB + P.B;
-    const long long items = (long long)total_rows * P.nchunks;
-    const size_t esz = DT == SV_BF16 ? 2 : 4;
-    for (long long w = blockIdx.x; w < items; w += gridDim.x) {
-        const int32_t r = (int32_t)(w / P.nchunks), c = (int32_t)(w % P.nchunks);
-        const int32_t b = find_seq<GREEDY>(P, r);
-        int32_t g, o0;
-        if (!seq_ok(P, b, g, o0)) continue;
-        const int32_t j = r - (GREEDY ? o0 + b : 2 * o0 + b);
-        if (j < 0 || j >= stat_rows<GREEDY>(g)) continue;
-        const size_t row = j <= g ? (size_t)(o0 + b + j) : (size_t)(o0 + j - g - 1);
-        const char* base = (const char*)(j <= g ? P.target : P.draft);
-        const int32_t k0 = c * kChunk;
-        const int len = min(kChunk, P.V - k0);
-        const char* rowp = base + (row * (size_t)P.V + (size_t)k0) * esz;
-
-        float x[32];
-        Loader<DT, VEC>::load(rowp, len, t, x);
-
-        float m = -INFINITY;
-        int arg = 0x7FFFFFFF;
-        uint32_t bad = 0;
-        if (GREEDY) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                bad |= (x[i] != x[i]);
-                if (x[i] > m) { m = x[i]; arg = Loader<DT, VEC>::offset(i, t); }
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) m = fmaxf(m, x[i]);
-        }
-        // block max (and first argmax)
-        float wm = warp_max(m);
-        if (GREEDY) {
-            int a = (m == wm) ? arg : 0x7FFFFFFF;
-#pragma unroll
-            for (int o = 16; o; o >>= 1) a = min(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            bad = warp_or(bad);
-            if (lane == 0) { s_redf[warp] = wm; s_redi[warp] = a; s_redu[warp] = bad; }
-        } else if (lane == 0) {
-            s_redf[warp] = wm;
-        }
-        __syncthreads();
-        float bm = s_redf[0];
-#pragma unroll
-        for (int i = 1; i < kThreads / 32; ++i) bm = fmaxf(bm, s_redf[i]);
-
-        if (GREEDY) {
-            if (t == 0) {
-                int a = 0x7FFFFFFF;
-                uint32_t bb = 0;
-                for (int i = 0; i < kThreads / 32; ++i) {
-                    if (s_redf[i] == bm) a = min(a, s_redi[i]);
-                    bb |= s_redu[i];
-                }
-                uint32_t flags = (bb || bm == INFINITY) ? (1u << SV_ERR_NONFINITE) : 0u;
-                P.partials[(size_t)r * P.nchunks + c] = Partial{bm, 0.f, a == 0x7FFFFFFF ? -1 : k0 + a, flags};
-            }
-        } else {
-            float s = 0.f;
-            if (bm != -INFINITY) {
-                const float K = P.K_hi;
-                const float mK = bm * K;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s += ex2_approx(__fmaf_rn(x[i], K, -mK));
-            } else {
-                // no finite maximum: only a NaN can still hide among the -inf entries
-                bool nan = false;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) nan |= x[i] != x[i];
-                s = nan ? __int_as_float(0x7FC00000) : 0.f;
-            }
-            s = warp_sumf(s);
-            __syncthreads();
-            if (lane == 0) s_redf[warp] = s;
-            __syncthreads();
-            if (t == 0) {
-                float tot = 0.f;
-                for (int i = 0; i < kThreads / 32; ++i) tot += s_redf[i];
-                // a NaN or +inf logit turns the sum into NaN (see the max pass above)
-                const uint32_t flags = (tot != tot) ? (1u << SV_ERR_NONFINITE) : 0u;
-                P.partials[(size_t)r * P.nchunks + c] = Partial{bm, tot, -1, flags};
-            }
-        }
-        __syncthreads();
-    }
+    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
 }
-
-// ------------------------------------------------------------------------------------------------
-// k_decide: one warp per sequence.
-// ------------------------------------------------------------------------------------------------
-template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(kThreads) k_decide(const Params P) {
-    constexpr int kW = kThreads / 32;
-    __shared__ float s_m[kW][2 * SV_MAX_GAMMA + 2];
-    __shared__ double s_s[kW][2 * SV_MAX_GAMMA + 2];
-    __shared__ int s_a[kW][SV_MAX_GAMMA + 1];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t b = blockIdx.x * kW + warp;
-    if (b >= P.B) return;
-
-    if (*P.batch_bad) {  // unusable offsets: every sequence fails, no token position is trusted
-        if (lane == 0) {
-            P.out_n[b] = -1;
-            if (!GREEDY) P.tasks[b].mode = kModeNone;
-        }
-        return;
-    }
-    int32_t g = 0, o0 = 0;
-    const bool bok = batch_ok(P);
-    if (!(bok && seq_ok(P, b, g, o0))) {
-        if (lane == 0) {
-            atomicOr(P.status, 1u << SV_ERR_BAD_OFFSETS);
-            P.out_n[b] = -1;
-            if (!GREEDY) P.tasks[b].mode = kModeNone;
-        }
-        // tokens only where this sequence's slots are provably inside out_tokens
-        const int32_t oB = __ldg(P.offs + P.B), a0 = __ldg(P.offs + b), a1 = __ldg(P.offs + b + 1);
-        if (bok && a0 >= 0 && a0 <= a1 && a1 <= oB)
-            for (int32_t j = lane; j <= a1 - a0; j += 32) P.out_tokens[a0 + b + j] = -1;
-        return;
-    }
-    const int32_t t0 = o0 + b;
-    // draft tokens
-    int32_t x = 0;
-    uint32_t err = 0;
-    if (lane < g) {
-        x = __ldg(P.tokens + o0 + lane);
-        if (x < 0 || x >= P.V) err |= 1u << SV_ERR_BAD_TOKEN;
-    }
-    // merge chunk partials of each statistics row
-    const int nrows = stat_rows<GREEDY>(g);
-    const int32_t sbase = stat_base<GREEDY>(P, b);
-    for (int jr = lane; jr < nrows; jr += 32) {
-        const Partial* pp = P.partials + (size_t)(sbase + jr) * P.nchunks;
-        float m = -INFINITY;
-        int a = -1;
-        uint32_t fl = 0;
-        for (int c = 0; c < P.nchunks; ++c) {
-            const Partial q = pp[c];
-            fl |= q.flags;
-            if (q.m > m) { m = q.m; a = q.arg; }
-        }
-        double s = 0.0;
-        if (m == -INFINITY) {
-            fl |= 1u << SV_ERR_EMPTY_ROW;
-        } else if (!GREEDY) {
-            for (int c = 0; c < P.nchunks; ++c) {
-                const Partial q = pp[c];
-                if (q.m != -INFINITY) s += (double)q.s * exp2(((double)q.m - (double)m) * P.K64);
-            }
-        }
-        err |= fl;
-        s_m[warp][jr] = m;
-        s_s[warp][jr] = s;
-        if (GREEDY) s_a[warp][jr] = a;
-    }
-    err = warp_or(err);
-    __syncwarp();
-    if (err) {
-        if (lane == 0) {
-            atomicOr(P.status, err);
-            P.out_n[b] = -1;
-            if (!GREEDY) P.tasks[b].mode = kModeNone;
-        }
-        for (int32_t j = lane; j <= g; j += 32) P.out_tokens[t0 + j] = -1;
-        return;
-    }
-
-    if (GREEDY) {
-        const int a = lane <= g ? s_a[warp][lane] : -1;
-        if (lane <= g && P.dbg.row_argmax) P.dbg.row_argmax[t0 + lane] = a;
-        const uint32_t mism = __ballot_sync(0xFFFFFFFFu, lane < g && x != a);
-        const int n = mism ? __ffs(mism) - 1 : g;
-        if (lane <= g) P.out_tokens[t0 + lane] = lane < n ? x : (lane == n ? a : -1);
-        if (lane == 0) P.out_n[b] = n;
-        return;
-    }
-
-    // sampling: accept test of every slot in fp64 (u * q(x) < p(x), p/q from exact logits)
-    bool acc = true;
-    if (lane < g) {
-        const double lt = (double)logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
-        const double ld = (double)logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
-        const double px = exp2((lt - (double)s_m[warp][lane]) * P.K64) / s_s[warp][lane];
-        const double qx = exp2((ld - (double)s_m[warp][g + 1 + lane]) * P.K64) / s_s[warp][g + 1 + lane];
-        const double u = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);
-        acc = u * qx < px;
-        if (P.dbg.p_x) P.dbg.p_x[o0 + lane] = px;
-        if (P.dbg.q_x) P.dbg.q_x[o0 + lane] = qx;
-    }
-    if (P.dbg.row_lse) {
-        const int32_t R_t = __ldg(P.offs + P.B) + P.B;
-        for (int jr = lane; jr < nrows; jr += 32) {
-            const double lse = (double)s_m[warp][jr] * P.invT64 + log(s_s[warp][jr]);
-            const int32_t row = jr <= g ? t0 + jr : R_t + o0 + (jr - g - 1);
-            P.dbg.row_lse[row] = lse;
-        }
-    }
-    const uint32_t rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
-    const int n = rej ? __ffs(rej) - 1 : g;
-    if (lane <= g && lane != n) P.out_tokens[t0 + lane] = lane < n ? x : -1;
-    if (lane == 0) {
-        SeqTask tk;
-        tk.mode = n < g ? kModeResidual : kModeBonus;
-        tk.n = n;
-        tk.prow = t0 + n;
-        tk.qrow = n < g ? o0 + n : -1;
-        tk.m_p = s_m[warp][n];
-        tk.m_q = n < g ? s_m[warp][g + 1 + n] : 0.f;
-        tk.rho = n < g ? (float)(s_s[warp][n] / s_s[warp][g + 1 + n]) : 1.f;
-        tk.out_pos = t0 + n;
-        tk.u = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)n, 1);
-        P.tasks[b] = tk;
-        P.out_n[b] = n;
-    }
-}
-
-// ------------------------------------------------------------------------------------------------
-// Sampler: weights of the draw in float-float.
-// ------------------------------------------------------------------------------------------------
-// Load the 16 logits k0 .. k0 + 15 of `row` (-inf past V).
-template <int DT, bool VEC>
-__device__ __forceinline__ void load16(const void* base, size_t row, int32_t V, int32_t k0, float (&x)[16]) {
-    const size_t off = row * (size_t)V + (size_t)k0;
-    if (VEC && k0 + 16 <= V) {
-        if (DT == SV_BF16) {
-            const uint4* p = (const uint4*)((const unsigned short*)base + off);
-            const uint4 a = __ldg(p), c = __ldg(p + 1);
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+// float-float butterfly: every lane ends with the same total (the pairwise steps are symmetric)
+__device__ __forceinline__ double warp_sum_ff(ffacc a) {
+    float hi = a.hi, lo = a.lo;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) { x[2 * i] = bf16lo_to_f32(w[i]); x[2 * i + 1] = bf16hi_to_f32(w[i]); }
-        } else {
-            const float4* p = (const float4*)((const float*)base + off);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 v = __ldg(p + i);
-                x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[i] = k0 + i < V ? logit_at<DT>(base, off + i) : -INFINITY;
+    for (int o = 16; o; o >>= 1) {
+        const float oh = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+        const float ol = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+        float s, e;
+        two_sum(hi, oh, s, e);
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, ol), e);
     }
+    return (double)hi + (double)lo;
 }
-
-// 2^((l - m) K) as float-float, the subtraction made exact first.
-__device__ __forceinline__ ff weight_ff(float l, float m, float K_hi, float K_lo, const float2* tab) {
-    float dh, dl;
-    two_sum(l, -m, dh, dl);
-    return exp2_ff(dh, dl, K_hi, K_lo, tab);
-}
-
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) k_sample_sums(const Params P) {
-    __shared__ float2 tab[64];
-    fill_exp2_table(tab);
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const long long items = (long long)P.B * P.nsub;
-    for (long long w = (long long)blockIdx.x * (kThreads / 32) + warp; w < items;
-         w += (long long)gridDim.x * (kThreads / 32)) {
-        const int32_t b = (int32_t)(w / P.nsub), sc = (int32_t)(w % P.nsub);
-        const SeqTask tk = P.tasks[b];
-        if (tk.mode == kModeNone) continue;
-        const bool resid = tk.mode == kModeResidual;
-        const int32_t k0 = sc * kSub + lane * kSubPerLane;
-        float lp[16], lq[16];
-        load16<DT, VEC>(P.target, (size_t)tk.prow, P.V, k0, lp);
-        if (resid) load16<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, k0, lq);
-        ffacc A, Bq, Pp, Qq;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const ff ep = weight_ff(lp[e], tk.m_p, P.K_hi, P.K_lo, tab);
-            Pp.add(ep.hi, ep.lo);
-            if (resid) {
-                const ff eq = weight_ff(lq[e], tk.m_q, P.K_hi, P.K_lo, tab);
-                Qq.add(eq.hi, eq.lo);
-                if (ep.hi > tk.rho * eq.hi) {
-                    A.add(ep.hi, ep.lo);
-                    Bq.add(eq.hi, eq.lo);
-                }
-            }
-        }
-        const double sp = warp_sumd(Pp.value());
-        double sa = sp, sb = 0.0, sq = 0.0;
-        if (resid) {
-            sa = warp_sumd(A.value());
-            sb = warp_sumd(Bq.value());
-            sq = warp_sumd(Qq.value());
-        }
-        if (lane == 0) P.subs[(size_t)b * P.nsub + sc] = SubSum{sa, sb, sp, sq};
-    }
-}
-
 // Exclusive prefix over the warp (fp64).
 __device__ __forceinline__ double warp_exscan(double v, int lane) {
     double incl = v;
@@ -478,116 +127,562 @@ __device__ __forceinline__ double warp_exscan(double v, int lane) {
     return incl - v;
 }
 
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) k_sample_find(const Params P) {
-    __shared__ float2 tab[64];
-    fill_exp2_table(tab);
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t b = blockIdx.x * (kThreads / 32) + warp;
-    if (b >= P.B) return;
-    const SeqTask tk = P.tasks[b];
-    if (tk.mode == kModeNone) return;
-    const SubSum* ss = P.subs + (size_t)b * P.nsub;
-    const int nsub = P.nsub;
+// ------------------------------------------------------------------------------------------------
+// CSR helpers (the offsets are validated by every CTA before any row is read).
+// ------------------------------------------------------------------------------------------------
+template <bool GREEDY>
+__device__ __forceinline__ int32_t stat_rows(int32_t g) { return GREEDY ? g + 1 : 2 * g + 1; }
 
+template <bool GREEDY>
+__device__ __forceinline__ int32_t stat_base(const Params& P, int32_t b) {
+    const int32_t o = __ldg(P.offs + b);
+    return GREEDY ? o + b : 2 * o + b;
+}
+
+// Largest b with stat_base(b) <= r.
+template <bool GREEDY>
+__device__ int32_t find_seq(const Params& P, int32_t r) {
+    int32_t lo = 0, hi = P.B - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (stat_base<GREEDY>(P, mid) <= r) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int DT>
+__device__ __forceinline__ float logit_at(const void* base, size_t idx) {
+    if (DT == SV_BF16) return __uint_as_float((uint32_t)__ldg((const unsigned short*)base + idx) << 16);
+    return __ldg((const float*)base + idx);
+}
+
+// Table of 2^(j/64), j = 0..63, as float-float, from the fp64 exp2 of the CUDA math library.
+__device__ __forceinline__ void fill_exp2_table(float2* tab) {
+    if (threadIdx.x < 64) {
+        const double v = exp2((double)threadIdx.x * (1.0 / 64.0));
+        const float hi = (float)v;
+        tab[threadIdx.x] = make_float2(hi, (float)(v - (double)hi));
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Statistics of one row segment [0, len) of up to 4096 columns, one warp. Result on every lane:
+// m (raw max), s (sum of 2^((l - m) K), fp32; NaN when a NaN or +inf logit was seen), arg (first
+// argmax, greedy), bad (greedy: NaN or +inf seen).
+// ------------------------------------------------------------------------------------------------
+struct SegStats {
+    float m, s;
+    int arg;
+    uint32_t bad;
+};
+
+// Merge two partial (m, s) pairs of the same row (online softmax rescaling in fp32).
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float K) {
+    const float M = fmaxf(m, m2);
+    if (M == -INFINITY) return;
+    s = (m == -INFINITY ? 0.f : s * ex2_approx((m - M) * K)) + (m2 == -INFINITY ? 0.f : s2 * ex2_approx((m2 - M) * K));
+    m = M;
+}
+
+template <int DT, bool VEC, bool GREEDY>
+__device__ __forceinline__ SegStats seg_stats(const char* rowp, int len, int lane, float K) {
+    SegStats r{-INFINITY, 0.f, 0x7FFFFFFF, 0u};
+    if (VEC && DT == SV_BF16) {
+        // 4096 columns: 16 loads of 8 bf16 per lane, all in flight before any arithmetic
+        uint4 v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int e0 = (q * 32 + lane) * 8;
+            v[q] = e0 < len ? ldg_stream((const uint4*)rowp + q * 32 + lane)
+                            : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        }
+        if (GREEDY) {
+            float m = -INFINITY;
+            int a = 0x7FFFFFFF;
+            uint32_t bad = 0;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    const float x = (h & 1) ? bf16hi_to_f32(w[h >> 1]) : bf16lo_to_f32(w[h >> 1]);
+                    bad |= x != x;
+                    if (x > m) { m = x; a = (q * 32 + lane) * 8 + h; }
+                }
+            }
+            const float M = warp_max(m);
+            r.arg = warp_min_i(m == M ? a : 0x7FFFFFFF);
+            r.m = M;
+            r.bad = warp_or(bad) | (M == INFINITY);
+        } else {
+            __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].x));
+                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].y));
+                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].z));
+                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].w));
+            }
+            const float m = warp_max(fmaxf(__low2float(mx), __high2float(mx)));
+            float s = 0.f;
+            if (m != -INFINITY) {
+                const float2 K2 = make_float2(K, K);
+                const float2 nmK2 = make_float2(-m * K, -m * K);
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float2 x = make_float2(bf16lo_to_f32(w[h]), bf16hi_to_f32(w[h]));
+                        const float2 t = __ffma2_rn(x, K2, nmK2);
+                        acc = __fadd2_rn(acc, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                    }
+                }
+                s = acc.x + acc.y;
+            } else {
+                // no finite maximum: only a NaN can still hide among -inf entries
+                uint32_t nan = 0;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+                        nan |= ((w[h] & 0x7F80u) == 0x7F80u && (w[h] & 0x7Fu)) ||
+                               ((w[h] & 0x7F800000u) == 0x7F800000u && (w[h] & 0x7F0000u));
+                }
+                s = nan ? __int_as_float(0x7FC00000) : 0.f;
+            }
+            r.m = m;
+            r.s = warp_sumf(s);  // a NaN or +inf logit makes this NaN (flagged by the caller)
+        }
+        return r;
+    }
+    // fp32 rows (vectorised) and unaligned rows (scalar): 64 columns per lane per pass, merged online
+    constexpr int kPerLane = 64;
+    for (int base = 0; base < len; base += 32 * kPerLane) {
+        float x[kPerLane];
+        if (VEC) {
+#pragma unroll
+            for (int q = 0; q < kPerLane / 4; ++q) {
+                const int e0 = base + (q * 32 + lane) * 4;
+                const uint4 v = e0 < len ? ldg_stream((const uint4*)(rowp + (size_t)base * 4) + q * 32 + lane)
+                                         : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+                x[q * 4 + 0] = __uint_as_float(v.x); x[q * 4 + 1] = __uint_as_float(v.y);
+                x[q * 4 + 2] = __uint_as_float(v.z); x[q * 4 + 3] = __uint_as_float(v.w);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) {
+                const int e = base + i * 32 + lane;
+                x[i] = e < len ? logit_at<DT>(rowp, (size_t)e) : -INFINITY;
+            }
+        }
+        float m = -INFINITY;
+        int a = 0x7FFFFFFF;
+        uint32_t bad = 0;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            if (GREEDY) {
+                bad |= x[i] != x[i];
+                const int col = VEC ? base + ((i / 4) * 32 + lane) * 4 + (i % 4) : base + i * 32 + lane;
+                if (x[i] > m) { m = x[i]; a = col; }
+            } else {
+                m = fmaxf(m, x[i]);
+            }
+        }
+        const float M = warp_max(m);
+        if (GREEDY) {
+            const int A = warp_min_i(m == M ? a : 0x7FFFFFFF);
+            bad = warp_or(bad) | (M == INFINITY);
+            if (M > r.m) { r.m = M; r.arg = A; }
+            r.bad |= bad;
+        } else {
+            float s = 0.f;
+            if (M != -INFINITY) {
+                const float nmK = -M * K;
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i) s += ex2_approx(__fmaf_rn(x[i], K, nmK));
+            } else {
+                bool nan = false;
+#pragma unroll
+                for (int i = 0; i < kPerLane; ++i) nan |= x[i] != x[i];
+                s = nan ? __int_as_float(0x7FC00000) : 0.f;
+            }
+            s = warp_sumf(s);
+            if (s != s) {
+                r.s = s;
+                r.m = fmaxf(r.m, M);
+            } else if (r.s == r.s) {
+                merge_ms(r.m, r.s, M, s, K);
+            }
+        }
+    }
+    return r;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Decision for sequence b (one warp): merge partials, accept tests, first rejection, outputs.
+// ------------------------------------------------------------------------------------------------
+template <int DT, bool GREEDY>
+__device__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float2* tab) {
+    const int32_t t0 = o0 + b;
+    const int nrows = stat_rows<GREEDY>(g);
+    const int32_t sbase = stat_base<GREEDY>(P, b);
+    const int nch = P.nchA;
+    const float K = P.K_hi;
+    float my_m[2] = {-INFINITY, -INFINITY};
+    float my_s[2] = {0.f, 0.f};
+    int my_a[2] = {-1, -1};
+    uint32_t err = 0;
+    for (int j0 = 0; j0 < nrows; j0 += 8) {
+        // lanes over chunks, 8 rows per batch with their loads in flight together
+        float lm[8], ls[8];
+        int la[8];
+        uint32_t lf[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { lm[k] = -INFINITY; ls[k] = 0.f; la[k] = 0x7FFFFFFF; lf[k] = 0u; }
+        for (int c = lane; c < nch; c += 32) {
+            Partial q[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (j0 + k < nrows) q[k] = ld_partial(P.partials + (size_t)(sbase + j0 + k) * nch + c);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (j0 + k >= nrows) continue;
+                lf[k] |= q[k].flags;
+                if (GREEDY) {
+                    if (q[k].m > lm[k]) { lm[k] = q[k].m; la[k] = q[k].arg; }
+                } else if (q[k].s != q[k].s) {
+                    ls[k] = q[k].s;
+                    lm[k] = fmaxf(lm[k], q[k].m);
+                } else if (ls[k] == ls[k]) {
+                    merge_ms(lm[k], ls[k], q[k].m, q[k].s, K);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int jr = j0 + k;
+            if (jr >= nrows) break;
+            const float M = warp_max(lm[k]);
+            float v = 0.f;
+            int a = 0x7FFFFFFF;
+            if (GREEDY) {
+                a = warp_min_i(lm[k] == M ? la[k] : 0x7FFFFFFF);
+            } else {
+                v = ls[k] != ls[k] ? ls[k] : (lm[k] == -INFINITY ? 0.f : ls[k] * ex2_approx((lm[k] - M) * K));
+                v = warp_sumf(v);
+            }
+            // a row with a NaN or +inf is reported as such, not as empty (both fail the sequence)
+            const uint32_t rf = warp_or(lf[k]) | (v != v ? 1u << SV_ERR_NONFINITE : 0u);
+            err |= rf;
+            if (M == -INFINITY && !rf) err |= 1u << SV_ERR_EMPTY_ROW;
+            if (lane == (jr & 31)) {
+                my_m[jr >> 5] = M;
+                my_s[jr >> 5] = v;
+                my_a[jr >> 5] = a;
+            }
+        }
+    }
+    int32_t x = 0;
+    if (lane < g) {
+        x = __ldg(P.tokens + o0 + lane);
+        if (x < 0 || x >= P.V) err |= 1u << SV_ERR_BAD_TOKEN;
+    }
+    err = warp_or(err);
+    if (err) {
+        if (lane == 0) {
+            atomicOr(P.status, err);
+            P.out_n[b] = -1;
+            if (!GREEDY) {
+                SeqTask tk{};
+                tk.mode = kModeNone;
+                P.tasks[b] = tk;
+            }
+        }
+        for (int32_t j = lane; j <= g; j += 32) P.out_tokens[t0 + j] = -1;
+        return;
+    }
+    if (GREEDY) {
+        const int a = my_a[0];  // argmax of target row `lane` (lane <= g <= 31)
+        if (lane <= g && P.dbg.row_argmax) P.dbg.row_argmax[t0 + lane] = a;
+        const uint32_t mism = __ballot_sync(0xFFFFFFFFu, lane < g && x != a);
+        const int n = mism ? __ffs(mism) - 1 : g;
+        if (lane <= g) P.out_tokens[t0 + lane] = lane < n ? x : (lane == n ? a : -1);
+        if (lane == 0) P.out_n[b] = n;
+        return;
+    }
+    // the draft row of slot `lane` is statistics row g + 1 + lane: lane (g+1+lane) & 31, register >> 5
+    const int jd = g + 1 + lane;
+    const float dm0 = __shfl_sync(0xFFFFFFFFu, my_m[0], jd & 31), dm1 = __shfl_sync(0xFFFFFFFFu, my_m[1], jd & 31);
+    const float ds0 = __shfl_sync(0xFFFFFFFFu, my_s[0], jd & 31), ds1 = __shfl_sync(0xFFFFFFFFu, my_s[1], jd & 31);
+    const float dm = (jd >> 5) ? dm1 : dm0, ds = (jd >> 5) ? ds1 : ds0;
+    bool acc = true;
+    if (lane < g) {
+        // p(x) and q(x) from the precise exponential of the exact logit gaps, over the fp32 normalisers
+        const float lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
+        const float ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
+        const ff2 e = exp2_ff2(make_float2(lt, ld), make_float2(my_m[0], dm), P.K_hi, P.K_lo, tab);
+        const float px = __fdiv_rn(e.hi.x + e.lo.x, my_s[0]);
+        const float qx = __fdiv_rn(e.hi.y + e.lo.y, ds);
+        const float u = (float)philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);  // exact
+        acc = u * qx < px;
+        if (P.dbg.p_x) P.dbg.p_x[o0 + lane] = (double)px;
+        if (P.dbg.q_x) P.dbg.q_x[o0 + lane] = (double)qx;
+    }
+    if (P.dbg.row_lse) {
+        const int32_t R_t = __ldg(P.offs + P.B) + P.B;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int jr = lane + 32 * h;
+            if (jr < nrows) {
+                const double lse = (double)my_m[h] * P.invT64 + log((double)my_s[h]);
+                P.dbg.row_lse[jr <= g ? t0 + jr : R_t + o0 + (jr - g - 1)] = lse;
+            }
+        }
+    }
+    const uint32_t rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
+    const int n = rej ? __ffs(rej) - 1 : g;
+    if (lane <= g && lane != n) P.out_tokens[t0 + lane] = lane < n ? x : -1;
+    // statistics of the emitting slot's rows
+    const float pm = __shfl_sync(0xFFFFFFFFu, my_m[0], n), ps = __shfl_sync(0xFFFFFFFFu, my_s[0], n);
+    const float qm = __shfl_sync(0xFFFFFFFFu, dm, n), qs = __shfl_sync(0xFFFFFFFFu, ds, n);
+    if (lane == 0) {
+        SeqTask tk;
+        tk.mode = n < g ? kModeResidual : kModeBonus;
+        tk.n = n;
+        tk.prow = t0 + n;
+        tk.qrow = n < g ? o0 + n : -1;
+        tk.m_p = pm;
+        tk.m_q = n < g ? qm : 0.f;
+        tk.rho = n < g ? (float)((double)ps / (double)qs) : 1.f;
+        tk.out_pos = t0 + n;
+        tk.u = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)n, 1);
+        P.tasks[b] = tk;
+        P.out_n[b] = n;
+    }
+}
+
+// Publish sequence b's sampler work: lane 0 wrote the task record, and its release store orders that
+// write before the flag.
+__device__ __forceinline__ void publish(const Params& P, int32_t b, int lane) {
+    if (lane == 0) st_release(P.seq_ready + b, 1u);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Sampler weights
+// ------------------------------------------------------------------------------------------------
+// 16 consecutive columns k0 .. k0 + 15 of `row`, kept packed (bf16: 8 words; fp32: 16 words); -inf
+// past V.
+struct Cols16 {
+    uint32_t w[16];
+};
+
+template <int DT, bool VEC>
+__device__ __forceinline__ Cols16 load_cols16(const void* base, size_t row, int32_t V, int32_t k0) {
+    Cols16 c;
+    const size_t off = row * (size_t)V + (size_t)k0;
+    if (VEC && k0 + 16 <= V) {
+        if (DT == SV_BF16) {
+            const uint4* p = (const uint4*)((const unsigned short*)base + off);
+            const uint4 a = __ldg(p), d = __ldg(p + 1);
+            c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+            c.w[4] = d.x; c.w[5] = d.y; c.w[6] = d.z; c.w[7] = d.w;
+        } else {
+            const uint4* p = (const uint4*)((const float*)base + off);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = __ldg(p + i);
+                c.w[4 * i] = v.x; c.w[4 * i + 1] = v.y; c.w[4 * i + 2] = v.z; c.w[4 * i + 3] = v.w;
+            }
+        }
+    } else if (DT == SV_BF16) {
+        const unsigned short* p = (const unsigned short*)base + off;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = k0 + 2 * i < V ? __ldg(p + 2 * i) : 0xFF80u;
+            const uint32_t hi = k0 + 2 * i + 1 < V ? __ldg(p + 2 * i + 1) : 0xFF80u;
+            c.w[i] = lo | (hi << 16);
+        }
+    } else {
+        const float* p = (const float*)base + off;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) c.w[i] = k0 + i < V ? __float_as_uint(__ldg(p + i)) : 0xFF800000u;
+    }
+    return c;
+}
+
+template <int DT>
+__device__ __forceinline__ float col(const Cols16& c, int e) {
+    if (DT == SV_BF16) return (e & 1) ? bf16hi_to_f32(c.w[e >> 1]) : bf16lo_to_f32(c.w[e >> 1]);
+    return __uint_as_float(c.w[e]);
+}
+
+// columns 2e and 2e + 1 as a float2
+template <int DT>
+__device__ __forceinline__ float2 col2(const Cols16& c, int e) {
+    if (DT == SV_BF16) return make_float2(bf16lo_to_f32(c.w[e]), bf16hi_to_f32(c.w[e]));
+    return make_float2(__uint_as_float(c.w[2 * e]), __uint_as_float(c.w[2 * e + 1]));
+}
+
+// Residual selection of two columns: p > q, judged on the approximate normaliser ratio rho. The same
+// rule (same float operations) is applied by every step that sums or scans the residual.
+__device__ __forceinline__ float2 sel_mask(const ff2& ep, const ff2& eq, float rho) {
+    return make_float2(ep.hi.x > rho * eq.hi.x ? 1.f : 0.f, ep.hi.y > rho * eq.hi.y ? 1.f : 0.f);
+}
+
+// Inverse-CDF search over the columns [k_lo, k_hi) for the remaining target `rem`, in blocks of 512
+// columns with fp64 running sums. Returns the token, or the last column of positive weight when the
+// crossing is lost to rounding (or `tail_rule` asks for exactly that).
+template <int DT, bool VEC>
+__device__ int32_t scan_elements(const Params& P, const SeqTask& tk, bool resid, double rho, int32_t k_lo,
+                                 int32_t k_hi, double rem, bool tail_rule, const float2* tab, int lane) {
+    int32_t last_pos = -1;
+    for (int32_t base = k_lo; base < k_hi; base += kSub) {
+        const int32_t k0 = base + lane * kSubPerLane;
+        const Cols16 cp = load_cols16<DT, VEC>(P.target, (size_t)tk.prow, P.V, k0);
+        Cols16 cq;
+        if (resid) cq = load_cols16<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, k0);
+        double w[16];
+        double tot = 0.0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const ff2 ep = exp2_ff2(col2<DT>(cp, e), f2(tk.m_p), P.K_hi, P.K_lo, tab);
+            double w0 = (double)ep.hi.x + (double)ep.lo.x, w1 = (double)ep.hi.y + (double)ep.lo.y;
+            if (resid) {
+                const ff2 eq = exp2_ff2(col2<DT>(cq, e), f2(tk.m_q), P.K_hi, P.K_lo, tab);
+                const float2 mk = sel_mask(ep, eq, tk.rho);
+                w0 = mk.x != 0.f ? fmax(0.0, w0 - rho * ((double)eq.hi.x + (double)eq.lo.x)) : 0.0;
+                w1 = mk.y != 0.f ? fmax(0.0, w1 - rho * ((double)eq.hi.y + (double)eq.lo.y)) : 0.0;
+            }
+            if (k0 + 2 * e >= k_hi) w0 = 0.0;
+            if (k0 + 2 * e + 1 >= k_hi) w1 = 0.0;
+            w[2 * e] = w0;
+            w[2 * e + 1] = w1;
+            tot += w0 + w1;
+        }
+        int lastp = -1;
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            if (w[e] > 0.0) lastp = k0 + e;
+        lastp = warp_max_i(lastp);
+        if (lastp >= 0) last_pos = lastp;
+        const double lpre = warp_exscan(tot, lane);
+        const double btot = __shfl_sync(0xFFFFFFFFu, lpre + tot, 31);
+        if (!tail_rule && btot > rem) {
+            int my_k = -1;
+            if (lpre + tot > rem) {
+                double c = lpre;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    if (my_k < 0 && w[e] > 0.0 && c + w[e] > rem) my_k = k0 + e;
+                    c += w[e];
+                }
+            }
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, my_k >= 0);
+            if (hit) return __shfl_sync(0xFFFFFFFFu, my_k, __ffs(hit) - 1);
+            return last_pos;
+        }
+        rem -= btot;
+    }
+    return last_pos;
+}
+
+// Find for sequence b (one warp): normalisers, sub-chunk search, element search, output.
+template <int DT, bool VEC>
+__device__ void find(const Params& P, int32_t b, const float2* tab, int lane) {
+    const SeqTask tk = ld_task(P.tasks + b);
+    if (tk.mode == kModeNone) return;
+    const double2* ss = P.subs + (size_t)b * P.nsub;
+    const double2* st = P.stot + (size_t)b * P.nS;
+    const int nsub = P.nsub, nS = P.nS;
     double sp = 0.0, sq = 0.0;
-    for (int i = lane; i < nsub; i += 32) { sp += ss[i].p; sq += ss[i].q; }
+    for (int i = lane; i < nS; i += 32) {
+        const double2 v = __ldcg(st + i);
+        sp += v.x;
+        sq += v.y;
+    }
     sp = warp_sumd(sp);
     sq = warp_sumd(sq);
     bool resid = tk.mode == kModeResidual;
     const double rho = resid ? sp / sq : 0.0;
 
-    // sub-chunk weights: lane owns the contiguous range [s0, s1)
-    const int per = (nsub + 31) / 32;
-    const int s0 = min(nsub, lane * per), s1 = min(nsub, s0 + per);
-    auto wsub = [&](int i, bool r) -> double { return r ? ss[i].a - rho * ss[i].b : ss[i].p; };
-    double lsum = 0.0;
-    for (int i = s0; i < s1; ++i) lsum += wsub(i, resid);
+    // level 1: units (sub-chunks, or sampler tasks for the p-only fallback); lane owns [s0, s1)
+    int units = nsub;
+    bool by_task = false;
+    auto unit_w = [&](int i) -> double {
+        if (by_task) return __ldcg(st + i).x;
+        const double2 v = __ldcg(ss + i);
+        return resid ? v.x - rho * v.y : v.x;
+    };
+    // the loads of a lane's range are issued 8 at a time, not one dependent round trip each
+    auto range_sum = [&](int s0, int s1) -> double {
+        double sum = 0.0;
+        for (int i0 = s0; i0 < s1; i0 += 8) {
+            double v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = i0 + k < s1 ? unit_w(i0 + k) : 0.0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sum += v[k];
+        }
+        return sum;
+    };
+    int per = (units + 31) / 32;
+    int s0 = min(units, lane * per), s1 = min(units, s0 + per);
+    double lsum = range_sum(s0, s1);
     double S = warp_sumd(lsum);
     if (resid && !(S > 0.0)) {  // residual mass 0 (only through rounding): draw from p
         resid = false;
-        lsum = 0.0;
-        for (int i = s0; i < s1; ++i) lsum += wsub(i, false);
+        by_task = true;
+        units = nS;
+        per = (units + 31) / 32;
+        s0 = min(units, lane * per);
+        s1 = min(units, s0 + per);
+        lsum = range_sum(s0, s1);
         S = warp_sumd(lsum);
     }
     const double target = tk.u * S;
-
-    // sub-chunk holding the crossing
     const double pre = warp_exscan(lsum, lane);
-    int sc = -1;
+    int unit = -1;
     double before = 0.0;
     {
-        int my_sc = -1;
+        int my_u = -1;
         double my_before = 0.0;
         if (pre + lsum > target) {
             double c = pre;
-            for (int i = s0; i < s1; ++i) {
-                const double wi = wsub(i, resid);
-                if (wi > 0.0 && c + wi > target) { my_sc = i; my_before = c; break; }
-                c += wi;
+            for (int i0 = s0; i0 < s1 && my_u < 0; i0 += 8) {
+                double v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = i0 + k < s1 ? unit_w(i0 + k) : 0.0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (my_u < 0 && v[k] > 0.0 && c + v[k] > target) { my_u = i0 + k; my_before = c; }
+                    c += v[k];
+                }
             }
         }
-        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, my_sc >= 0);
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, my_u >= 0);
         if (hit) {
             const int L = __ffs(hit) - 1;
-            sc = __shfl_sync(0xFFFFFFFFu, my_sc, L);
+            unit = __shfl_sync(0xFFFFFFFFu, my_u, L);
             before = __shfl_sync(0xFFFFFFFFu, my_before, L);
         }
     }
     bool tail_rule = false;
-    if (sc < 0) {  // rounding left no crossing: the last sub-chunk with positive weight
+    if (unit < 0) {  // rounding left no crossing: the last unit with positive weight
         int last = -1;
         for (int i = s0; i < s1; ++i)
-            if (wsub(i, resid) > 0.0) last = i;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, o));
-        sc = last;
+            if (unit_w(i) > 0.0) last = i;
+        unit = warp_max_i(last);
         tail_rule = true;
     }
-
     int32_t token = -1;
-    if (sc >= 0) {
-        const int32_t k0 = sc * kSub + lane * kSubPerLane;
-        float lp[16], lq[16];
-        load16<DT, VEC>(P.target, (size_t)tk.prow, P.V, k0, lp);
-        if (resid) load16<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, k0, lq);
-        double w[16];
-        double tot = 0.0;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const ff ep = weight_ff(lp[e], tk.m_p, P.K_hi, P.K_lo, tab);
-            double we = (double)ep.hi + (double)ep.lo;
-            if (resid) {
-                const ff eq = weight_ff(lq[e], tk.m_q, P.K_hi, P.K_lo, tab);
-                we = (ep.hi > tk.rho * eq.hi) ? fmax(0.0, we - rho * ((double)eq.hi + (double)eq.lo)) : 0.0;
-            }
-            w[e] = we;
-            tot += we;
-        }
-        const double rem = target - before;
-        const double lpre = warp_exscan(tot, lane);
-        int my_k = -1;
-        if (!tail_rule && lpre + tot > rem) {
-            double c = lpre;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                if (my_k < 0 && w[e] > 0.0 && c + w[e] > rem) my_k = k0 + e;
-                c += w[e];
-            }
-        }
-        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, my_k >= 0);
-        if (hit) {
-            token = __shfl_sync(0xFFFFFFFFu, my_k, __ffs(hit) - 1);
-        } else {  // no crossing inside (rounding): the last positive weight of the sub-chunk
-            int last = -1;
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (w[e] > 0.0) last = k0 + e;
-#pragma unroll
-            for (int o = 16; o; o >>= 1) last = max(last, __shfl_xor_sync(0xFFFFFFFFu, last, o));
-            token = last;
-        }
+    if (unit >= 0) {
+        const int32_t span = by_task ? kSTask : kSub;
+        const int32_t k_lo = unit * span, k_hi = min(P.V, k_lo + span);
+        token = scan_elements<DT, VEC>(P, tk, resid, rho, k_lo, k_hi, target - before, tail_rule, tab, lane);
     }
     if (lane == 0) {
         P.out_tokens[tk.out_pos] = token;
@@ -595,63 +690,279 @@ __global__ void __launch_bounds__(kThreads) k_sample_find(const Params P) {
     }
 }
 
+// 8 consecutive columns k0 .. k0 + 7 of `row`, packed (bf16: 4 words; fp32: 8 words); -inf past V.
+struct Cols8 {
+    uint32_t w[8];
+};
+
+template <int DT, bool VEC>
+__device__ __forceinline__ Cols8 load_cols8(const void* base, size_t row, int32_t V, int32_t k0) {
+    Cols8 c;
+    const size_t off = row * (size_t)V + (size_t)k0;
+    if (VEC && k0 + 8 <= V) {
+        if (DT == SV_BF16) {
+            const uint4 a = __ldg((const uint4*)((const unsigned short*)base + off));
+            c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+        } else {
+            const uint4* q = (const uint4*)((const float*)base + off);
+            const uint4 a = __ldg(q), d = __ldg(q + 1);
+            c.w[0] = a.x; c.w[1] = a.y; c.w[2] = a.z; c.w[3] = a.w;
+            c.w[4] = d.x; c.w[5] = d.y; c.w[6] = d.z; c.w[7] = d.w;
+        }
+    } else if (DT == SV_BF16) {
+        const unsigned short* q = (const unsigned short*)base + off;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = k0 + 2 * i < V ? __ldg(q + 2 * i) : 0xFF80u;
+            const uint32_t hi = k0 + 2 * i + 1 < V ? __ldg(q + 2 * i + 1) : 0xFF80u;
+            c.w[i] = lo | (hi << 16);
+        }
+    } else {
+        const float* q = (const float*)base + off;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c.w[i] = k0 + i < V ? __float_as_uint(__ldg(q + i)) : 0xFF800000u;
+    }
+    return c;
+}
+
+template <int DT>
+__device__ __forceinline__ float2 pair8(const Cols8& c, int e) {
+    if (DT == SV_BF16) return make_float2(bf16lo_to_f32(c.w[e]), bf16hi_to_f32(c.w[e]));
+    return make_float2(__uint_as_float(c.w[2 * e]), __uint_as_float(c.w[2 * e + 1]));
+}
+
+// Sampler task c: sequence b = c / nS, columns [i * 2048, (i + 1) * 2048) for i = c % nS. The warp walks
+// the task in 8 steps of 256 columns (8 consecutive columns per lane, one 16-byte load per row,
+// prefetched one step ahead); every 2 steps close a 512-column sub-chunk, whose selected sums are
+// reduced over the warp and stored.
+template <int DT, bool VEC>
+__device__ void s_task(const Params& P, uint32_t c, const float2* tab, int lane) {
+    const int32_t b = (int32_t)(c / (uint32_t)P.nS);
+    const int i = (int)(c % (uint32_t)P.nS);
+    uint32_t ok = 1;
+    if (lane == 0) {
+        uint32_t spins = 0;
+        while (ld_relaxed(P.seq_ready + b) == 0u && spins <= kSpinLimit) {
+            __nanosleep(100);
+            ++spins;
+        }
+        if (spins > kSpinLimit) {
+            ok = 0;
+            atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+        }
+        __threadfence();
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();
+    if (!ok) return;
+    const SeqTask tk = ld_task(P.tasks + b);
+    if (tk.mode != kModeNone) {
+        const bool resid = tk.mode == kModeResidual;
+        const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
+        const int32_t cbase = i * kSTask;
+        const int steps = min(kSTask / 256, (P.V - cbase + 255) / 256);
+        ffacc2 Pp, Qq, A, Bq;
+        Cols8 np = load_cols8<DT, VEC>(P.target, (size_t)tk.prow, P.V, cbase + 8 * lane);
+        Cols8 nq;
+        if (resid) nq = load_cols8<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, cbase + 8 * lane);
+#pragma unroll 1
+        for (int e = 0; e < steps; ++e) {
+            const Cols8 cp = np, cq = nq;
+            if (e + 1 < steps) {
+                const int32_t k1 = cbase + 256 * (e + 1) + 8 * lane;
+                np = load_cols8<DT, VEC>(P.target, (size_t)tk.prow, P.V, k1);
+                if (resid) nq = load_cols8<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, k1);
+            }
+            if (resid) {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const ff2 ep = exp2_ff2(pair8<DT>(cp, h), mp, P.K_hi, P.K_lo, tab);
+                    const ff2 eq = exp2_ff2(pair8<DT>(cq, h), mq, P.K_hi, P.K_lo, tab);
+                    Pp.add(ep.hi, ep.lo);
+                    Qq.add(eq.hi, eq.lo);
+                    const float2 mk = sel_mask(ep, eq, tk.rho);
+                    A.add(mul2(ep.hi, mk), mul2(ep.lo, mk));
+                    Bq.add(mul2(eq.hi, mk), mul2(eq.lo, mk));
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const ff2 ep = exp2_ff2(pair8<DT>(cp, h), mp, P.K_hi, P.K_lo, tab);
+                    A.add(ep.hi, ep.lo);
+                }
+            }
+            if ((e & 1) || e + 1 == steps) {  // a 512-column sub-chunk is complete
+                const int sc = i * kSubPerTask + (e >> 1);
+                const double sa = warp_sum_ff(A.fold());
+                const double sb = resid ? warp_sum_ff(Bq.fold()) : 0.0;
+                if (lane == 0) P.subs[(size_t)b * P.nsub + sc] = make_double2(sa, sb);
+                if (!resid) {  // the p total of a bonus draw is the sum of its sub-chunk sums
+                    const float hs = (float)sa;
+                    Pp.add(make_float2(hs, 0.f), make_float2((float)(sa - (double)hs), 0.f));
+                }
+                A = ffacc2();
+                Bq = ffacc2();
+            }
+        }
+        const double sp = resid ? warp_sum_ff(Pp.fold()) : Pp.fold().value();
+        const double sq = resid ? warp_sum_ff(Qq.fold()) : 0.0;
+        if (lane == 0) P.stot[(size_t)b * P.nS + i] = make_double2(sp, sq);
+    }
+    uint32_t last = 0;
+    if (lane == 0) {
+        __threadfence();
+        last = atomicAdd(P.s_done + b, 1u) == (uint32_t)P.nS - 1u;
+    }
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    if (last) {
+        __threadfence();
+        find<DT, VEC>(P, b, tab, lane);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// The kernel
+// ------------------------------------------------------------------------------------------------
+template <int DT, bool VEC, bool GREEDY>
+__global__ void __launch_bounds__(kThreads, 2) k_verify(const Params P) {
+    __shared__ float2 tab[64];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (!GREEDY) fill_exp2_table(tab);
+    if (tid == 0) s_bad = __ldg(P.offs) != 0;
+    __syncthreads();
+    // every CTA checks the whole CSR structure before any row is read
+    int bad = 0;
+    for (int32_t b = tid; b < P.B; b += kThreads) {
+        const int32_t o0 = __ldg(P.offs + b), o1 = __ldg(P.offs + b + 1), g = __ldg(P.gammas + b);
+        bad |= !(g >= 0 && g <= P.max_gamma && o0 >= 0 && o1 - o0 == g);
+    }
+    if (__syncthreads_or(bad) || s_bad) {
+        if (blockIdx.x == 0) {
+            for (int32_t b = tid; b < P.B; b += kThreads) P.out_n[b] = -1;
+            if (tid == 0) atomicOr(P.status, 1u << SV_ERR_BAD_OFFSETS);
+        }
+        return;
+    }
+    const int32_t oB = __ldg(P.offs + P.B);
+    const long long nA = (long long)(GREEDY ? oB + P.B : 2 * oB + P.B) * P.nchA;
+    const uint32_t nStot = GREEDY ? 0u : (uint32_t)P.B * (uint32_t)P.nS;
+    const long long W = (long long)gridDim.x * kWarps;
+    long long a = (long long)blockIdx.x * kWarps + warp;
+    const size_t esz = DT == SV_BF16 ? 2 : 4;
+
+    // Phase 1: this warp still owns statistics tasks. Between them it takes sampler work, but only work
+    // already published (compare-and-swap on the claim counter after seeing the sequence's ready flag),
+    // so it never blocks while others may depend on its statistics tasks.
+    while (a < nA) {
+        if (!GREEDY) {
+            int32_t c = -1;
+            if (lane == 0) {
+                const uint32_t cl = ld_relaxed(&P.ctr->claim);
+                if (cl < nStot && ld_relaxed(P.seq_ready + cl / (uint32_t)P.nS) != 0u &&
+                    atomicCAS(&P.ctr->claim, cl, cl + 1u) == cl)
+                    c = (int32_t)cl;
+            }
+            c = __shfl_sync(0xFFFFFFFFu, c, 0);
+            if (c >= 0) {
+                s_task<DT, VEC>(P, (uint32_t)c, tab, lane);
+                continue;
+            }
+        }
+        const int32_t r = (int32_t)(a / P.nchA), ch = (int32_t)(a % P.nchA);
+        const int32_t b = find_seq<GREEDY>(P, r);
+        const int32_t o0 = __ldg(P.offs + b), g = __ldg(P.gammas + b);
+        const int32_t j = r - (GREEDY ? o0 + b : 2 * o0 + b);
+        const size_t row = j <= g ? (size_t)(o0 + b + j) : (size_t)(o0 + j - g - 1);
+        const char* rowp = (const char*)(j <= g ? P.target : P.draft) + (row * (size_t)P.V + (size_t)ch * kAChunk) * esz;
+        const int len = min(kAChunk, P.V - ch * kAChunk);
+        const SegStats st = seg_stats<DT, VEC, GREEDY>(rowp, len, lane, P.K_hi);
+        uint32_t last = 0;
+        if (lane == 0) {
+            const uint32_t fl = (GREEDY ? st.bad : (st.s != st.s)) ? (1u << SV_ERR_NONFINITE) : 0u;
+            const int arg = st.arg == 0x7FFFFFFF ? -1 : ch * kAChunk + st.arg;
+            P.partials[(size_t)r * P.nchA + ch] = Partial{st.m, st.s, arg, fl};
+            __threadfence();
+            last = atomicAdd(P.a_done + b, 1u) == (uint32_t)(stat_rows<GREEDY>(g) * P.nchA) - 1u;
+        }
+        last = __shfl_sync(0xFFFFFFFFu, last, 0);
+        if (last) {
+            __threadfence();
+            decide<DT, GREEDY>(P, b, g, o0, lane, tab);
+            if (!GREEDY) publish(P, b, lane);
+        }
+        a += W;
+    }
+    if (GREEDY) return;
+    // Phase 2: no statistics tasks left. Take sampler tickets in order; a ticket not yet published is
+    // waited for (bounded), which is safe now that this warp holds nothing others depend on.
+    while (true) {
+        uint32_t cl = 0;
+        if (lane == 0) cl = atomicAdd(&P.ctr->claim, 1u);
+        cl = __shfl_sync(0xFFFFFFFFu, cl, 0);
+        if (cl >= nStot) break;
+        s_task<DT, VEC>(P, cl, tab, lane);
+    }
+}
+
 // ------------------------------------------------------------------------------------------------
 // Launch
 // ------------------------------------------------------------------------------------------------
-static int sm_count() {
-    static int cached[64] = {0};
+template <int DT, bool VEC, bool GREEDY>
+static cudaError_t launch_typed(const Params& P, cudaStream_t st) {
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64) {
-        if (!cached[dev]) {
-            int n = 0;
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-            cached[dev] = n > 0 ? n : 1;
-        }
-        return cached[dev];
-    }
-    return 1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_verify<DT, VEC, GREEDY>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(per_sm * sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_verify<DT, VEC, GREEDY>, P);
 }
 
-template <int DT, bool VEC>
-static cudaError_t launch_typed(const Params& P, bool greedy, cudaStream_t st) {
-    const int sms = sm_count();
-    const long long max_rows = (long long)P.B * (greedy ? P.max_gamma + 1 : 2 * P.max_gamma + 1);
-    const long long stat_items = max_rows * P.nchunks;
-    const int g_stats = (int)std::max(1LL, std::min(stat_items, (long long)sms * 8));
-    const int g_warp = (P.B + kThreads / 32 - 1) / (kThreads / 32);
-    k_validate<<<1, kThreads, 0, st>>>(P);
-    if (greedy) {
-        k_stats<DT, VEC, true><<<g_stats, kThreads, 0, st>>>(P);
-        k_decide<DT, true><<<g_warp, kThreads, 0, st>>>(P);
-    } else {
-        k_stats<DT, VEC, false><<<g_stats, kThreads, 0, st>>>(P);
-        k_decide<DT, false><<<g_warp, kThreads, 0, st>>>(P);
-        const long long sub_items = (long long)P.B * P.nsub;
-        const int g_sub = (int)std::max(1LL, std::min((sub_items + 7) / 8, (long long)sms * 8));
-        k_sample_sums<DT, VEC><<<g_sub, kThreads, 0, st>>>(P);
-        k_sample_find<DT, VEC><<<g_warp, kThreads, 0, st>>>(P);
-    }
-    return cudaGetLastError();
-}
-
-cudaError_t launch_verify(const Params& P, int dtype, bool vec, bool greedy, cudaStream_t st) {
+cudaError_t launch_verify(const Params& P, const Layout& L, void* ws, int dtype, bool vec, bool greedy,
+                          cudaStream_t st) {
     if (P.B == 0) return cudaSuccess;
-    if (dtype == SV_BF16) return vec ? launch_typed<SV_BF16, true>(P, greedy, st) : launch_typed<SV_BF16, false>(P, greedy, st);
-    return vec ? launch_typed<SV_F32, true>(P, greedy, st) : launch_typed<SV_F32, false>(P, greedy, st);
+    const cudaError_t e = cudaMemsetAsync((char*)ws + L.zero_begin, 0, L.zero_end - L.zero_begin, st);
+    if (e != cudaSuccess) return e;
+    if (dtype == SV_BF16) {
+        if (vec) return greedy ? launch_typed<SV_BF16, true, true>(P, st) : launch_typed<SV_BF16, true, false>(P, st);
+        return greedy ? launch_typed<SV_BF16, false, true>(P, st) : launch_typed<SV_BF16, false, false>(P, st);
+    }
+    if (vec) return greedy ? launch_typed<SV_F32, true, true>(P, st) : launch_typed<SV_F32, true, false>(P, st);
+    return greedy ? launch_typed<SV_F32, false, true>(P, st) : launch_typed<SV_F32, false, false>(P, st);
 }
 
 Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    const size_t nchunks = ((size_t)V + kChunk - 1) / kChunk;
+    const size_t nchA = ((size_t)V + kAChunk - 1) / kAChunk;
     const size_t nsub = ((size_t)V + kSub - 1) / kSub;
+    const size_t nS = ((size_t)V + kSTask - 1) / kSTask;
     Layout L;
     L.partials = 0;
-    L.tasks = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchunks * sizeof(Partial));
+    L.tasks = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchA * sizeof(Partial));
     L.subs = up(L.tasks + (size_t)B * sizeof(SeqTask));
-    L.status = up(L.subs + (size_t)B * nsub * sizeof(SubSum));
-    L.batch_bad = L.status + 128;
-    L.total = up(L.batch_bad + sizeof(uint32_t));
+    L.stot = up(L.subs + (size_t)B * nsub * sizeof(double2));
+    L.status = up(L.stot + (size_t)B * nS * sizeof(double2));
+    L.counters = up(L.status + sizeof(uint32_t));
+    L.a_done = up(L.counters + sizeof(Counters));
+    L.s_done = up(L.a_done + (size_t)B * sizeof(uint32_t));
+    L.seq_ready = up(L.s_done + (size_t)B * sizeof(uint32_t));
+    L.zero_begin = L.counters;
+    L.zero_end = up(L.seq_ready + (size_t)B * sizeof(uint32_t));
+    L.total = L.zero_end;
     return L;
 }
 
