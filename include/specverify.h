@@ -117,6 +117,25 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
                    uint32_t* device_status, void* workspace, size_t workspace_bytes,
                    const sv_debug* debug, void* cuda_stream);
 
+/*
+ * Allocation-free form, for callers that cannot call cudaMalloc (for example code running inside a
+ * stream capture it does not own, or a runtime without a device allocator). The pages describe no
+ * such entry point; it exists for those callers only. It behaves as spec_verify_ex on the same
+ * arguments, but its scratch is a fixed 8 MiB array compiled into the library (held on every GPU that
+ * loads the library until the process exits) instead of a caller workspace. It allocates and frees
+ * nothing. Batches whose spec_verify_workspace_size(B, V, max_gamma) exceeds 8 MiB are rejected with
+ * SV_ERR_WORKSPACE before anything is launched. The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress with that device current); make that first call before any
+ * stream capture. All calls share the one array and each call clears what it needs at its start, so
+ * calls that may overlap on the GPU (other streams, other threads) race and must be serialised by the
+ * caller.
+ */
+int spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                        const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                        int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
+                        uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                        uint32_t* device_status, const sv_debug* debug, void* cuda_stream);
+
 /* Map a device status word (OR of 1u << code) to one status code, by the priority above. */
 int spec_verify_status_from_bits(uint32_t bits);
 

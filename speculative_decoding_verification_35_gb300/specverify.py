@@ -18,7 +18,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_MAX_GAMMA = 31
 
 # every exported symbol of the C ABI, in header order
-EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex",
+EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
            "spec_verify_status_from_bits", "spec_verify_status_string")
 
 
@@ -39,6 +39,9 @@ def _load():
     L.spec_verify_ex.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
                                  vp, vp, sz, ctypes.POINTER(SvDebug), vp]
     L.spec_verify_ex.restype = ctypes.c_int
+    L.spec_verify_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
+                                      vp, ctypes.POINTER(SvDebug), vp]
+    L.spec_verify_noalloc.restype = ctypes.c_int
     L.spec_verify_status_from_bits.argtypes = [ctypes.c_uint32]
     L.spec_verify_status_from_bits.restype = ctypes.c_int
     L.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -68,6 +71,17 @@ def spec_verify_ex(target_logits, draft_logits, dtype, draft_tokens, seq_offsets
                               max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
                               device_status, workspace, workspace_bytes,
                               ctypes.byref(debug) if debug is not None else None, cuda_stream)
+
+
+def spec_verify_noalloc(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                        temperature, seed, step, out_tokens, out_num_accepted, device_status,
+                        debug: SvDebug | None, cuda_stream) -> int:
+    """Allocation-free form for callers that cannot allocate device memory: the library's fixed 8 MiB
+    scratch replaces the workspace. Calls sharing it must not overlap on the GPU."""
+    return lib.spec_verify_noalloc(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V,
+                                   max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
+                                   device_status, ctypes.byref(debug) if debug is not None else None,
+                                   cuda_stream)
 
 
 def spec_verify_status_from_bits(bits: int) -> int:

@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_api():
     names = declared_functions()
-    assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex",
+    assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
                           "spec_verify_status_from_bits", "spec_verify_status_string"}
 
 
