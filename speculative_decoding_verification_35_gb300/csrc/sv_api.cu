@@ -91,12 +91,11 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
     P.out_n = out_num_accepted;
     P.status = device_status ? device_status : (uint32_t*)(ws + L.status);
     if (debug) P.dbg = *debug;
-    P.partials = (Partial*)(ws + L.partials);
+    P.partials = (PartialWord*)(ws + L.partials);
     P.tasks = (SeqTask*)(ws + L.tasks);
     P.subs = (double2*)(ws + L.subs);
     P.stot = (double2*)(ws + L.stot);
     P.ctr = (Counters*)(ws + L.counters);
-    P.a_done = (uint32_t*)(ws + L.a_done);
     P.s_done = (uint32_t*)(ws + L.s_done);
     P.seq_ready = (uint32_t*)(ws + L.seq_ready);
     const cudaError_t e = launch_verify(P, L, workspace, (int)dtype, vec, greedy, (cudaStream_t)cuda_stream);

@@ -14,19 +14,23 @@ constexpr int kWarps = kThreads / 32;       // independent warp workers per CTA
 constexpr int kAChunk = 4096;               // vocabulary columns of one statistics task (one warp, one row)
 constexpr int kSub = 512;                   // sampler sub-chunk: the finest unit of the inverse-CDF search
 constexpr int kSubPerLane = kSub / 32;      // 16 consecutive columns per lane
-constexpr int kSTask = 2048;                // vocabulary columns of one sampler task (one warp)
-constexpr int kSubPerTask = kSTask / kSub;  // 4
+constexpr int kSTask = 1024;                // vocabulary columns of one sampler task (one warp)
+constexpr int kSubPerTask = kSTask / kSub;  // 2
+constexpr int kStreamWarps = 4;             // statistics streamers per CTA on the bulk-copy path
+constexpr int kStages = 3;                  // bulk-copy stages per streamer
+constexpr int kStageBytes = kAChunk * 2;    // one bf16 statistics task
+constexpr int kTmaSmemBytes = kStreamWarps * kStages * (kStageBytes + 8);
+constexpr int kFlagStride = 32;             // ready flags one per 128-byte line (words)
+constexpr int kBaseCache = 1024;            // batches up to this size keep their row bases in shared memory
 
 enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2 };
 
-// Partial statistics of one (row, chunk): raw-logit max, sum of 2^((l - m) K) in fp32, first
-// argmax (greedy) and error flags (bit codes of sv_status).
-struct Partial {
-    float m;
-    float s;
-    int32_t arg;
-    uint32_t flags;
-};
+// Partial statistics of one (row, chunk), one 64-bit word written with a single store. The region is
+// zeroed before every call and a written word is never 0, so readers poll the word itself:
+//   sampling: low = bits(raw max m), high = bits(sum of 2^((l - m) K)) (m = +0 implies sum >= 1;
+//             sum = 0 implies m = -inf; a NaN or +inf logit makes the sum NaN);
+//   greedy:   low = bits(m), high = (first argmax + 1) | (1 << 31 if a NaN was seen).
+typedef unsigned long long PartialWord;
 
 // What the sampler draws for one sequence, written by the decision step. 48 bytes, 16-byte
 // aligned: readers fetch it with 16-byte loads.
@@ -67,18 +71,17 @@ struct Params {
     uint32_t* status;
     sv_debug dbg;
     // workspace
-    Partial* partials;  // [B * (2 max_gamma + 1) * nchA]
+    PartialWord* partials;  // [B * (2 max_gamma + 1) * nchA]
     SeqTask* tasks;     // [B]
     double2* subs;      // [B * nsub]: (sum_sel 2^{(l_p-m_p)K}, sum_sel 2^{(l_q-m_q)K}) per sub-chunk
     double2* stot;      // [B * nS]: (sum_all p-weight, sum_all q-weight) per sampler task
     Counters* ctr;
-    uint32_t* a_done;   // [B] statistics tasks finished per sequence
     uint32_t* s_done;   // [B] sampler tasks finished per sequence
-    uint32_t* seq_ready;  // [B] set (release) once a sequence's sampler task record is written
+    uint32_t* seq_ready;  // [B * kFlagStride] set (release) once a sequence's sampler task record is written
 };
 
 struct Layout {
-    size_t partials, tasks, subs, stot, counters, a_done, s_done, seq_ready, status;
+    size_t counters, s_done, seq_ready, partials, tasks, subs, stot, status;
     size_t zero_begin, zero_end;  // byte range the launch sequence clears
     size_t total;
 };

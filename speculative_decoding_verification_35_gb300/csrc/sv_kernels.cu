@@ -36,7 +36,7 @@
 
 namespace sv {
 
-constexpr uint32_t kSpinLimit = 1u << 22;  // ~0.5-1 s of short sleeps before a wait gives up
+constexpr uint32_t kSpinLimit = 1u << 21;  // polls before a wait gives up (about 1-4 s with back-off)
 
 // ------------------------------------------------------------------------------------------------
 // Memory-model helpers for data written by other warps during this launch (never through L1's
@@ -50,12 +50,29 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+// Lane 0 waits (bounded, exponential back-off) until *p >= target, then fences so the data published
+// before the flag is visible. Returns false on time-out (the status word gets SV_ERR_TIMEOUT).
+__device__ __forceinline__ bool wait_geq(const uint32_t* p, uint32_t target, uint32_t* status) {
+    uint32_t spins = 0, ns = 64;
+    while (*(const volatile uint32_t*)p < target) {
+        if (++spins > (1u << 21)) {
+            atomicOr(status, 1u << SV_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(ns);
+        ns = ns < 2048 ? 2 * ns : 2048;
+    }
+    __threadfence();
+    return true;
+}
 __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ Partial ld_partial(const Partial* p) {
-    const int4 v = __ldcg((const int4*)p);
-    return Partial{__int_as_float(v.x), __int_as_float(v.y), v.z, (uint32_t)v.w};
+__device__ __forceinline__ PartialWord ld_word(const PartialWord* p) {
+    return *(const volatile PartialWord*)p;
+}
+__device__ __forceinline__ void st_word(PartialWord* p, PartialWord v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ SeqTask ld_task(const SeqTask* p) {
     static_assert(sizeof(SeqTask) == 48 && alignof(SeqTask) == 16, "SeqTask layout");
@@ -139,18 +156,6 @@ __device__ __forceinline__ int32_t stat_base(const Params& P, int32_t b) {
     return GREEDY ? o + b : 2 * o + b;
 }
 
-// Largest b with stat_base(b) <= r.
-template <bool GREEDY>
-__device__ int32_t find_seq(const Params& P, int32_t r) {
-    int32_t lo = 0, hi = P.B - 1;
-    while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (stat_base<GREEDY>(P, mid) <= r) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
 template <int DT>
 __device__ __forceinline__ float logit_at(const void* base, size_t idx) {
     if (DT == SV_BF16) return __uint_as_float((uint32_t)__ldg((const unsigned short*)base + idx) << 16);
@@ -185,6 +190,65 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
     m = M;
 }
 
+// Sampling-mode statistics of 16 x 8 bf16 values per lane (4096 columns per warp): bf16x2 max, then the
+// fp32 sum of 2^((l - m) K) with packed FMA/ADD and one MUFU ex2 per value.
+__device__ __forceinline__ SegStats stats_bf16(const uint4 (&v)[16], float K) {
+    SegStats r{-INFINITY, 0.f, 0x7FFFFFFF, 0u};
+    __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].x));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].y));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].z));
+        mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].w));
+    }
+    const float m = warp_max(fmaxf(__low2float(mx), __high2float(mx)));
+    float s = 0.f;
+    if (m != -INFINITY) {
+        const float2 K2 = make_float2(K, K);
+        const float2 nmK2 = make_float2(-m * K, -m * K);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float2 x = make_float2(bf16lo_to_f32(w[h]), bf16hi_to_f32(w[h]));
+                const float2 t = __ffma2_rn(x, K2, nmK2);
+                acc = __fadd2_rn(acc, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+            }
+        }
+        s = acc.x + acc.y;
+    } else {
+        // no finite maximum: only a NaN can still hide among -inf entries
+        uint32_t nan = 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                nan |= ((w[h] & 0x7F80u) == 0x7F80u && (w[h] & 0x7Fu)) ||
+                       ((w[h] & 0x7F800000u) == 0x7F800000u && (w[h] & 0x7F0000u));
+        }
+        s = nan ? __int_as_float(0x7FC00000) : 0.f;
+    }
+    r.m = m;
+    r.s = warp_sumf(s);  // a NaN or +inf logit makes this NaN (flagged by the caller)
+    return r;
+}
+
+// The same statistics from a bulk-copied shared-memory stage of `len` columns.
+__device__ __forceinline__ SegStats stats_bf16_smem(const unsigned char* buf, int len, int lane, float K) {
+    uint4 v[16];
+    const uint4* b4 = reinterpret_cast<const uint4*>(buf);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const int e0 = (q * 32 + lane) * 8;
+        v[q] = e0 < len ? b4[q * 32 + lane] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    }
+    return stats_bf16(v, K);
+}
+
 template <int DT, bool VEC, bool GREEDY>
 __device__ __forceinline__ SegStats seg_stats(const char* rowp, int len, int lane, float K) {
     SegStats r{-INFINITY, 0.f, 0x7FFFFFFF, 0u};
@@ -216,46 +280,7 @@ __device__ __forceinline__ SegStats seg_stats(const char* rowp, int len, int lan
             r.m = M;
             r.bad = warp_or(bad) | (M == INFINITY);
         } else {
-            __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].x));
-                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].y));
-                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].z));
-                mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].w));
-            }
-            const float m = warp_max(fmaxf(__low2float(mx), __high2float(mx)));
-            float s = 0.f;
-            if (m != -INFINITY) {
-                const float2 K2 = make_float2(K, K);
-                const float2 nmK2 = make_float2(-m * K, -m * K);
-                float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float2 x = make_float2(bf16lo_to_f32(w[h]), bf16hi_to_f32(w[h]));
-                        const float2 t = __ffma2_rn(x, K2, nmK2);
-                        acc = __fadd2_rn(acc, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
-                    }
-                }
-                s = acc.x + acc.y;
-            } else {
-                // no finite maximum: only a NaN can still hide among -inf entries
-                uint32_t nan = 0;
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h)
-                        nan |= ((w[h] & 0x7F80u) == 0x7F80u && (w[h] & 0x7Fu)) ||
-                               ((w[h] & 0x7F800000u) == 0x7F800000u && (w[h] & 0x7F0000u));
-                }
-                s = nan ? __int_as_float(0x7FC00000) : 0.f;
-            }
-            r.m = m;
-            r.s = warp_sumf(s);  // a NaN or +inf logit makes this NaN (flagged by the caller)
+            r = stats_bf16(v, K);
         }
         return r;
     }
@@ -326,7 +351,7 @@ __device__ __forceinline__ SegStats seg_stats(const char* rowp, int len, int lan
 // Decision for sequence b (one warp): merge partials, accept tests, first rejection, outputs.
 // ------------------------------------------------------------------------------------------------
 template <int DT, bool GREEDY>
-__device__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float2* tab) {
+__device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float2* tab) {
     const int32_t t0 = o0 + b;
     const int nrows = stat_rows<GREEDY>(g);
     const int32_t sbase = stat_base<GREEDY>(P, b);
@@ -343,22 +368,43 @@ __device__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int la
         uint32_t lf[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) { lm[k] = -INFINITY; ls[k] = 0.f; la[k] = 0x7FFFFFFF; lf[k] = 0u; }
-        for (int c = lane; c < nch; c += 32) {
-            Partial q[8];
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int c = c0 + lane;
+            PartialWord q[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                if (j0 + k < nrows) q[k] = ld_partial(P.partials + (size_t)(sbase + j0 + k) * nch + c);
+                q[k] = (j0 + k < nrows && c < nch) ? ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c) : 1ull;
+            // words still 0 are statistics tasks in flight: poll them (bounded back-off)
+            uint32_t spins = 0, ns = 64;
+            while (__any_sync(0xFFFFFFFFu, q[0] == 0 || q[1] == 0 || q[2] == 0 || q[3] == 0 || q[4] == 0 ||
+                                               q[5] == 0 || q[6] == 0 || q[7] == 0)) {
+                if (++spins > (1u << 21)) {
+                    if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+                    err |= 1u << SV_ERR_TIMEOUT;
+                    break;
+                }
+                __nanosleep(ns);
+                ns = ns < 2048 ? 2 * ns : 2048;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (q[k] == 0) q[k] = ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c);
+            }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                if (j0 + k >= nrows) continue;
-                lf[k] |= q[k].flags;
+                if (j0 + k >= nrows || c >= nch) continue;
+                const float qm = __uint_as_float((uint32_t)q[k]);
+                const uint32_t qh = (uint32_t)(q[k] >> 32);
                 if (GREEDY) {
-                    if (q[k].m > lm[k]) { lm[k] = q[k].m; la[k] = q[k].arg; }
-                } else if (q[k].s != q[k].s) {
-                    ls[k] = q[k].s;
-                    lm[k] = fmaxf(lm[k], q[k].m);
-                } else if (ls[k] == ls[k]) {
-                    merge_ms(lm[k], ls[k], q[k].m, q[k].s, K);
+                    if (qh >> 31) lf[k] |= 1u << SV_ERR_NONFINITE;
+                    if (qm > lm[k]) { lm[k] = qm; la[k] = (int)(qh & 0x7FFFFFFFu) - 1; }
+                } else {
+                    const float qs = __uint_as_float(qh);
+                    if (qs != qs) {
+                        ls[k] = qs;
+                        lm[k] = fmaxf(lm[k], qm);
+                    } else if (ls[k] == ls[k]) {
+                        merge_ms(lm[k], ls[k], qm, qs, K);
+                    }
                 }
             }
         }
@@ -468,7 +514,7 @@ __device__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int la
 // Publish sequence b's sampler work: lane 0 wrote the task record, and its release store orders that
 // write before the flag.
 __device__ __forceinline__ void publish(const Params& P, int32_t b, int lane) {
-    if (lane == 0) st_release(P.seq_ready + b, 1u);
+    if (lane == 0) st_release(P.seq_ready + (size_t)b * kFlagStride, 1u);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -592,7 +638,7 @@ __device__ int32_t scan_elements(const Params& P, const SeqTask& tk, bool resid,
 
 // Find for sequence b (one warp): normalisers, sub-chunk search, element search, output.
 template <int DT, bool VEC>
-__device__ void find(const Params& P, int32_t b, const float2* tab, int lane) {
+__device__ __noinline__ void find(const Params& P, int32_t b, const float2* tab, int lane) {
     const SeqTask tk = ld_task(P.tasks + b);
     if (tk.mode == kModeNone) return;
     const double2* ss = P.subs + (size_t)b * P.nsub;
@@ -740,18 +786,7 @@ __device__ void s_task(const Params& P, uint32_t c, const float2* tab, int lane)
     const int32_t b = (int32_t)(c / (uint32_t)P.nS);
     const int i = (int)(c % (uint32_t)P.nS);
     uint32_t ok = 1;
-    if (lane == 0) {
-        uint32_t spins = 0;
-        while (ld_relaxed(P.seq_ready + b) == 0u && spins <= kSpinLimit) {
-            __nanosleep(100);
-            ++spins;
-        }
-        if (spins > kSpinLimit) {
-            ok = 0;
-            atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
-        }
-        __threadfence();
-    }
+    if (lane == 0) ok = wait_geq(P.seq_ready + (size_t)b * kFlagStride, 1u, P.status);  // back-off wait
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     __syncwarp();
     if (!ok) return;
@@ -821,22 +856,132 @@ __device__ void s_task(const Params& P, uint32_t c, const float2* tab, int lane)
 }
 
 // ------------------------------------------------------------------------------------------------
+// Statistics tasks
+// ------------------------------------------------------------------------------------------------
+struct ATask {
+    int32_t r, ch, b, g, o0;
+    const char* rowp;
+    int len;
+};
+
+// Row, chunk and sequence of statistics task t (sequence-major order). `cur` is a sequence cursor that
+// only moves forward: a warp visits its tasks in increasing order, so the owning sequence is found
+// with a couple of cached offset reads instead of a search.
+template <int DT, bool GREEDY>
+__device__ __forceinline__ ATask a_task_at(const Params& P, long long t, int32_t& cur, const int32_t* bases) {
+    ATask at;
+    at.r = (int32_t)(t / P.nchA);
+    at.ch = (int32_t)(t % P.nchA);
+    // bases: the sequences' first statistics rows in shared memory (small batches), else from offsets
+    while (cur + 1 < P.B && (bases ? bases[cur + 1] : stat_base<GREEDY>(P, cur + 1)) <= at.r) ++cur;
+    at.b = cur;
+    at.o0 = __ldg(P.offs + at.b);
+    at.g = __ldg(P.gammas + at.b);
+    const int32_t j = at.r - (GREEDY ? at.o0 + at.b : 2 * at.o0 + at.b);
+    const size_t row = j <= at.g ? (size_t)(at.o0 + at.b + j) : (size_t)(at.o0 + j - at.g - 1);
+    const size_t esz = DT == SV_BF16 ? 2 : 4;
+    at.rowp = (const char*)(j <= at.g ? P.target : P.draft) + (row * (size_t)P.V + (size_t)at.ch * kAChunk) * esz;
+    at.len = min(kAChunk, P.V - at.ch * kAChunk);
+    return at;
+}
+
+// Store the task's partial word (one 64-bit store; no fence, no counter: the decision polls the words).
+template <bool GREEDY>
+__device__ __forceinline__ void a_finish(const Params& P, const ATask& at, const SegStats& st, int lane) {
+    if (lane == 0) {
+        uint32_t hi;
+        if (GREEDY) {
+            const int arg = st.arg == 0x7FFFFFFF ? -1 : at.ch * kAChunk + st.arg;
+            hi = (uint32_t)(arg + 1) | (st.bad ? 0x80000000u : 0u);
+        } else {
+            hi = __float_as_uint(st.s);
+        }
+        st_word(P.partials + (size_t)at.r * P.nchA + at.ch, ((PartialWord)hi << 32) | __float_as_uint(st.m));
+    }
+}
+
+// Decision of sequence b, run by the warp holding its first ticket; it waits for the partials itself.
+template <int DT, bool GREEDY>
+__device__ void lead_decide(const Params& P, int32_t b, const float2* tab, int lane) {
+    const int32_t o0 = __ldg(P.offs + b), g = __ldg(P.gammas + b);
+    decide<DT, GREEDY>(P, b, g, o0, lane, tab);  // polls the sequence's partial words
+    if (!GREEDY) publish(P, b, lane);
+}
+
+// A streamer warp on the bulk-copy path: its statistics tasks (statically strided over all streamers)
+// arrive through a ring of kStages shared-memory stages filled by 1-D bulk copies, so up to
+// kStages - 1 tasks stay in flight while one is reduced, without holding registers.
+__device__ void stream_bulk(const Params& P, long long nA, unsigned char* dsmem, const int32_t* bases, int warp,
+                            int lane) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(dsmem + kStreamWarps * kStages * kStageBytes) + warp * kStages;
+    unsigned char* bufs = dsmem + (size_t)warp * kStages * kStageBytes;
+    const long long SW = (long long)gridDim.x * kStreamWarps;
+    const long long sw = (long long)blockIdx.x * kStreamWarps + warp;
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    int32_t cur_issue = 0, cur_proc = 0;
+    auto issue = [&](long long t, int s) {  // lane 0
+        const ATask at = a_task_at<SV_BF16, false>(P, t, cur_issue, bases);
+        const uint32_t bytes = (uint32_t)at.len * 2u;
+        mbar_arrive_expect_tx(&bars[s], bytes);
+        bulk_g2s(bufs + (size_t)s * kStageBytes, at.rowp, bytes, &bars[s]);
+    };
+    if (lane == 0)
+        for (int s = 0; s < kStages; ++s)
+            if (sw + s * SW < nA) issue(sw + s * SW, s);
+    uint32_t parity = 0;  // bit s: parity of stage s's next completion
+    int k = 0;
+    for (long long t = sw; t < nA; t += SW, ++k) {
+        const int s = k % kStages;
+        const bool ok = mbar_wait(&bars[s], (parity >> s) & 1u, kSpinLimit);
+        parity ^= 1u << s;
+        if (!ok) {
+            // a copy that never lands: report, let the copies still in flight land, stop streaming
+            if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+            for (int q = 1; q < kStages; ++q) {
+                const int s2 = (k + q) % kStages;
+                if (t + q * SW < nA) mbar_wait(&bars[s2], (parity >> s2) & 1u, kSpinLimit);
+            }
+            return;
+        }
+        const ATask at = a_task_at<SV_BF16, false>(P, t, cur_proc, bases);
+        const SegStats st = stats_bf16_smem(bufs + (size_t)s * kStageBytes, at.len, lane, P.K_hi);
+        __syncwarp();
+        if (lane == 0 && t + kStages * SW < nA) {
+            fence_proxy_async_smem();  // this stage's reads come before the copy that overwrites it
+            issue(t + kStages * SW, s);
+        }
+        a_finish<false>(P, at, st, lane);
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
 // The kernel
 // ------------------------------------------------------------------------------------------------
 template <int DT, bool VEC, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 2) k_verify(const Params P) {
+    constexpr bool kBulk = DT == SV_BF16 && VEC && !GREEDY;
+    extern __shared__ __align__(128) unsigned char dsmem[];
     __shared__ float2 tab[64];
     __shared__ int s_bad;
+    __shared__ int32_t s_base[kBaseCache];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (!GREEDY) fill_exp2_table(tab);
     if (tid == 0) s_bad = __ldg(P.offs) != 0;
     __syncthreads();
-    // every CTA checks the whole CSR structure before any row is read
+    // every CTA checks the whole CSR structure before any row is read (and caches small batches' row
+    // bases for the statistics tasks)
     int bad = 0;
+    const bool cache = P.B <= kBaseCache;
     for (int32_t b = tid; b < P.B; b += kThreads) {
         const int32_t o0 = __ldg(P.offs + b), o1 = __ldg(P.offs + b + 1), g = __ldg(P.gammas + b);
         bad |= !(g >= 0 && g <= P.max_gamma && o0 >= 0 && o1 - o0 == g);
+        if (cache) s_base[b] = GREEDY ? o0 + b : 2 * o0 + b;
     }
+    const int32_t* bases = cache ? s_base : nullptr;
     if (__syncthreads_or(bad) || s_bad) {
         if (blockIdx.x == 0) {
             for (int32_t b = tid; b < P.B; b += kThreads) P.out_n[b] = -1;
@@ -847,60 +992,36 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const Params P) {
     const int32_t oB = __ldg(P.offs + P.B);
     const long long nA = (long long)(GREEDY ? oB + P.B : 2 * oB + P.B) * P.nchA;
     const uint32_t nStot = GREEDY ? 0u : (uint32_t)P.B * (uint32_t)P.nS;
-    const long long W = (long long)gridDim.x * kWarps;
-    long long a = (long long)blockIdx.x * kWarps + warp;
-    const size_t esz = DT == SV_BF16 ? 2 : 4;
 
-    // Phase 1: this warp still owns statistics tasks. Between them it takes sampler work, but only work
-    // already published (compare-and-swap on the claim counter after seeing the sequence's ready flag),
-    // so it never blocks while others may depend on its statistics tasks.
-    while (a < nA) {
-        if (!GREEDY) {
-            int32_t c = -1;
-            if (lane == 0) {
-                const uint32_t cl = ld_relaxed(&P.ctr->claim);
-                if (cl < nStot && ld_relaxed(P.seq_ready + cl / (uint32_t)P.nS) != 0u &&
-                    atomicCAS(&P.ctr->claim, cl, cl + 1u) == cl)
-                    c = (int32_t)cl;
-            }
-            c = __shfl_sync(0xFFFFFFFFu, c, 0);
-            if (c >= 0) {
-                s_task<DT, VEC>(P, (uint32_t)c, tab, lane);
-                continue;
-            }
+    // Statistics. Bulk-copy path: kStreamWarps warps per CTA stream while the others start sampling at
+    // once. Other paths: every warp streams its strided tasks from registers first.
+    if (kBulk) {
+        if (warp < kStreamWarps) stream_bulk(P, nA, dsmem, bases, warp, lane);
+    } else {
+        const long long W = (long long)gridDim.x * kWarps;
+        int32_t cur = 0;
+        for (long long a = (long long)blockIdx.x * kWarps + warp; a < nA; a += W) {
+            const ATask at = a_task_at<DT, GREEDY>(P, a, cur, bases);
+            const SegStats st = seg_stats<DT, VEC, GREEDY>(at.rowp, at.len, lane, P.K_hi);
+            a_finish<GREEDY>(P, at, st, lane);
         }
-        const int32_t r = (int32_t)(a / P.nchA), ch = (int32_t)(a % P.nchA);
-        const int32_t b = find_seq<GREEDY>(P, r);
-        const int32_t o0 = __ldg(P.offs + b), g = __ldg(P.gammas + b);
-        const int32_t j = r - (GREEDY ? o0 + b : 2 * o0 + b);
-        const size_t row = j <= g ? (size_t)(o0 + b + j) : (size_t)(o0 + j - g - 1);
-        const char* rowp = (const char*)(j <= g ? P.target : P.draft) + (row * (size_t)P.V + (size_t)ch * kAChunk) * esz;
-        const int len = min(kAChunk, P.V - ch * kAChunk);
-        const SegStats st = seg_stats<DT, VEC, GREEDY>(rowp, len, lane, P.K_hi);
-        uint32_t last = 0;
-        if (lane == 0) {
-            const uint32_t fl = (GREEDY ? st.bad : (st.s != st.s)) ? (1u << SV_ERR_NONFINITE) : 0u;
-            const int arg = st.arg == 0x7FFFFFFF ? -1 : ch * kAChunk + st.arg;
-            P.partials[(size_t)r * P.nchA + ch] = Partial{st.m, st.s, arg, fl};
-            __threadfence();
-            last = atomicAdd(P.a_done + b, 1u) == (uint32_t)(stat_rows<GREEDY>(g) * P.nchA) - 1u;
-        }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (last) {
-            __threadfence();
-            decide<DT, GREEDY>(P, b, g, o0, lane, tab);
-            if (!GREEDY) publish(P, b, lane);
-        }
-        a += W;
     }
-    if (GREEDY) return;
-    // Phase 2: no statistics tasks left. Take sampler tickets in order; a ticket not yet published is
-    // waited for (bounded), which is safe now that this warp holds nothing others depend on.
+    // Tickets in sequence order. Greedy: one ticket per sequence, its decision. Sampling: nS sampler
+    // tasks per sequence; the holder of a sequence's first ticket first waits for the sequence's
+    // statistics, decides and publishes it; the others wait for that ready flag. Waits are bounded.
+    // Only warps whose statistics tasks are done ever wait, so every awaited count is completed by warps
+    // that never wait.
+    const uint32_t ntick = GREEDY ? (uint32_t)P.B : nStot;
     while (true) {
         uint32_t cl = 0;
         if (lane == 0) cl = atomicAdd(&P.ctr->claim, 1u);
         cl = __shfl_sync(0xFFFFFFFFu, cl, 0);
-        if (cl >= nStot) break;
+        if (cl >= ntick) break;
+        if (GREEDY) {
+            lead_decide<DT, true>(P, (int32_t)cl, tab, lane);
+            continue;
+        }
+        if (cl % (uint32_t)P.nS == 0u) lead_decide<DT, false>(P, (int32_t)(cl / (uint32_t)P.nS), tab, lane);
         s_task<DT, VEC>(P, cl, tab, lane);
     }
 }
@@ -910,19 +1031,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const Params P) {
 // ------------------------------------------------------------------------------------------------
 template <int DT, bool VEC, bool GREEDY>
 static cudaError_t launch_typed(const Params& P, cudaStream_t st) {
+    constexpr bool kBulk = DT == SV_BF16 && VEC && !GREEDY;
+    constexpr int smem = kBulk ? kTmaSmemBytes : 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (kBulk) {
+        e = cudaFuncSetAttribute(k_verify<DT, VEC, GREEDY>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_verify<DT, VEC, GREEDY>, kThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_verify<DT, VEC, GREEDY>, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(per_sm * sms));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -951,18 +1078,18 @@ Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma) {
     const size_t nsub = ((size_t)V + kSub - 1) / kSub;
     const size_t nS = ((size_t)V + kSTask - 1) / kSTask;
     Layout L;
-    L.partials = 0;
-    L.tasks = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchA * sizeof(Partial));
+    // the first four regions are cleared before every call, with one memset
+    L.counters = 0;
+    L.s_done = up(L.counters + sizeof(Counters));
+    L.seq_ready = up(L.s_done + (size_t)B * sizeof(uint32_t));
+    L.partials = up(L.seq_ready + (size_t)B * kFlagStride * sizeof(uint32_t));
+    L.tasks = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchA * sizeof(PartialWord));
+    L.zero_begin = 0;
+    L.zero_end = L.tasks;
     L.subs = up(L.tasks + (size_t)B * sizeof(SeqTask));
     L.stot = up(L.subs + (size_t)B * nsub * sizeof(double2));
     L.status = up(L.stot + (size_t)B * nS * sizeof(double2));
-    L.counters = up(L.status + sizeof(uint32_t));
-    L.a_done = up(L.counters + sizeof(Counters));
-    L.s_done = up(L.a_done + (size_t)B * sizeof(uint32_t));
-    L.seq_ready = up(L.s_done + (size_t)B * sizeof(uint32_t));
-    L.zero_begin = L.counters;
-    L.zero_end = up(L.seq_ready + (size_t)B * sizeof(uint32_t));
-    L.total = L.zero_end;
+    L.total = up(L.status + sizeof(uint32_t));
     return L;
 }
 
