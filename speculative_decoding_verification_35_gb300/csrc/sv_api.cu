@@ -62,6 +62,10 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
         (uintptr_t)out_num_accepted % 4 || (draft_tokens && (uintptr_t)draft_tokens % 4))
         return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
+    // task indices are 32-bit on the device: statistics tasks and tickets stay below 2^31
+    const uint64_t nchA = ((uint64_t)V + kAChunk - 1) / kAChunk, nS = ((uint64_t)V + kSTask - 1) / kSTask;
+    if ((uint64_t)B * (2 * (uint64_t)max_gamma + 1) * nchA >= (1ull << 31) || (uint64_t)B * (nS + 1) >= (1ull << 31))
+        return SV_ERR_INVALID_ARG;
     const Layout L = workspace_layout(B, V, max_gamma);
     if (!workspace || workspace_bytes < L.total || (uintptr_t)workspace % 256) return SV_ERR_WORKSPACE;
 
@@ -79,11 +83,11 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
     P.V = V;
     P.max_gamma = max_gamma;
     P.nchA = (V + kAChunk - 1) / kAChunk;
-    P.nsub = (V + kSub - 1) / kSub;
     P.nS = (V + kSTask - 1) / kSTask;
+    P.nS_recip = P.nS >= 2 ? ~0ull / (unsigned long long)P.nS + 1ull : 0ull;
     P.K_hi = K_hi;
     P.K_lo = (float)(K64 - (double)K_hi);
-    P.K64 = K64;
+    P.d_min = greedy ? 0.f : (float)(-126.5 / (double)K_hi);
     P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;
     P.seed = seed;
     P.step = step;
@@ -91,13 +95,16 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
     P.out_n = out_num_accepted;
     P.status = device_status ? device_status : (uint32_t*)(ws + L.status);
     if (debug) P.dbg = *debug;
+    for (int j = 0; j < 64; ++j) {  // Tang's table: 2^(j/64) as a float pair (hi, lo)
+        const double v = std::exp2((double)j / 64.0);
+        const float hi = (float)v;
+        P.exp2_tab[j] = make_float2(hi, (float)(v - (double)hi));
+    }
     P.partials = (PartialWord*)(ws + L.partials);
-    P.tasks = (SeqTask*)(ws + L.tasks);
-    P.subs = (double2*)(ws + L.subs);
-    P.stot = (double2*)(ws + L.stot);
+    P.taskw = (Word*)(ws + L.taskw);
+    P.recw = (Word*)(ws + L.recw);
+    P.groupw = (Word*)(ws + L.groupw);
     P.ctr = (Counters*)(ws + L.counters);
-    P.s_done = (uint32_t*)(ws + L.s_done);
-    P.seq_ready = (uint32_t*)(ws + L.seq_ready);
     const cudaError_t e = launch_verify(P, L, workspace, (int)dtype, vec, greedy, (cudaStream_t)cuda_stream);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -29,13 +29,53 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
     return c;
 }
 
-// Uniform of one draw: the top 24 bits of word 0, scaled by 2^-24 (exact in float and double).
+// ------------------------------------------------------------------------------------------------
+// Arithmetic on the FMA and integer pipes only. The statistics pass keeps the multi-function unit
+// (MUFU: ex2, reciprocal, conversions) saturated; a warp on the critical path (a decision, a sampler
+// task, a find) that needs that unit waits behind it, so those warps use these instead.
+// ------------------------------------------------------------------------------------------------
+// float(v), exact for v < 2^24: the low 23 bits through the 2^23 mantissa trick, bit 23 added after.
+__device__ __forceinline__ float u24_to_float(uint32_t v) {
+    const float lo = __fsub_rn(__uint_as_float(0x4B000000u | (v & 0x7FFFFFu)), 8388608.f);
+    return (v & 0x800000u) ? __fadd_rn(lo, 8388608.f) : lo;
+}
+
+// 2^x for x <= 0 (fp32 accuracy, a few ulp): x = n + f with n = rint(x), |f| <= 1/2, and 2^f = e^(f ln 2)
+// by its Taylor series to degree 7 (truncation below 5e-9 for |f ln 2| <= 0.35). 0 below -126.
+__device__ __forceinline__ float exp2_fma(float x) {
+    x = fmaxf(x, -127.f);
+    const float jm = __fadd_rn(x, 12582912.f);  // rint(x) in the low mantissa bits
+    const int n = __float_as_int(jm) - 0x4B400000;
+    const float y = __fmul_rn(__fsub_rn(x, __fsub_rn(jm, 12582912.f)), 0.693147180559945309f);
+    float p = __fmaf_rn(y, 1.f / 5040.f, 1.f / 720.f);
+    p = __fmaf_rn(p, y, 1.f / 120.f);
+    p = __fmaf_rn(p, y, 1.f / 24.f);
+    p = __fmaf_rn(p, y, 1.f / 6.f);
+    p = __fmaf_rn(p, y, 0.5f);
+    p = __fmaf_rn(p, y, 1.f);
+    p = __fmaf_rn(p, y, 1.f);
+    return n >= -126 ? __fmul_rn(p, __int_as_float((n + 127) << 23)) : 0.f;
+}
+
+// a / b for finite a and b in [2^-125, 2^125] (within an ulp or so): reciprocal by Newton's iteration
+// r <- r (2 - b r) from the seed with bits 0x7F000000 - bits(b), which is 2^(-e-1) (3 - m) for
+// b = 2^e m, 1 <= m < 2, i.e. within 1/8 of 1/b (four steps reach float precision); then one residual
+// correction of the quotient.
+__device__ __forceinline__ float div_fma(float a, float b) {
+    float r = __int_as_float(0x7F000000 - __float_as_int(b));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r = __fmul_rn(r, __fmaf_rn(-b, r, 2.f));
+    const float q = __fmul_rn(a, r);
+    return __fmaf_rn(r, __fmaf_rn(-b, q, a), q);
+}
+
+// Uniform of one draw: the top 24 bits of word 0, scaled by 2^-24 (exact in float).
 // purpose 0: accept test of `slot`; purpose 1: the residual / bonus draw at the emitting slot.
-__device__ __forceinline__ double philox_uniform(uint64_t seed, uint64_t step, uint32_t seq,
-                                                uint32_t slot, uint32_t purpose) {
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t step, uint32_t seq, uint32_t slot,
+                                                uint32_t purpose) {
     const uint4 ctr = make_uint4((uint32_t)step, (uint32_t)(step >> 32), seq, (slot << 8) | (purpose & 0xFFu));
     const uint2 key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
-    return (double)(philox4x32_10(ctr, key).x >> 8) * (1.0 / 16777216.0);
+    return u24_to_float(philox4x32_10(ctr, key).x >> 8) * 5.9604644775390625e-8f;  // 2^-24
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -67,44 +107,35 @@ struct ffacc {
         hi = s;
         lo = __fadd_rn(lo, __fadd_rn(e, l));
     }
-    __device__ __forceinline__ double value() const { return (double)hi + (double)lo; }
 };
 
-// ------------------------------------------------------------------------------------------------
-// Precise 2^t for t = d * K <= 0, d = d_hi + d_lo, K = K_hi + K_lo (float-float).
-// Returns a float-float value (|lo| a few ulp(hi) at most) with relative error below about 1e-9
-// (the fp32 roundings of r, y and e^y - 1, each ~3e-10 of a quantity below 0.0055); values below
-// 2^-125 return 0 (they are below any weight the draw can see).
-// `tab` holds 2^(j/64), j = 0..63, as (hi, lo) pairs.
-// ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ ff exp2_ff(float d_hi, float d_lo, float K_hi, float K_lo, const float2* tab) {
-    const float t_hi = __fmul_rn(d_hi, K_hi);
-    float t_lo = __fmaf_rn(d_hi, K_hi, -t_hi);  // exact rounding error of the product
-    t_lo = __fmaf_rn(d_hi, K_lo, t_lo);
-    t_lo = __fmaf_rn(d_lo, K_hi, t_lo);
-    if (!(t_hi > -125.5f)) return ff{0.f, 0.f};  // also catches -inf and NaN
-    const float jf = rintf(__fmul_rn(t_hi, 64.f));
-    const int j = (int)jf;
-    // t_hi - j/64 is exact: both are multiples of ulp(t_hi) and |difference| <= 1/128
-    const float r = __fadd_rn(__fmaf_rn(jf, -0.015625f, t_hi), t_lo);
-    // y = r * ln 2 with ln 2 split in two floats (hi = 0.693145751953125 exactly, 12 bits)
-    const float y = __fmaf_rn(r, 0.693145751953125f, __fmul_rn(r, 1.42860682030941723212e-6f));
-    // e^y - 1 = y + y^2 (1/2 + y/6 + y^2/24) + O(y^5), |y| <= 0.0055
-    float c = __fmaf_rn(y, 1.0f / 24.0f, 1.0f / 6.0f);
-    c = __fmaf_rn(c, y, 0.5f);
-    const float em1 = __fmaf_rn(__fmul_rn(c, y), y, y);
-    const float2 T = tab[j & 63];
-    // 2^(j/64) * e^y = T.x + T.x*em1 + T.y*(1 + em1); the middle product is split exactly
-    const float p = __fmul_rn(T.x, em1);
-    const float pe = __fmaf_rn(T.x, em1, -p);
-    float h, l;
-    fast_two_sum(T.x, p, h, l);
-    l = __fadd_rn(l, __fadd_rn(pe, __fmaf_rn(T.y, em1, T.y)));
-    // scale by 2^(j >> 6): exact power-of-two multiply while the result stays normal
-    const int n = j >> 6;  // floor(j / 64)
-    const float sc = __int_as_float((n + 127) << 23);
-    return ff{__fmul_rn(h, sc), __fmul_rn(l, sc)};
+// Normalised float-float arithmetic (hi = RN(hi + lo)); about 2^-44 relative accuracy, which is all
+// the inverse CDF needs. Normalised values compare lexicographically.
+__device__ __forceinline__ ff ff_norm(float hi, float lo) {
+    ff r;
+    fast_two_sum(hi, lo, r.hi, r.lo);
+    return r;
 }
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    return ff_norm(s, __fadd_rn(e, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, ff{-b.hi, -b.lo}); }
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+    const float p = __fmul_rn(a.hi, b.hi);
+    float e = __fmaf_rn(a.hi, b.hi, -p);  // exact rounding error of the leading product
+    e = __fmaf_rn(a.hi, b.lo, e);
+    e = __fmaf_rn(a.lo, b.hi, e);
+    return ff_norm(p, e);
+}
+// a / b: one correction step on the float quotient
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+    const float q1 = div_fma(a.hi, b.hi);
+    const ff r = ff_sub(a, ff_mul(ff{q1, 0.f}, b));
+    return ff_norm(q1, div_fma(r.hi, b.hi));
+}
+__device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 
 // ------------------------------------------------------------------------------------------------
 // Packed forms: two independent float-float values per register pair, so every floating-point step
@@ -112,7 +143,8 @@ __device__ __forceinline__ ff exp2_ff(float d_hi, float d_lo, float K_hi, float 
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+// a - b as one packed fused multiply-add (b * -1 is exact, so this rounds exactly like a - b)
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
@@ -130,55 +162,66 @@ struct ffacc2 {
         hi = s;
         lo = add2(lo, add2(e, l));
     }
-    // sum of both streams as one float-float value (exact split of the two hi parts)
-    __device__ __forceinline__ ffacc fold() const {
-        ffacc r;
+    // sum of both streams as one normalised float-float value (exact split of the two hi parts)
+    __device__ __forceinline__ ff fold() const {
         float s, e;
         two_sum(hi.x, hi.y, s, e);
-        r.hi = s;
-        r.lo = __fadd_rn(__fadd_rn(lo.x, lo.y), e);
-        return r;
+        return ff_norm(s, __fadd_rn(__fadd_rn(lo.x, lo.y), e));
     }
 };
 
-// 2^((l - m) K) for two columns, precise as exp2_ff: the subtraction split exactly (TwoSum), the
-// argument carried as float-float, Tang's table step and the e^y - 1 series on |y| <= ln2/128.
-// Columns whose argument is below -125.5 (including -inf logits) give exactly 0.
-__device__ __forceinline__ ff2 exp2_ff2(float2 l, float2 m, float K_hi, float K_lo, const float2* tab) {
-    const float2 Kh = f2(K_hi), Kl = f2(K_lo);
-    // d = l - m exactly as d_hi + d_lo
-    const float2 d_hi = sub2(l, m);
-    const float2 bb = sub2(d_hi, l);
-    const float2 d_lo = add2(sub2(l, sub2(d_hi, bb)), sub2(make_float2(-m.x, -m.y), bb));
-    // t = d * K as t_hi + t_lo
-    const float2 t_hi = mul2(d_hi, Kh);
-    float2 t_lo = fma2(d_hi, Kh, make_float2(-t_hi.x, -t_hi.y));
-    t_lo = fma2(d_hi, Kl, t_lo);
-    t_lo = fma2(d_lo, Kh, t_lo);
-    const bool ok0 = t_hi.x > -125.5f, ok1 = t_hi.y > -125.5f;  // false for -inf and NaN as well
-    // columns that are not ok run on a harmless argument and are zeroed at the end
-    const float2 tc = make_float2(ok0 ? t_hi.x : 0.f, ok1 ? t_hi.y : 0.f);
-    t_lo = make_float2(ok0 ? t_lo.x : 0.f, ok1 ? t_lo.y : 0.f);
-    // j = rint(64 t): adding 1.5 * 2^23 rounds to an integer held in the low mantissa bits
-    const float2 jm = fma2(tc, f2(64.f), f2(12582912.f));
-    const int j0 = __float_as_int(jm.x) - 0x4B400000, j1 = __float_as_int(jm.y) - 0x4B400000;
-    const float2 jf = sub2(jm, f2(12582912.f));
-    const float2 r = add2(fma2(jf, f2(-0.015625f), tc), t_lo);  // |r| <= 1/128 (+ rounding)
+// Constants of the precise exponential: K = log2(e) / T as float-float, and the clamp of l - m that
+// maps every argument at or below it (and -inf logits) to exactly 0.
+struct ExpConst {
+    float K_hi, K_lo, nK_hi;  // nK_hi = -K_hi
+    float d_min;              // about -126.5 / K: 2^(d_min K) would be subnormal
+};
+
+// 2^((l - m) K) for two columns, m the row maximum (so the argument is <= 0), as float-float with
+// relative error below about 1e-9. Tang's method: t = d K carried as t_hi + t_lo, j = rint(64 t),
+// 2^t = 2^(j >> 6) * 2^((j & 63) / 64) * e^y with |y| <= ln2/128 and e^y - 1 from its Taylor series.
+// tab holds 2^(i/64) split in floats: tab[i] (high part) and tab[64 + i] (low part), i = 0..63.
+// EXACT_D: l - m is exact in float (bf16 logits); otherwise its rounding error is carried too.
+// Arguments at or below d_min K, including -inf logits, give exactly 0 (2^-126 and below only).
+template <bool EXACT_D>
+__device__ __forceinline__ ff2 exp2_ff2(float2 l, float2 m, const ExpConst& C, const float* tab) {
+    float2 d = sub2(l, m);
+    float2 dl = make_float2(0.f, 0.f);
+    if (!EXACT_D) {  // TwoSum error of l - m; zero where the clamp below applies (incl. -inf)
+        const float2 bb = sub2(d, l);
+        dl = add2(sub2(l, sub2(d, bb)), sub2(make_float2(-m.x, -m.y), bb));
+        dl = make_float2(d.x > C.d_min ? dl.x : 0.f, d.y > C.d_min ? dl.y : 0.f);
+    }
+    d = make_float2(fmaxf(d.x, C.d_min), fmaxf(d.y, C.d_min));
+    const float2 nt = mul2(d, f2(C.nK_hi));          // -t_hi
+    float2 tl = fma2(d, f2(C.K_hi), nt);              // exact rounding error of d * K_hi
+    tl = fma2(d, f2(C.K_lo), tl);
+    if (!EXACT_D) tl = fma2(dl, f2(C.K_hi), tl);
+    // j = rint(64 t_hi) lands in the low mantissa bits of jm (adding 1.5 * 2^23 rounds to an integer)
+    const float2 jm = fma2(nt, f2(-64.f), f2(12582912.f));
+    const uint32_t b0 = __float_as_uint(jm.x), b1 = __float_as_uint(jm.y);
+    const float2 jf = add2(jm, f2(-12582912.f));
+    // r = t - j/64 = t_lo - (-t_hi + j/64), the bracket exact; y = r ln 2 with ln 2 in two parts
+    const float2 r = sub2(tl, fma2(jf, f2(0.015625f), nt));
     const float2 y = fma2(r, f2(0.693145751953125f), mul2(r, f2(1.42860682030941723212e-6f)));
     float2 c = fma2(y, f2(1.0f / 24.0f), f2(1.0f / 6.0f));
     c = fma2(c, y, f2(0.5f));
-    const float2 em1 = fma2(mul2(c, y), y, y);
-    const float2 T0 = tab[j0 & 63], T1 = tab[j1 & 63];
-    const float2 Tx = make_float2(T0.x, T1.x), Ty = make_float2(T0.y, T1.y);
-    const float2 p = mul2(Tx, em1);
-    const float2 pe = fma2(Tx, em1, make_float2(-p.x, -p.y));
-    const float2 h = add2(Tx, p);
-    float2 lo = sub2(p, sub2(h, Tx));
-    lo = add2(lo, add2(pe, fma2(Ty, em1, Ty)));
-    const float2 sc = make_float2(__int_as_float(((j0 >> 6) + 127) << 23), __int_as_float(((j1 >> 6) + 127) << 23));
-    const float2 vh = mul2(h, sc), vl = mul2(lo, sc);
-    return ff2{make_float2(ok0 ? vh.x : 0.f, ok1 ? vh.y : 0.f), make_float2(ok0 ? vl.x : 0.f, ok1 ? vl.y : 0.f)};
+    const float2 em1 = fma2(mul2(c, y), y, y);  // e^y - 1
+    const uint32_t i0 = b0 & 63u, i1 = b1 & 63u;
+    const float2 Th = make_float2(tab[i0], tab[i1]), Tl = make_float2(tab[64 + i0], tab[64 + i1]);
+    // Th (1 + em1) + Tl (1 + em1) as h + lo: Th - h is exact, and the fused product-add recovers
+    // the rounding error of h
+    const float2 h = fma2(Th, em1, Th);
+    const float2 lo = add2(fma2(Th, em1, sub2(Th, h)), fma2(Tl, em1, Tl));
+    // 2^n, n = floor(j / 64), from j << 17 masked to the exponent field; n = -127 gives exactly 0
+    const float2 sc = make_float2(__uint_as_float(((b0 << 17) & 0xFF800000u) + 0x3F800000u),
+                                  __uint_as_float(((b1 << 17) & 0xFF800000u) + 0x3F800000u));
+    return ff2{mul2(h, sc), mul2(lo, sc)};
 }
+
+// Split of a weight w in [0, 1] into a part on the 2^-20 grid (hi) and the rest (lo, |lo| <= 2^-21):
+// sums of up to 16 grid parts are exact in float, so an accumulator only needs plain adds.
+__device__ __forceinline__ float2 grid_hi(float2 w) { return add2(add2(w, f2(12.f)), f2(-12.f)); }
 
 // ------------------------------------------------------------------------------------------------
 // Fast (MUFU) 2^x for the statistics pass: relative error about 2^-22, ex2(-inf) = 0.

@@ -12,43 +12,56 @@ namespace sv {
 constexpr int kThreads = 256;               // threads per CTA
 constexpr int kWarps = kThreads / 32;       // independent warp workers per CTA
 constexpr int kAChunk = 4096;               // vocabulary columns of one statistics task (one warp, one row)
-constexpr int kSub = 512;                   // sampler sub-chunk: the finest unit of the inverse-CDF search
-constexpr int kSubPerLane = kSub / 32;      // 16 consecutive columns per lane
-constexpr int kSTask = 1024;                // vocabulary columns of one sampler task (one warp)
-constexpr int kSubPerTask = kSTask / kSub;  // 2
+constexpr int kSTask = 1024;                // vocabulary columns of one sampler task (one warp): the unit
+                                            // of the inverse-CDF search's first level
+constexpr int kScanBlock = 512;             // columns the find's element scan covers per pass
+constexpr int kScanPerLane = kScanBlock / 32;  // 16 consecutive columns per lane
 constexpr int kStreamWarps = 4;             // statistics streamers per CTA on the bulk-copy path
 constexpr int kStages = 3;                  // bulk-copy stages per streamer
 constexpr int kStageBytes = kAChunk * 2;    // one bf16 statistics task
 constexpr int kTmaSmemBytes = kStreamWarps * kStages * (kStageBytes + 8);
-constexpr int kFlagStride = 32;             // ready flags one per 128-byte line (words)
 constexpr int kBaseCache = 1024;            // batches up to this size keep their row bases in shared memory
+constexpr int kRowCache = 2048;             // sampling batches with up to this many statistics rows keep a
+                                            // row map (target or draft, row index) in shared memory
 
 enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2 };
 
-// Partial statistics of one (row, chunk), one 64-bit word written with a single store. The region is
-// zeroed before every call and a written word is never 0, so readers poll the word itself:
+// Data handed between warps of one launch is written as 64-bit words, each exactly once per call with
+// one relaxed store, into a region zeroed before the call, and each non-zero once written. A reader
+// polls the words themselves (bounded back-off): no fence, flag or counter orders them.
+typedef unsigned long long Word;
+
+// Partial statistics of one (row, chunk):
 //   sampling: low = bits(raw max m), high = bits(sum of 2^((l - m) K)) (m = +0 implies sum >= 1;
 //             sum = 0 implies m = -inf; a NaN or +inf logit makes the sum NaN);
 //   greedy:   low = bits(m), high = (first argmax + 1) | (1 << 31 if a NaN was seen).
-typedef unsigned long long PartialWord;
+typedef Word PartialWord;
 
-// What the sampler draws for one sequence, written by the decision step. 48 bytes, 16-byte
-// aligned: readers fetch it with 16-byte loads.
-struct alignas(16) SeqTask {
-    int32_t mode;    // kMode*
-    int32_t n;       // emitting slot
-    int32_t prow;    // target row of the draw
-    int32_t qrow;    // draft row of the draw (residual), -1 otherwise
-    float m_p, m_q;  // raw-logit row maxima
-    float rho;       // approximate s_p / s_q: selects the tokens with p > q
-    int32_t out_pos; // index into out_tokens of the emitting slot
-    double u;        // uniform of the draw
-    int32_t pad[2];
-};
+// A sequence's sampler work, written by its decision as kTaskWords words:
+//   w0 = (0x80000000 | mode << 8 | n) << 32 | bits(m_p)   mode kMode*, n the emitting slot
+//   w1 = bits(rho) << 32 | bits(m_q)                      rho = approximate s_p / s_q (> 0)
+//   w2 = 0x80000000 << 32 | bits(u)                       u the draw's uniform
+// m_p, m_q are the raw-logit maxima of the draw's target and draft rows.
+constexpr int kTaskWords = 4;
+constexpr uint32_t kWordMark = 0x80000000u;
+
+// A sampler task's record, kRecWords words: word k = bits(lo) << 32 | (bits(hi) | 0x80000000) of a
+// non-negative float-float sum over the task's columns of the weights 2^((l - m) K):
+//   k = 0: all p weights, 1: all q weights, 2: p weights of the selected columns, 3: q weights of the
+//   selected columns (a bonus draw stores its p total as 0 and 2, zeros as 1 and 3).
+constexpr int kRecWords = 4;
+// Per group of kGroupLanes lanes of a sampler task (lane L covers the task's columns [32 L, 32 L + 32),
+// so group G covers [128 G, 128 G + 128)): two words, the group's selected p weights and selected q
+// weights (a bonus draw: its p weights and 0), packed like the record words. The find locates the
+// crossing group from them.
+constexpr int kGroupLanes = 4;
+constexpr int kGroups = 32 / kGroupLanes;            // 8 per task
+constexpr int kGroupCols = kSTask / kGroups;         // 128 columns
+constexpr int kGroupWords = 2;
 
 // Counters of one call (zeroed before the kernel by the launch sequence).
 struct Counters {
-    uint32_t claim;  // sampler tasks claimed, in sequence order
+    uint32_t claim;  // tickets claimed: the B decisions first, then the sampler tasks in sequence order
     uint32_t pad[31];
 };
 
@@ -60,11 +73,11 @@ struct Params {
     const int32_t* gammas;
     int32_t B, V, max_gamma;
     int32_t nchA;      // statistics chunks per row
-    int32_t nsub;      // sampler sub-chunks per row
     int32_t nS;        // sampler tasks per sequence
+    unsigned long long nS_recip;  // floor(2^64 / nS) + 1 (nS >= 2): c / nS = high 64 bits of c * nS_recip
     float K_hi, K_lo;  // log2(e) / T as float-float
-    double K64;        // log2(e) / T
-    double invT64;     // 1 / T
+    float d_min;       // clamp of l - m in the precise exponential (about -126.5 / K)
+    double invT64;     // 1 / T (debug output of the row log-normalisers only)
     uint64_t seed, step;
     int32_t* out_tokens;
     int32_t* out_n;
@@ -72,23 +85,23 @@ struct Params {
     sv_debug dbg;
     // workspace
     PartialWord* partials;  // [B * (2 max_gamma + 1) * nchA]
-    SeqTask* tasks;     // [B]
-    double2* subs;      // [B * nsub]: (sum_sel 2^{(l_p-m_p)K}, sum_sel 2^{(l_q-m_q)K}) per sub-chunk
-    double2* stot;      // [B * nS]: (sum_all p-weight, sum_all q-weight) per sampler task
+    Word* taskw;            // [B * kTaskWords]
+    Word* recw;             // [B * nS * kRecWords]
+    Word* groupw;           // [B * nS * kGroups * kGroupWords]
     Counters* ctr;
-    uint32_t* s_done;   // [B] sampler tasks finished per sequence
-    uint32_t* seq_ready;  // [B * kFlagStride] set (release) once a sequence's sampler task record is written
+    float2 exp2_tab[64];  // 2^(j/64), j = 0..63, as (hi, lo) floats, built on the host
 };
 
 struct Layout {
-    size_t counters, s_done, seq_ready, partials, tasks, subs, stot, status;
+    size_t counters, partials, taskw, recw, groupw, status;
     size_t zero_begin, zero_end;  // byte range the launch sequence clears
     size_t total;
 };
 
 Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma);
 
-// Enqueue the whole verify step on `stream`: one memset of the counters and one cooperative launch.
+// Enqueue the whole verify step on `stream`: one memset of the zeroed regions and one cooperative
+// launch.
 // dtype: SV_F32 / SV_BF16; vec: rows 16-byte aligned and V * elem_size a multiple of 16.
 cudaError_t launch_verify(const Params& P, const Layout& L, void* workspace, int dtype, bool vec, bool greedy,
                           cudaStream_t stream);

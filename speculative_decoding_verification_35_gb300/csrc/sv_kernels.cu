@@ -36,54 +36,29 @@
 
 namespace sv {
 
-constexpr uint32_t kSpinLimit = 1u << 21;  // polls before a wait gives up (about 1-4 s with back-off)
+constexpr uint32_t kSpinLimit = 1u << 21;  // polls before a wait gives up (about 1 s with back-off)
 
 // ------------------------------------------------------------------------------------------------
-// Memory-model helpers for data written by other warps during this launch (never through L1's
-// non-coherent path).
+// Words handed between warps during the launch (never read through L1's non-coherent path)
 // ------------------------------------------------------------------------------------------------
-// Relaxed polling loads (no acquire on every poll: an acquire load discards the SM's L1 contents,
-// which the other warps' cached data and spills would then miss). A poll that succeeds is followed by
-// one fence before the published data is read.
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// Relaxed 64-bit accesses to the words handed between warps (see Word): a word is written once per
+// call with one store and is single-copy atomic, so a reader sees either 0 or the final value.
+__device__ __forceinline__ Word ld_word(const Word* p) {
+    Word v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-// Lane 0 waits (bounded, exponential back-off) until *p >= target, then fences so the data published
-// before the flag is visible. Returns false on time-out (the status word gets SV_ERR_TIMEOUT).
-__device__ __forceinline__ bool wait_geq(const uint32_t* p, uint32_t target, uint32_t* status) {
-    uint32_t spins = 0, ns = 64;
-    while (*(const volatile uint32_t*)p < target) {
-        if (++spins > (1u << 21)) {
-            atomicOr(status, 1u << SV_ERR_TIMEOUT);
-            return false;
-        }
-        __nanosleep(ns);
-        ns = ns < 2048 ? 2 * ns : 2048;
-    }
-    __threadfence();
-    return true;
-}
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ PartialWord ld_word(const PartialWord* p) {
-    return *(const volatile PartialWord*)p;
-}
-__device__ __forceinline__ void st_word(PartialWord* p, PartialWord v) {
+__device__ __forceinline__ void st_word(Word* p, Word v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ SeqTask ld_task(const SeqTask* p) {
-    static_assert(sizeof(SeqTask) == 48 && alignof(SeqTask) == 16, "SeqTask layout");
-    const int4 a = __ldcg((const int4*)p);
-    const int4 c = __ldcg((const int4*)p + 1);
-    const double u = __ldcg((const double*)p + 4);
-    SeqTask t;
-    t.mode = a.x; t.n = a.y; t.prow = a.z; t.qrow = a.w;
-    t.m_p = __int_as_float(c.x); t.m_q = __int_as_float(c.y); t.rho = __int_as_float(c.z); t.out_pos = c.w;
-    t.u = u;
-    return t;
+__device__ __forceinline__ Word pack_words(uint32_t hi32, uint32_t lo32) { return ((Word)hi32 << 32) | lo32; }
+// a non-negative float-float value with the marker bit in its high part's sign
+__device__ __forceinline__ Word pack_ff(ff v) { return pack_words(__float_as_uint(v.lo), __float_as_uint(v.hi) | kWordMark); }
+__device__ __forceinline__ ff unpack_ff(Word w) {
+    return ff{__uint_as_float((uint32_t)w & 0x7FFFFFFFu), __uint_as_float((uint32_t)(w >> 32))};
+}
+__device__ __forceinline__ Word shfl_word(Word v, int src) {
+    return pack_words(__shfl_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), src), __shfl_sync(0xFFFFFFFFu, (uint32_t)v, src));
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -95,11 +70,6 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 __device__ __forceinline__ float warp_sumf(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-__device__ __forceinline__ double warp_sumd(double v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
     return v;
@@ -119,29 +89,36 @@ __device__ __forceinline__ int warp_max_i(int v) {
     for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
 }
-// float-float butterfly: every lane ends with the same total (the pairwise steps are symmetric)
-__device__ __forceinline__ double warp_sum_ff(ffacc a) {
-    float hi = a.hi, lo = a.lo;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        const float oh = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
-        const float ol = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
-        float s, e;
-        two_sum(hi, oh, s, e);
-        hi = s;
-        lo = __fadd_rn(__fadd_rn(lo, ol), e);
-    }
-    return (double)hi + (double)lo;
+// A lane's grid-split accumulator pair (two streams each) as one normalised float-float value; the two
+// grid parts are combined by TwoSum, so nothing is lost when their sum leaves the grid's exact range.
+__device__ __forceinline__ ff lane_ff(float2 h, float2 l) {
+    float s, e;
+    two_sum(h.x, h.y, s, e);
+    return ff_norm(s, __fadd_rn(e, __fadd_rn(l.x, l.y)));
 }
-// Exclusive prefix over the warp (fp64).
-__device__ __forceinline__ double warp_exscan(double v, int lane) {
-    double incl = v;
+// float-float butterfly: every lane ends with the same total (ff_add is symmetric in its operands)
+__device__ __forceinline__ ff warp_sum_ff(ff a) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        a = ff_add(a, ff{__shfl_xor_sync(0xFFFFFFFFu, a.hi, o), __shfl_xor_sync(0xFFFFFFFFu, a.lo, o)});
+    return a;
+}
+// Inclusive float-float prefix over the warp.
+__device__ __forceinline__ ff warp_inscan_ff(ff v, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
+        const ff y{__shfl_up_sync(0xFFFFFFFFu, v.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.lo, o)};
+        if (lane >= o) v = ff_add(y, v);
     }
-    return incl - v;
+    return v;
+}
+__device__ __forceinline__ ff shfl_ff(ff v, int src) {
+    return ff{__shfl_sync(0xFFFFFFFFu, v.hi, src), __shfl_sync(0xFFFFFFFFu, v.lo, src)};
+}
+// exclusive prefix from an inclusive one (lane 0 gets 0)
+__device__ __forceinline__ ff exclusive_of(ff incl, int lane) {
+    const ff y{__shfl_up_sync(0xFFFFFFFFu, incl.hi, 1), __shfl_up_sync(0xFFFFFFFFu, incl.lo, 1)};
+    return lane ? y : ff{0.f, 0.f};
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -162,14 +139,15 @@ __device__ __forceinline__ float logit_at(const void* base, size_t idx) {
     return __ldg((const float*)base + idx);
 }
 
-// Table of 2^(j/64), j = 0..63, as float-float, from the fp64 exp2 of the CUDA math library.
-__device__ __forceinline__ void fill_exp2_table(float2* tab) {
+// Shared-memory copy of the table of 2^(j/64), j = 0..63 (built on the host): high parts in
+// tab[0..63], low parts in tab[64..127].
+__device__ __forceinline__ void fill_exp2_table(const Params& P, float* tab) {
     if (threadIdx.x < 64) {
-        const double v = exp2((double)threadIdx.x * (1.0 / 64.0));
-        const float hi = (float)v;
-        tab[threadIdx.x] = make_float2(hi, (float)(v - (double)hi));
+        tab[threadIdx.x] = P.exp2_tab[threadIdx.x].x;
+        tab[64 + threadIdx.x] = P.exp2_tab[threadIdx.x].y;
     }
 }
+__device__ __forceinline__ ExpConst exp_const(const Params& P) { return ExpConst{P.K_hi, P.K_lo, -P.K_hi, P.d_min}; }
 
 // ------------------------------------------------------------------------------------------------
 // Statistics of one row segment [0, len) of up to 4096 columns, one warp. Result on every lane:
@@ -182,11 +160,14 @@ struct SegStats {
     uint32_t bad;
 };
 
-// Merge two partial (m, s) pairs of the same row (online softmax rescaling in fp32).
+// Merge two partial (m, s) pairs of the same row (online softmax rescaling in fp32). FMA_EXP: 2^x on the
+// FMA pipe (critical-path warps) instead of the MUFU.
+template <bool FMA_EXP = false>
 __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float K) {
     const float M = fmaxf(m, m2);
     if (M == -INFINITY) return;
-    s = (m == -INFINITY ? 0.f : s * ex2_approx((m - M) * K)) + (m2 == -INFINITY ? 0.f : s2 * ex2_approx((m2 - M) * K));
+    auto e2 = [](float x) { return FMA_EXP ? exp2_fma(x) : ex2_approx(x); };
+    s = (m == -INFINITY ? 0.f : s * e2((m - M) * K)) + (m2 == -INFINITY ? 0.f : s2 * e2((m2 - M) * K));
     m = M;
 }
 
@@ -348,19 +329,78 @@ __device__ __forceinline__ SegStats seg_stats(const char* rowp, int len, int lan
 }
 
 // ------------------------------------------------------------------------------------------------
+// Sampler work of a sequence (see kTaskWords)
+// ------------------------------------------------------------------------------------------------
+struct TaskInfo {
+    int32_t mode, n;
+    float m_p, m_q, rho, u;
+};
+
+// Written by the decision (lanes 0-2 store one word each).
+__device__ __forceinline__ void put_task(const Params& P, int32_t b, int lane, int32_t mode, int32_t n, float m_p,
+                                         float m_q, float rho, float u) {
+    Word w = 0;
+    if (lane == 0) w = pack_words(kWordMark | (uint32_t)mode << 8 | (uint32_t)n, __float_as_uint(m_p));
+    if (lane == 1) w = pack_words(__float_as_uint(rho), __float_as_uint(m_q));
+    if (lane == 2) w = pack_words(kWordMark, __float_as_uint(u));
+    if (lane < 3) st_word(P.taskw + (size_t)b * kTaskWords + lane, w);
+}
+
+// Read by each sampler task: lanes 0-2 poll one word each (bounded back-off). False on time-out.
+__device__ __forceinline__ bool get_task(const Params& P, int32_t b, int lane, TaskInfo& t) {
+    const Word* w = P.taskw + (size_t)b * kTaskWords;
+    Word v = lane < 3 ? ld_word(w + lane) : 1ull;
+    uint32_t spins = 0, ns = 32;
+    while (__any_sync(0xFFFFFFFFu, v == 0)) {
+        if (++spins > kSpinLimit) {
+            if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(ns);
+        ns = ns < 256 ? 2 * ns : 256;
+        if (v == 0) v = ld_word(w + lane);
+    }
+    const Word w0 = shfl_word(v, 0), w1 = shfl_word(v, 1), w2 = shfl_word(v, 2);
+    t.mode = (int32_t)((w0 >> 40) & 0xFF);
+    t.n = (int32_t)((w0 >> 32) & 0xFF);
+    t.m_p = __uint_as_float((uint32_t)w0);
+    t.m_q = __uint_as_float((uint32_t)w1);
+    t.rho = __uint_as_float((uint32_t)(w1 >> 32));
+    t.u = __uint_as_float((uint32_t)w2);
+    return true;
+}
+
+// ------------------------------------------------------------------------------------------------
 // Decision for sequence b (one warp): merge partials, accept tests, first rejection, outputs.
+// Everything that does not depend on the statistics (the draft tokens, the two logits at each token,
+// both uniforms of every slot) is fetched before the partials are polled. Rows are reduced 8 at a
+// time without control flow between them, so their shuffle trees overlap.
 // ------------------------------------------------------------------------------------------------
 template <int DT, bool GREEDY>
-__device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float2* tab) {
+__device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float* tab) {
     const int32_t t0 = o0 + b;
     const int nrows = stat_rows<GREEDY>(g);
     const int32_t sbase = stat_base<GREEDY>(P, b);
     const int nch = P.nchA;
     const float K = P.K_hi;
-    float my_m[2] = {-INFINITY, -INFINITY};
-    float my_s[2] = {0.f, 0.f};
-    int my_a[2] = {-1, -1};
+    int32_t x = 0;
     uint32_t err = 0;
+    float lt = 0.f, ld = 0.f, u_acc = 0.f, u_draw = 0.f;
+    if (lane < g) {
+        x = __ldg(P.tokens + o0 + lane);
+        if (x < 0 || x >= P.V) err |= 1u << SV_ERR_BAD_TOKEN;
+        else if (!GREEDY) {
+            lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
+            ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
+        }
+    }
+    if (!GREEDY) {
+        if (lane < g) u_acc = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);
+        if (lane <= g) u_draw = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 1);
+    }
+    // row statistics: row jr's (max, sum) or (max, argmax) ends on lane jr & 31, register jr >> 5
+    float my_m0 = -INFINITY, my_m1 = -INFINITY, my_s0 = 0.f, my_s1 = 0.f;
+    int my_a0 = -1;
     for (int j0 = 0; j0 < nrows; j0 += 8) {
         // lanes over chunks, 8 rows per batch with their loads in flight together
         float lm[8], ls[8];
@@ -371,88 +411,104 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         for (int c0 = 0; c0 < nch; c0 += 32) {
             const int c = c0 + lane;
             PartialWord q[8];
+            bool v[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                q[k] = (j0 + k < nrows && c < nch) ? ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c) : 1ull;
+            for (int k = 0; k < 8; ++k) {
+                v[k] = j0 + k < nrows && c < nch;
+                q[k] = v[k] ? ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c) : 1ull;
+            }
             // words still 0 are statistics tasks in flight: poll them (bounded back-off)
             uint32_t spins = 0, ns = 64;
             while (__any_sync(0xFFFFFFFFu, q[0] == 0 || q[1] == 0 || q[2] == 0 || q[3] == 0 || q[4] == 0 ||
                                                q[5] == 0 || q[6] == 0 || q[7] == 0)) {
-                if (++spins > (1u << 21)) {
+                if (++spins > kSpinLimit) {
                     if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
                     err |= 1u << SV_ERR_TIMEOUT;
                     break;
                 }
                 __nanosleep(ns);
-                ns = ns < 2048 ? 2 * ns : 2048;
+                ns = ns < 256 ? 2 * ns : 256;
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     if (q[k] == 0) q[k] = ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c);
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                if (j0 + k >= nrows || c >= nch) continue;
-                const float qm = __uint_as_float((uint32_t)q[k]);
+                const float qm = v[k] ? __uint_as_float((uint32_t)q[k]) : -INFINITY;
                 const uint32_t qh = (uint32_t)(q[k] >> 32);
                 if (GREEDY) {
-                    if (qh >> 31) lf[k] |= 1u << SV_ERR_NONFINITE;
-                    if (qm > lm[k]) { lm[k] = qm; la[k] = (int)(qh & 0x7FFFFFFFu) - 1; }
+                    lf[k] |= v[k] && (qh >> 31) ? 1u << SV_ERR_NONFINITE : 0u;
+                    const bool take = qm > lm[k];
+                    la[k] = take ? (int)(qh & 0x7FFFFFFFu) - 1 : la[k];
+                    lm[k] = take ? qm : lm[k];
                 } else {
-                    const float qs = __uint_as_float(qh);
-                    if (qs != qs) {
+                    const float qs = v[k] ? __uint_as_float(qh) : 0.f;
+                    if (c0 == 0) {  // first chunk of the lane: nothing to merge with
+                        lm[k] = qm;
+                        ls[k] = qs;
+                    } else if (qs != qs) {
                         ls[k] = qs;
                         lm[k] = fmaxf(lm[k], qm);
                     } else if (ls[k] == ls[k]) {
-                        merge_ms(lm[k], ls[k], qm, qs, K);
+                        merge_ms<true>(lm[k], ls[k], qm, qs, K);
                     }
                 }
             }
         }
+        // the 8 rows' lane reductions, interleaved
+        float M[8], S[8];
+        int A[8];
+        uint32_t F[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) M[k] = lm[k];
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) M[k] = fmaxf(M[k], __shfl_xor_sync(0xFFFFFFFFu, M[k], o));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (GREEDY) {
+                A[k] = lm[k] == M[k] ? la[k] : 0x7FFFFFFF;
+                F[k] = lf[k];
+            } else {
+                S[k] = ls[k] != ls[k] ? ls[k] : (lm[k] == -INFINITY ? 0.f : ls[k] * exp2_fma((lm[k] - M[k]) * K));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (GREEDY) {
+                    A[k] = min(A[k], __shfl_xor_sync(0xFFFFFFFFu, A[k], o));
+                    F[k] |= __shfl_xor_sync(0xFFFFFFFFu, F[k], o);
+                } else {
+                    S[k] += __shfl_xor_sync(0xFFFFFFFFu, S[k], o);
+                }
+            }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int jr = j0 + k;
-            if (jr >= nrows) break;
-            const float M = warp_max(lm[k]);
-            float v = 0.f;
-            int a = 0x7FFFFFFF;
-            if (GREEDY) {
-                a = warp_min_i(lm[k] == M ? la[k] : 0x7FFFFFFF);
-            } else {
-                v = ls[k] != ls[k] ? ls[k] : (lm[k] == -INFINITY ? 0.f : ls[k] * ex2_approx((lm[k] - M) * K));
-                v = warp_sumf(v);
-            }
+            const bool in = jr < nrows;
             // a row with a NaN or +inf is reported as such, not as empty (both fail the sequence)
-            const uint32_t rf = warp_or(lf[k]) | (v != v ? 1u << SV_ERR_NONFINITE : 0u);
-            err |= rf;
-            if (M == -INFINITY && !rf) err |= 1u << SV_ERR_EMPTY_ROW;
-            if (lane == (jr & 31)) {
-                my_m[jr >> 5] = M;
-                my_s[jr >> 5] = v;
-                my_a[jr >> 5] = a;
-            }
+            const uint32_t rf = GREEDY ? (F[k] | (M[k] == INFINITY ? 1u << SV_ERR_NONFINITE : 0u))
+                                       : (S[k] != S[k] ? 1u << SV_ERR_NONFINITE : 0u);
+            if (in) err |= rf | (M[k] == -INFINITY && !rf ? 1u << SV_ERR_EMPTY_ROW : 0u);
+            if (in && lane == jr) { my_m0 = M[k]; my_s0 = GREEDY ? 0.f : S[k]; my_a0 = GREEDY ? A[k] : -1; }
+            if (in && lane == jr - 32) { my_m1 = M[k]; my_s1 = GREEDY ? 0.f : S[k]; }
         }
-    }
-    int32_t x = 0;
-    if (lane < g) {
-        x = __ldg(P.tokens + o0 + lane);
-        if (x < 0 || x >= P.V) err |= 1u << SV_ERR_BAD_TOKEN;
     }
     err = warp_or(err);
     if (err) {
         if (lane == 0) {
             atomicOr(P.status, err);
             P.out_n[b] = -1;
-            if (!GREEDY) {
-                SeqTask tk{};
-                tk.mode = kModeNone;
-                P.tasks[b] = tk;
-            }
         }
+        if (!GREEDY) put_task(P, b, lane, kModeNone, 0, 0.f, 0.f, 1.f, 0.f);
         for (int32_t j = lane; j <= g; j += 32) P.out_tokens[t0 + j] = -1;
         return;
     }
     if (GREEDY) {
-        const int a = my_a[0];  // argmax of target row `lane` (lane <= g <= 31)
+        const int a = my_a0;  // argmax of target row `lane` (lane <= g <= 31)
         if (lane <= g && P.dbg.row_argmax) P.dbg.row_argmax[t0 + lane] = a;
         const uint32_t mism = __ballot_sync(0xFFFFFFFFu, lane < g && x != a);
         const int n = mism ? __ffs(mism) - 1 : g;
@@ -462,19 +518,16 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     }
     // the draft row of slot `lane` is statistics row g + 1 + lane: lane (g+1+lane) & 31, register >> 5
     const int jd = g + 1 + lane;
-    const float dm0 = __shfl_sync(0xFFFFFFFFu, my_m[0], jd & 31), dm1 = __shfl_sync(0xFFFFFFFFu, my_m[1], jd & 31);
-    const float ds0 = __shfl_sync(0xFFFFFFFFu, my_s[0], jd & 31), ds1 = __shfl_sync(0xFFFFFFFFu, my_s[1], jd & 31);
+    const float dm0 = __shfl_sync(0xFFFFFFFFu, my_m0, jd & 31), dm1 = __shfl_sync(0xFFFFFFFFu, my_m1, jd & 31);
+    const float ds0 = __shfl_sync(0xFFFFFFFFu, my_s0, jd & 31), ds1 = __shfl_sync(0xFFFFFFFFu, my_s1, jd & 31);
     const float dm = (jd >> 5) ? dm1 : dm0, ds = (jd >> 5) ? ds1 : ds0;
     bool acc = true;
     if (lane < g) {
         // p(x) and q(x) from the precise exponential of the exact logit gaps, over the fp32 normalisers
-        const float lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
-        const float ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
-        const ff2 e = exp2_ff2(make_float2(lt, ld), make_float2(my_m[0], dm), P.K_hi, P.K_lo, tab);
-        const float px = __fdiv_rn(e.hi.x + e.lo.x, my_s[0]);
-        const float qx = __fdiv_rn(e.hi.y + e.lo.y, ds);
-        const float u = (float)philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);  // exact
-        acc = u * qx < px;
+        const ff2 e = exp2_ff2<DT == SV_BF16>(make_float2(lt, ld), make_float2(my_m0, dm), exp_const(P), tab);
+        const float px = div_fma(e.hi.x + e.lo.x, my_s0);
+        const float qx = div_fma(e.hi.y + e.lo.y, ds);
+        acc = u_acc * qx < px;
         if (P.dbg.p_x) P.dbg.p_x[o0 + lane] = (double)px;
         if (P.dbg.q_x) P.dbg.q_x[o0 + lane] = (double)qx;
     }
@@ -484,7 +537,8 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         for (int h = 0; h < 2; ++h) {
             const int jr = lane + 32 * h;
             if (jr < nrows) {
-                const double lse = (double)my_m[h] * P.invT64 + log((double)my_s[h]);
+                const float m = h ? my_m1 : my_m0, sum = h ? my_s1 : my_s0;
+                const double lse = (double)m * P.invT64 + log((double)sum);
                 P.dbg.row_lse[jr <= g ? t0 + jr : R_t + o0 + (jr - g - 1)] = lse;
             }
         }
@@ -493,28 +547,12 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     const int n = rej ? __ffs(rej) - 1 : g;
     if (lane <= g && lane != n) P.out_tokens[t0 + lane] = lane < n ? x : -1;
     // statistics of the emitting slot's rows
-    const float pm = __shfl_sync(0xFFFFFFFFu, my_m[0], n), ps = __shfl_sync(0xFFFFFFFFu, my_s[0], n);
+    const float pm = __shfl_sync(0xFFFFFFFFu, my_m0, n), ps = __shfl_sync(0xFFFFFFFFu, my_s0, n);
     const float qm = __shfl_sync(0xFFFFFFFFu, dm, n), qs = __shfl_sync(0xFFFFFFFFu, ds, n);
-    if (lane == 0) {
-        SeqTask tk;
-        tk.mode = n < g ? kModeResidual : kModeBonus;
-        tk.n = n;
-        tk.prow = t0 + n;
-        tk.qrow = n < g ? o0 + n : -1;
-        tk.m_p = pm;
-        tk.m_q = n < g ? qm : 0.f;
-        tk.rho = n < g ? (float)((double)ps / (double)qs) : 1.f;
-        tk.out_pos = t0 + n;
-        tk.u = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)n, 1);
-        P.tasks[b] = tk;
-        P.out_n[b] = n;
-    }
-}
-
-// Publish sequence b's sampler work: lane 0 wrote the task record, and its release store orders that
-// write before the flag.
-__device__ __forceinline__ void publish(const Params& P, int32_t b, int lane) {
-    if (lane == 0) st_release(P.seq_ready + (size_t)b * kFlagStride, 1u);
+    const float un = __shfl_sync(0xFFFFFFFFu, u_draw, n);
+    put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, pm, n < g ? qm : 0.f,
+             n < g ? div_fma(ps, qs) : 1.f, un);
+    if (lane == 0) P.out_n[b] = n;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -579,160 +617,334 @@ __device__ __forceinline__ float2 sel_mask(const ff2& ep, const ff2& eq, float r
     return make_float2(ep.hi.x > rho * eq.hi.x ? 1.f : 0.f, ep.hi.y > rho * eq.hi.y ? 1.f : 0.f);
 }
 
-// Inverse-CDF search over the columns [k_lo, k_hi) for the remaining target `rem`, in blocks of 512
-// columns with fp64 running sums. Returns the token, or the last column of positive weight when the
-// crossing is lost to rounding (or `tail_rule` asks for exactly that).
+// Residual weight of a selected column, max(0, e_p - rho e_q) in float-float; 0 when not selected.
+__device__ __forceinline__ ff resid_weight(float hp, float lp, float hq, float lq, float sel, ff rho) {
+    if (sel == 0.f) return ff{0.f, 0.f};
+    const ff w = ff_sub(ff_norm(hp, lp), ff_mul(rho, ff_norm(hq, lq)));
+    return w.hi > 0.f ? w : ff{0.f, 0.f};
+}
+
+// Weight of one column in the find's element search: the precise p weight, or the residual weight of
+// a selected column (float-float); 0 at or past k_hi.
+template <int DT, bool EXACT_D>
+__device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& tk, const ExpConst& EC, bool resid,
+                                            ff rho, const float* tab) {
+    const ff2 e = exp2_ff2<EXACT_D>(make_float2(lp, lq), make_float2(tk.m_p, tk.m_q), EC, tab);
+    if (!resid) return ff_norm(e.hi.x, e.lo.x);
+    const bool sel = e.hi.x > tk.rho * e.hi.y;  // the selection rule of sel_mask
+    return resid_weight(e.hi.x, e.lo.x, e.hi.y, e.lo.y, sel ? 1.f : 0.f, rho);
+}
+
+// Inverse-CDF search over the columns [k_lo, k_hi) for the remaining target `rem`, kScanBlock columns
+// per pass (16 consecutive columns per lane, float-float). Each lane keeps only its total; once the
+// crossing lane is known, 16 lanes recompute its columns in parallel (their data are L1-resident) and
+// a 16-lane prefix picks the column. Returns the first column whose running sum exceeds `rem`, or the
+// last column of positive weight when the crossing is lost to rounding (or `tail_rule` asks for it).
 template <int DT, bool VEC>
-__device__ int32_t scan_elements(const Params& P, const SeqTask& tk, bool resid, double rho, int32_t k_lo,
-                                 int32_t k_hi, double rem, bool tail_rule, const float2* tab, int lane) {
-    int32_t last_pos = -1;
-    for (int32_t base = k_lo; base < k_hi; base += kSub) {
-        const int32_t k0 = base + lane * kSubPerLane;
-        const Cols16 cp = load_cols16<DT, VEC>(P.target, (size_t)tk.prow, P.V, k0);
-        Cols16 cq;
-        if (resid) cq = load_cols16<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, k0);
-        double w[16];
-        double tot = 0.0;
+__device__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t prow, size_t qrow, bool resid, ff rho,
+                                 int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, const float* tab, int lane) {
+    const ExpConst EC = exp_const(P);
+    constexpr bool kExact = DT == SV_BF16;
+    // a unit spans at most kSTask columns: NB passes; bf16 issues every pass's loads first
+    constexpr int NB = kSTask / kScanBlock;
+    constexpr bool kAhead = DT == SV_BF16;
+    Cols16 cpa[kAhead ? NB : 1], cqa[kAhead ? NB : 1];
+    if (kAhead) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const ff2 ep = exp2_ff2(col2<DT>(cp, e), f2(tk.m_p), P.K_hi, P.K_lo, tab);
-            double w0 = (double)ep.hi.x + (double)ep.lo.x, w1 = (double)ep.hi.y + (double)ep.lo.y;
-            if (resid) {
-                const ff2 eq = exp2_ff2(col2<DT>(cq, e), f2(tk.m_q), P.K_hi, P.K_lo, tab);
-                const float2 mk = sel_mask(ep, eq, tk.rho);
-                w0 = mk.x != 0.f ? fmax(0.0, w0 - rho * ((double)eq.hi.x + (double)eq.lo.x)) : 0.0;
-                w1 = mk.y != 0.f ? fmax(0.0, w1 - rho * ((double)eq.hi.y + (double)eq.lo.y)) : 0.0;
-            }
-            if (k0 + 2 * e >= k_hi) w0 = 0.0;
-            if (k0 + 2 * e + 1 >= k_hi) w1 = 0.0;
-            w[2 * e] = w0;
-            w[2 * e + 1] = w1;
-            tot += w0 + w1;
+        for (int nb = 0; nb < (kAhead ? NB : 1); ++nb) {
+            const int32_t k0 = k_lo + nb * kScanBlock + lane * kScanPerLane;
+            cpa[nb] = load_cols16<DT, VEC>(P.target, prow, P.V, k0);
+            if (resid) cqa[nb] = load_cols16<DT, VEC>(P.draft, qrow, P.V, k0);
         }
+    }
+    int32_t last_pos = -1;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+        const int32_t base = k_lo + nb * kScanBlock;
+        if (base >= k_hi) break;
+        const int32_t k0 = base + lane * kScanPerLane;
+        Cols16 cp, cq;
+        if (kAhead) {
+            cp = cpa[kAhead ? nb : 0];
+            cq = cqa[kAhead ? nb : 0];
+        } else {
+            cp = load_cols16<DT, VEC>(P.target, prow, P.V, k0);
+            if (resid) cq = load_cols16<DT, VEC>(P.draft, qrow, P.V, k0);
+        }
+        ff tot{0.f, 0.f};
         int lastp = -1;
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-            if (w[e] > 0.0) lastp = k0 + e;
+        for (int e = 0; e < 8; ++e) {
+            const float2 lpv = col2<DT>(cp, e), lqv = resid ? col2<DT>(cq, e) : f2(0.f);
+            const ff w0 = column_weight<DT, kExact>(lpv.x, lqv.x, tk, EC, resid, rho, tab);
+            const ff w1 = column_weight<DT, kExact>(lpv.y, lqv.y, tk, EC, resid, rho, tab);
+            if (k0 + 2 * e < k_hi && w0.hi > 0.f) {
+                tot = ff_add(tot, w0);
+                lastp = k0 + 2 * e;
+            }
+            if (k0 + 2 * e + 1 < k_hi && w1.hi > 0.f) {
+                tot = ff_add(tot, w1);
+                lastp = k0 + 2 * e + 1;
+            }
+        }
         lastp = warp_max_i(lastp);
         if (lastp >= 0) last_pos = lastp;
-        const double lpre = warp_exscan(tot, lane);
-        const double btot = __shfl_sync(0xFFFFFFFFu, lpre + tot, 31);
-        if (!tail_rule && btot > rem) {
-            int my_k = -1;
-            if (lpre + tot > rem) {
-                double c = lpre;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    if (my_k < 0 && w[e] > 0.0 && c + w[e] > rem) my_k = k0 + e;
-                    c += w[e];
-                }
+        const ff incl = warp_inscan_ff(tot, lane);
+        const ff btot = shfl_ff(incl, 31);
+        if (!tail_rule && ff_gt(btot, rem)) {
+            // the first lane whose inclusive prefix exceeds rem holds the crossing column
+            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, ff_gt(incl, rem));
+            const int L = __ffs(hit) - 1;
+            const ff pre = shfl_ff(exclusive_of(incl, lane), L);
+            // lanes j < 16 take column kL + j of lane L
+            const int32_t kL = base + L * kScanPerLane, kj = kL + (lane & 15);
+            ff w{0.f, 0.f};
+            if (lane < kScanPerLane && kj < k_hi) {
+                const float lpj = logit_at<DT>(P.target, prow * (size_t)P.V + kj);
+                const float lqj = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + kj) : 0.f;
+                w = column_weight<DT, kExact>(lpj, lqj, tk, EC, resid, rho, tab);
+                if (!(w.hi > 0.f)) w = ff{0.f, 0.f};
             }
-            const uint32_t hit = __ballot_sync(0xFFFFFFFFu, my_k >= 0);
-            if (hit) return __shfl_sync(0xFFFFFFFFu, my_k, __ffs(hit) - 1);
-            return last_pos;
+            const ff c = ff_add(pre, warp_inscan_ff(w, lane));  // lanes >= 16 add zeros
+            const uint32_t cross = __ballot_sync(0xFFFFFFFFu, lane < kScanPerLane && w.hi > 0.f && ff_gt(c, rem));
+            if (cross) return kL + __ffs(cross) - 1;
+            // the lane's sum crossed, its running sum fell short by rounding: its last positive column
+            const uint32_t pos = __ballot_sync(0xFFFFFFFFu, lane < kScanPerLane && w.hi > 0.f);
+            return pos ? kL + 31 - __clz(pos) : last_pos;
         }
-        rem -= btot;
+        rem = ff_sub(rem, btot);
     }
     return last_pos;
 }
 
-// Find for sequence b (one warp): normalisers, sub-chunk search, element search, output.
+// Element level of the find for the residual (or bonus) weights, inside sampler task `unit`: the
+// crossing group from the groups' selected sums (polled until written), then the crossing column among
+// that group's kGroupCols columns, 4 consecutive ones recomputed per lane. `rem` is the target left
+// after the tasks before. Rounding that loses the crossing (or tail_rule) picks the last group, then
+// column, of positive weight. Returns -1 when nothing in the task has positive weight, -2 on a time-out.
 template <int DT, bool VEC>
-__device__ __noinline__ void find(const Params& P, int32_t b, const float2* tab, int lane) {
-    const SeqTask tk = ld_task(P.tasks + b);
-    if (tk.mode == kModeNone) return;
-    const double2* ss = P.subs + (size_t)b * P.nsub;
-    const double2* st = P.stot + (size_t)b * P.nS;
-    const int nsub = P.nsub, nS = P.nS;
-    double sp = 0.0, sq = 0.0;
-    for (int i = lane; i < nS; i += 32) {
-        const double2 v = __ldcg(st + i);
-        sp += v.x;
-        sq += v.y;
-    }
-    sp = warp_sumd(sp);
-    sq = warp_sumd(sq);
-    bool resid = tk.mode == kModeResidual;
-    const double rho = resid ? sp / sq : 0.0;
-
-    // level 1: units (sub-chunks, or sampler tasks for the p-only fallback); lane owns [s0, s1)
-    int units = nsub;
-    bool by_task = false;
-    auto unit_w = [&](int i) -> double {
-        if (by_task) return __ldcg(st + i).x;
-        const double2 v = __ldcg(ss + i);
-        return resid ? v.x - rho * v.y : v.x;
-    };
-    // the loads of a lane's range are issued 8 at a time, not one dependent round trip each
-    auto range_sum = [&](int s0, int s1) -> double {
-        double sum = 0.0;
-        for (int i0 = s0; i0 < s1; i0 += 8) {
-            double v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = i0 + k < s1 ? unit_w(i0 + k) : 0.0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) sum += v[k];
+__device__ int32_t group_search(const Params& P, int32_t b, int unit, const TaskInfo& tk, size_t prow, size_t qrow,
+                                bool resid, ff rho, ff rem, bool tail_rule, const float* tab, int lane) {
+    static_assert(kGroupCols == 4 * 32, "four columns per lane");
+    const Word* gw = P.groupw + (((size_t)b * P.nS + unit) * kGroups + (lane % kGroups)) * kGroupWords;
+    Word wa = lane < kGroups ? ld_word(gw) : (Word)kWordMark, wb = lane < kGroups ? ld_word(gw + 1) : (Word)kWordMark;
+    uint32_t spins = 0, ns = 32;
+    while (__any_sync(0xFFFFFFFFu, wa == 0 || wb == 0)) {
+        if (++spins > kSpinLimit) {
+            if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+            return -2;
         }
-        return sum;
-    };
-    int per = (units + 31) / 32;
-    int s0 = min(units, lane * per), s1 = min(units, s0 + per);
-    double lsum = range_sum(s0, s1);
-    double S = warp_sumd(lsum);
-    if (resid && !(S > 0.0)) {  // residual mass 0 (only through rounding): draw from p
-        resid = false;
-        by_task = true;
-        units = nS;
-        per = (units + 31) / 32;
-        s0 = min(units, lane * per);
-        s1 = min(units, s0 + per);
-        lsum = range_sum(s0, s1);
-        S = warp_sumd(lsum);
+        __nanosleep(ns);
+        ns = ns < 256 ? 2 * ns : 256;
+        if (wa == 0) wa = ld_word(gw);
+        if (wb == 0) wb = ld_word(gw + 1);
     }
-    const double target = tk.u * S;
-    const double pre = warp_exscan(lsum, lane);
-    int unit = -1;
-    double before = 0.0;
-    {
-        int my_u = -1;
-        double my_before = 0.0;
-        if (pre + lsum > target) {
-            double c = pre;
-            for (int i0 = s0; i0 < s1 && my_u < 0; i0 += 8) {
-                double v[8];
+    ff w = unpack_ff(wa);
+    if (resid) w = ff_sub(w, ff_mul(rho, unpack_ff(wb)));
+    if (!(w.hi > 0.f)) w = ff{0.f, 0.f};
+    const ff incl = warp_inscan_ff(w, lane);
+    const uint32_t gpos = __ballot_sync(0xFFFFFFFFu, w.hi > 0.f);
+    if (!gpos) return -1;
+    const uint32_t hit = tail_rule ? 0u : __ballot_sync(0xFFFFFFFFu, ff_gt(incl, rem));
+    const int G = hit ? __ffs(hit) - 1 : 31 - __clz(gpos);
+    const ff pre = shfl_ff(exclusive_of(incl, lane), G);
+    // lane j: columns k0 + 4 j .. k0 + 4 j + 3 of the group
+    const ExpConst EC = exp_const(P);
+    const int32_t k0 = unit * kSTask + kGroupCols * G + 4 * lane;
+    ff cw[4];
+    ff tot{0.f, 0.f};
 #pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = i0 + k < s1 ? unit_w(i0 + k) : 0.0;
+    for (int e = 0; e < 4; ++e) {
+        const int32_t k = k0 + e;
+        cw[e] = ff{0.f, 0.f};
+        if (k < P.V) {
+            const float lpk = logit_at<DT>(P.target, prow * (size_t)P.V + k);
+            const float lqk = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + k) : 0.f;
+            cw[e] = column_weight<DT, DT == SV_BF16>(lpk, lqk, tk, EC, resid, rho, tab);
+            if (!(cw[e].hi > 0.f)) cw[e] = ff{0.f, 0.f};
+        }
+        tot = ff_add(tot, cw[e]);
+    }
+    const ff tin = warp_inscan_ff(tot, lane);
+    const ff cincl = ff_add(pre, tin), cexcl = ff_add(pre, exclusive_of(tin, lane));
+    const uint32_t lpos = __ballot_sync(0xFFFFFFFFu, tot.hi > 0.f);
+    const uint32_t cross = hit ? __ballot_sync(0xFFFFFFFFu, ff_gt(cincl, rem)) : 0u;
+    // the lane holding the crossing (or, failing that, the last lane of positive weight) picks the column
+    const int J = cross ? __ffs(cross) - 1 : (lpos ? 31 - __clz(lpos) : -1);
+    if (J < 0) return -1;
+    int32_t col = -1;
+    if (lane == J) {  // no collectives in here
+        ff c = cexcl;
+        int lastc = -1;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (my_u < 0 && v[k] > 0.0 && c + v[k] > target) { my_u = i0 + k; my_before = c; }
-                    c += v[k];
-                }
+        for (int e = 0; e < 4; ++e) {
+            if (cw[e].hi > 0.f) {
+                c = ff_add(c, cw[e]);
+                if (cross && col < 0 && ff_gt(c, rem)) col = k0 + e;
+                lastc = k0 + e;
             }
         }
-        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, my_u >= 0);
-        if (hit) {
-            const int L = __ffs(hit) - 1;
-            unit = __shfl_sync(0xFFFFFFFFu, my_u, L);
-            before = __shfl_sync(0xFFFFFFFFu, my_before, L);
-        }
+        if (col < 0) col = lastc;
     }
+    return __shfl_sync(0xFFFFFFFFu, col, J);
+}
+
+// Find for sequence b (one warp): run by the warp that holds the sequence's last sampler task, after
+// its own task. Exact normalisers from all task records (polled until written), the crossing task over
+// the records' weights, then the crossing column inside that task.
+template <int DT, bool VEC>
+__device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk, size_t prow, size_t qrow,
+                                  int32_t out_pos, const float* tab, int lane) {
+    const int nS = P.nS;
+    const Word* rec = P.recw + (size_t)b * nS * kRecWords;
+    // lane owns the run of tasks [s0, s1), read four tasks (16 words) at a time
+    const int per = (nS + 31) / 32;
+    const int s0 = min(nS, lane * per), s1 = min(nS, s0 + per);
+    // Warp-collective (every lane calls it the same number of times): polls the words of tasks
+    // i0 .. i0 + 3 until written (false on time-out), adds their sums to the lane's and returns each
+    // task's selected sums.
+    auto poll4 = [&](int i0, ff& lp, ff& lq, ff& la, ff& lb, ff (&va)[4], ff (&vb)[4]) -> bool {
+        Word w[4][kRecWords];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int j = 0; j < kRecWords; ++j)
+                w[k][j] = i0 + k < s1 ? ld_word(rec + (size_t)(i0 + k) * kRecWords + j) : (Word)kWordMark;
+        uint32_t spins = 0, ns = 32;
+        while (true) {
+            bool missing = false;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int j = 0; j < kRecWords; ++j) missing |= w[k][j] == 0;
+            if (!__any_sync(0xFFFFFFFFu, missing)) break;
+            if (++spins > kSpinLimit) {
+                if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+                return false;
+            }
+            __nanosleep(ns);
+            ns = ns < 256 ? 2 * ns : 256;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int j = 0; j < kRecWords; ++j)
+                    if (w[k][j] == 0) w[k][j] = ld_word(rec + (size_t)(i0 + k) * kRecWords + j);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            va[k] = unpack_ff(w[k][2]);
+            vb[k] = unpack_ff(w[k][3]);
+            lp = ff_add(lp, unpack_ff(w[k][0]));
+            lq = ff_add(lq, unpack_ff(w[k][1]));
+            la = ff_add(la, va[k]);
+            lb = ff_add(lb, vb[k]);
+        }
+        return true;
+    };
+    // Per lane, no collective: task i's p total and selected sums, once every record is known written.
+    auto read1 = [&](int i, ff& vp, ff& va, ff& vb) {
+        const Word* r = rec + (size_t)i * kRecWords;
+        vp = unpack_ff(ld_word(r));
+        va = unpack_ff(ld_word(r + 2));
+        vb = unpack_ff(ld_word(r + 3));
+    };
+    ff lp{0.f, 0.f}, lq{0.f, 0.f}, la{0.f, 0.f}, lb{0.f, 0.f};
+    ff ka[4], kb[4];  // the lane's first four tasks, kept for the crossing search
+    const int nchunk = (per + 3) / 4;  // the same on every lane
+    if (!__all_sync(0xFFFFFFFFu, poll4(s0, lp, lq, la, lb, ka, kb))) return;
+    for (int q = 1; q < nchunk; ++q) {
+        ff va[4], vb[4];
+        if (!__all_sync(0xFFFFFFFFu, poll4(s0 + 4 * q, lp, lq, la, lb, va, vb))) return;
+    }
+    const ff sp = warp_sum_ff(lp);
+    bool resid = tk.mode == kModeResidual;
+    ff rho{0.f, 0.f};
+    ff W = la;  // the lane's weight: p mass (bonus) or A - rho B (residual)
+    if (resid) {
+        rho = ff_div(sp, warp_sum_ff(lq));  // exact s_p / s_q
+        W = ff_sub(la, ff_mul(rho, lb));
+    }
+    ff incl = warp_inscan_ff(W, lane);
+    ff S = shfl_ff(incl, 31);
+    bool by_p = false;
+    if (resid && !(S.hi > 0.f)) {  // residual mass 0 (only through rounding): draw from p
+        resid = false;
+        by_p = true;
+        W = lp;
+        incl = warp_inscan_ff(W, lane);
+        S = shfl_ff(incl, 31);
+    }
+    const ff target = ff_mul(ff{tk.u, 0.f}, S);
+    // the first lane whose inclusive prefix exceeds the target searches its own run of tasks
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, ff_gt(incl, target));
+    const ff pre = exclusive_of(incl, lane);
+    auto unit_w = [&](const ff& vp, const ff& va, const ff& vb) {
+        ff w = by_p ? vp : va;
+        if (resid) w = ff_sub(w, ff_mul(rho, vb));
+        return w;
+    };
+    int unit = -1;
+    ff before{0.f, 0.f};
     bool tail_rule = false;
-    if (unit < 0) {  // rounding left no crossing: the last unit with positive weight
+    if (hit) {
+        const int L = __ffs(hit) - 1;
+        if (lane == L) {  // no collectives in here
+            ff c = pre;
+            int lastu = -1;
+            ff lastc{0.f, 0.f};
+            for (int i = s0; i < s1 && unit < 0; ++i) {
+                ff vp{0.f, 0.f}, va{0.f, 0.f}, vb{0.f, 0.f};
+                if (i - s0 < 4 && !by_p) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (i - s0 == k) { va = ka[k]; vb = kb[k]; }
+                } else {
+                    read1(i, vp, va, vb);
+                }
+                const ff w = unit_w(vp, va, vb);
+                if (w.hi > 0.f) {
+                    const ff c2 = ff_add(c, w);
+                    if (ff_gt(c2, target)) {
+                        unit = i;
+                        before = c;
+                    }
+                    lastu = i;
+                    lastc = c;
+                    c = c2;
+                }
+            }
+            if (unit < 0) {  // the lane's sum crossed, its running sum fell short by rounding
+                unit = lastu;
+                before = lastc;
+            }
+        }
+        unit = __shfl_sync(0xFFFFFFFFu, unit, L);
+        before = shfl_ff(before, L);
+    }
+    if (unit < 0) {  // no crossing at all (rounding): the last task with positive weight
         int last = -1;
-        for (int i = s0; i < s1; ++i)
-            if (unit_w(i) > 0.0) last = i;
+        for (int i = s0; i < s1; ++i) {  // per lane, no collectives
+            ff vp, va, vb;
+            read1(i, vp, va, vb);
+            if (unit_w(vp, va, vb).hi > 0.f) last = i;
+        }
         unit = warp_max_i(last);
         tail_rule = true;
     }
     int32_t token = -1;
     if (unit >= 0) {
-        const int32_t span = by_task ? kSTask : kSub;
-        const int32_t k_lo = unit * span, k_hi = min(P.V, k_lo + span);
-        token = scan_elements<DT, VEC>(P, tk, resid, rho, k_lo, k_hi, target - before, tail_rule, tab, lane);
+        const ff rem = ff_sub(target, before);
+        // the groups' sums cover the residual and bonus weights; the p fallback scans the task's columns
+        if (!by_p) token = group_search<DT, VEC>(P, b, unit, tk, prow, qrow, resid, rho, rem, tail_rule, tab, lane);
+        if (by_p || token == -1) {
+            const int32_t k_lo = unit * kSTask, k_hi = min(P.V, k_lo + kSTask);
+            token = scan_elements<DT, VEC>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule, tab, lane);
+        }
+        if (token == -2) token = -1;  // time-out (reported in the status word)
     }
     if (lane == 0) {
-        P.out_tokens[tk.out_pos] = token;
-        if (P.dbg.seq_mass) P.dbg.seq_mass[b] = S / sp;
+        P.out_tokens[out_pos] = token;
+        if (P.dbg.seq_mass) P.dbg.seq_mass[b] = ((double)S.hi + (double)S.lo) / ((double)sp.hi + (double)sp.lo);
     }
 }
 
@@ -777,110 +989,146 @@ __device__ __forceinline__ float2 pair8(const Cols8& c, int e) {
     return make_float2(__uint_as_float(c.w[2 * e]), __uint_as_float(c.w[2 * e + 1]));
 }
 
-// Sampler task c: sequence b = c / nS, columns [i * 2048, (i + 1) * 2048) for i = c % nS. The warp walks
-// the task in 8 steps of 256 columns (8 consecutive columns per lane, one 16-byte load per row,
-// prefetched one step ahead); every 2 steps close a 512-column sub-chunk, whose selected sums are
-// reduced over the warp and stored.
+// Sampler task c: sequence b = c / nS, columns [i * kSTask, (i + 1) * kSTask) for i = c % nS. The warp
+// reads the sequence's sampler work (polled); lane L then walks its 32 consecutive columns
+// [32 L, 32 L + 32) of the task in 4 steps of 8 (one 16-byte load per row; a bf16 task's loads are
+// all issued before the first step), accumulating the p and q weights and their selected parts. It
+// stores the selected sums of each group of kGroupLanes lanes, then the warp's sums as the record. The warp holding the
+// last task of a sequence then runs its find.
 template <int DT, bool VEC>
-__device__ void s_task(const Params& P, uint32_t c, const float2* tab, int lane) {
-    const int32_t b = (int32_t)(c / (uint32_t)P.nS);
-    const int i = (int)(c % (uint32_t)P.nS);
-    uint32_t ok = 1;
-    if (lane == 0) ok = wait_geq(P.seq_ready + (size_t)b * kFlagStride, 1u, P.status);  // back-off wait
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    __syncwarp();
-    if (!ok) return;
-    const SeqTask tk = ld_task(P.tasks + b);
-    if (tk.mode != kModeNone) {
-        const bool resid = tk.mode == kModeResidual;
+__device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) {
+    // c / nS by a multiply-high with floor(2^64 / nS) + 1: exact for c, nS < 2^32 (no MUFU reciprocal)
+    const int32_t b = P.nS == 1 ? (int32_t)c : (int32_t)__umul64hi((unsigned long long)c, P.nS_recip);
+    const int i = (int)(c - (uint32_t)b * (uint32_t)P.nS);
+    const int32_t o0 = __ldg(P.offs + b);
+    TaskInfo tk;
+    if (!get_task(P, b, lane, tk) || tk.mode == kModeNone) return;
+    const bool resid = tk.mode == kModeResidual;
+    const size_t prow = (size_t)(o0 + b + tk.n), qrow = (size_t)(o0 + tk.n);
+    {
         const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
         const int32_t cbase = i * kSTask;
-        const int steps = min(kSTask / 256, (P.V - cbase + 255) / 256);
-        ffacc2 Pp, Qq, A, Bq;
-        Cols8 np = load_cols8<DT, VEC>(P.target, (size_t)tk.prow, P.V, cbase + 8 * lane);
-        Cols8 nq;
-        if (resid) nq = load_cols8<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, cbase + 8 * lane);
+        const ExpConst EC = exp_const(P);
+        // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
+        float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
+        float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
+        // a ring of D steps in flight: bf16 loads the whole task at once, fp32 two steps ahead
+        constexpr int kSteps = kSTask / 256;
+        constexpr int D = DT == SV_BF16 ? kSteps : 2;
+        Cols8 rp[D], rq[D];
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            rp[d] = load_cols8<DT, VEC>(P.target, prow, P.V, cbase + 32 * lane + 8 * d);
+            if (resid) rq[d] = load_cols8<DT, VEC>(P.draft, qrow, P.V, cbase + 32 * lane + 8 * d);
+        }
 #pragma unroll 1
-        for (int e = 0; e < steps; ++e) {
-            const Cols8 cp = np, cq = nq;
-            if (e + 1 < steps) {
-                const int32_t k1 = cbase + 256 * (e + 1) + 8 * lane;
-                np = load_cols8<DT, VEC>(P.target, (size_t)tk.prow, P.V, k1);
-                if (resid) nq = load_cols8<DT, VEC>(P.draft, (size_t)tk.qrow, P.V, k1);
+        for (int e = 0; e < kSteps; ++e) {
+            const Cols8 cp = rp[0], cq = rq[0];
+#pragma unroll
+            for (int d = 0; d + 1 < D; ++d) {
+                rp[d] = rp[d + 1];
+                rq[d] = rq[d + 1];
+            }
+            if (e + D < kSteps) {
+                const int32_t k1 = cbase + 32 * lane + 8 * (e + D);
+                rp[D - 1] = load_cols8<DT, VEC>(P.target, prow, P.V, k1);
+                if (resid) rq[D - 1] = load_cols8<DT, VEC>(P.draft, qrow, P.V, k1);
             }
             if (resid) {
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const ff2 ep = exp2_ff2(pair8<DT>(cp, h), mp, P.K_hi, P.K_lo, tab);
-                    const ff2 eq = exp2_ff2(pair8<DT>(cq, h), mq, P.K_hi, P.K_lo, tab);
-                    Pp.add(ep.hi, ep.lo);
-                    Qq.add(eq.hi, eq.lo);
+                    const ff2 ep = exp2_ff2<DT == SV_BF16>(pair8<DT>(cp, h), mp, EC, tab);
+                    const ff2 eq = exp2_ff2<DT == SV_BF16>(pair8<DT>(cq, h), mq, EC, tab);
                     const float2 mk = sel_mask(ep, eq, tk.rho);
-                    A.add(mul2(ep.hi, mk), mul2(ep.lo, mk));
-                    Bq.add(mul2(eq.hi, mk), mul2(eq.lo, mk));
+                    const float2 hp = grid_hi(ep.hi), hq = grid_hi(eq.hi);
+                    const float2 lp = add2(sub2(ep.hi, hp), ep.lo), lq = add2(sub2(eq.hi, hq), eq.lo);
+                    Ph = add2(Ph, hp);
+                    Pl = add2(Pl, lp);
+                    Qh = add2(Qh, hq);
+                    Ql = add2(Ql, lq);
+                    Ah = fma2(mk, hp, Ah);
+                    Al = fma2(mk, lp, Al);
+                    Bh = fma2(mk, hq, Bh);
+                    Bl = fma2(mk, lq, Bl);
                 }
             } else {
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    const ff2 ep = exp2_ff2(pair8<DT>(cp, h), mp, P.K_hi, P.K_lo, tab);
-                    A.add(ep.hi, ep.lo);
+                    const ff2 ep = exp2_ff2<DT == SV_BF16>(pair8<DT>(cp, h), mp, EC, tab);
+                    const float2 hp = grid_hi(ep.hi);
+                    Ph = add2(Ph, hp);
+                    Pl = add2(Pl, add2(sub2(ep.hi, hp), ep.lo));
                 }
-            }
-            if ((e & 1) || e + 1 == steps) {  // a 512-column sub-chunk is complete
-                const int sc = i * kSubPerTask + (e >> 1);
-                const double sa = warp_sum_ff(A.fold());
-                const double sb = resid ? warp_sum_ff(Bq.fold()) : 0.0;
-                if (lane == 0) P.subs[(size_t)b * P.nsub + sc] = make_double2(sa, sb);
-                if (!resid) {  // the p total of a bonus draw is the sum of its sub-chunk sums
-                    const float hs = (float)sa;
-                    Pp.add(make_float2(hs, 0.f), make_float2((float)(sa - (double)hs), 0.f));
-                }
-                A = ffacc2();
-                Bq = ffacc2();
             }
         }
-        const double sp = resid ? warp_sum_ff(Pp.fold()) : Pp.fold().value();
-        const double sq = resid ? warp_sum_ff(Qq.fold()) : 0.0;
-        if (lane == 0) P.stot[(size_t)b * P.nS + i] = make_double2(sp, sq);
+        // the group words first (read by the find only, which polls them): sums over kGroupLanes lanes
+        ff ga = resid ? lane_ff(Ah, Al) : lane_ff(Ph, Pl), gb = resid ? lane_ff(Bh, Bl) : ff{0.f, 0.f};
+#pragma unroll
+        for (int o = 1; o < kGroupLanes; o <<= 1) {
+            ga = ff_add(ga, ff{__shfl_xor_sync(0xFFFFFFFFu, ga.hi, o), __shfl_xor_sync(0xFFFFFFFFu, ga.lo, o)});
+            gb = ff_add(gb, ff{__shfl_xor_sync(0xFFFFFFFFu, gb.hi, o), __shfl_xor_sync(0xFFFFFFFFu, gb.lo, o)});
+        }
+        if (lane % kGroupLanes == 0) {
+            Word* gw = P.groupw + (((size_t)b * P.nS + i) * kGroups + lane / kGroupLanes) * kGroupWords;
+            st_word(gw, pack_ff(ga));
+            st_word(gw + 1, pack_ff(gb));
+        }
+        const ff sp = warp_sum_ff(lane_ff(Ph, Pl));
+        ff mine = sp;  // record word `lane` (lanes 0-3)
+        if (resid) {
+            const ff sq = warp_sum_ff(lane_ff(Qh, Ql)), sa = warp_sum_ff(lane_ff(Ah, Al));
+            const ff sb = warp_sum_ff(lane_ff(Bh, Bl));
+            mine = lane == 1 ? sq : lane == 2 ? sa : lane == 3 ? sb : sp;
+        } else if (lane == 1 || lane == 3) {
+            mine = ff{0.f, 0.f};
+        }
+        if (lane < kRecWords) st_word(P.recw + ((size_t)b * P.nS + i) * kRecWords + lane, pack_ff(mine));
     }
-    uint32_t last = 0;
-    if (lane == 0) {
-        __threadfence();
-        last = atomicAdd(P.s_done + b, 1u) == (uint32_t)P.nS - 1u;
-    }
-    last = __shfl_sync(0xFFFFFFFFu, last, 0);
-    if (last) {
-        __threadfence();
-        find<DT, VEC>(P, b, tab, lane);
-    }
+    if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0 + b + tk.n, tab, lane);
 }
 
 // ------------------------------------------------------------------------------------------------
 // Statistics tasks
 // ------------------------------------------------------------------------------------------------
 struct ATask {
-    int32_t r, ch, b, g, o0;
+    int32_t r, ch;
     const char* rowp;
     int len;
 };
 
-// Row, chunk and sequence of statistics task t (sequence-major order). `cur` is a sequence cursor that
-// only moves forward: a warp visits its tasks in increasing order, so the owning sequence is found
-// with a couple of cached offset reads instead of a search.
+// Source row of statistics row r. Greedy: the rows are the target rows themselves. Sampling: from the
+// shared-memory row map when the batch has one (entry: draft flag in the sign bit, row index below),
+// else through a sequence cursor that only moves forward (a warp visits its tasks in increasing
+// order, so the owning sequence is found with a couple of cached offset reads instead of a search).
 template <int DT, bool GREEDY>
-__device__ __forceinline__ ATask a_task_at(const Params& P, long long t, int32_t& cur, const int32_t* bases) {
-    ATask at;
-    at.r = (int32_t)(t / P.nchA);
-    at.ch = (int32_t)(t % P.nchA);
-    // bases: the sequences' first statistics rows in shared memory (small batches), else from offsets
-    while (cur + 1 < P.B && (bases ? bases[cur + 1] : stat_base<GREEDY>(P, cur + 1)) <= at.r) ++cur;
-    at.b = cur;
-    at.o0 = __ldg(P.offs + at.b);
-    at.g = __ldg(P.gammas + at.b);
-    const int32_t j = at.r - (GREEDY ? at.o0 + at.b : 2 * at.o0 + at.b);
-    const size_t row = j <= at.g ? (size_t)(at.o0 + at.b + j) : (size_t)(at.o0 + j - at.g - 1);
+__device__ __forceinline__ const char* stat_row_src(const Params& P, int32_t r, int32_t ch, int32_t& cur,
+                                                    const int32_t* bases, const int32_t* rows) {
     const size_t esz = DT == SV_BF16 ? 2 : 4;
-    at.rowp = (const char*)(j <= at.g ? P.target : P.draft) + (row * (size_t)P.V + (size_t)at.ch * kAChunk) * esz;
+    size_t row = (size_t)r;
+    bool draft = false;
+    if (!GREEDY) {
+        if (rows) {
+            const int32_t v = rows[r];
+            draft = v < 0;
+            row = (size_t)(v & 0x7FFFFFFF);
+        } else {
+            while (cur + 1 < P.B && (bases ? bases[cur + 1] : stat_base<false>(P, cur + 1)) <= r) ++cur;
+            const int32_t o0 = __ldg(P.offs + cur), g = __ldg(P.gammas + cur);
+            const int32_t j = r - (2 * o0 + cur);
+            draft = j > g;
+            row = draft ? (size_t)(o0 + j - g - 1) : (size_t)(o0 + cur + j);
+        }
+    }
+    return (const char*)(draft ? P.draft : P.target) + (row * (size_t)P.V + (size_t)ch * kAChunk) * esz;
+}
+
+template <int DT, bool GREEDY>
+__device__ __forceinline__ ATask a_task_at(const Params& P, uint32_t t, int32_t& cur, const int32_t* bases,
+                                           const int32_t* rows) {
+    ATask at;
+    at.r = (int32_t)(t / (uint32_t)P.nchA);
+    at.ch = (int32_t)(t % (uint32_t)P.nchA);
+    at.rowp = stat_row_src<DT, GREEDY>(P, at.r, at.ch, cur, bases, rows);
     at.len = min(kAChunk, P.V - at.ch * kAChunk);
     return at;
 }
@@ -900,43 +1148,68 @@ __device__ __forceinline__ void a_finish(const Params& P, const ATask& at, const
     }
 }
 
-// Decision of sequence b, run by the warp holding its first ticket; it waits for the partials itself.
+// Decision of sequence b, run by the warp holding its ticket; it polls the partial words itself.
 template <int DT, bool GREEDY>
-__device__ void lead_decide(const Params& P, int32_t b, const float2* tab, int lane) {
+__device__ void lead_decide(const Params& P, int32_t b, const float* tab, int lane) {
     const int32_t o0 = __ldg(P.offs + b), g = __ldg(P.gammas + b);
-    decide<DT, GREEDY>(P, b, g, o0, lane, tab);  // polls the sequence's partial words
-    if (!GREEDY) publish(P, b, lane);
+    decide<DT, GREEDY>(P, b, g, o0, lane, tab);
 }
 
 // A streamer warp on the bulk-copy path: its statistics tasks (statically strided over all streamers)
 // arrive through a ring of kStages shared-memory stages filled by 1-D bulk copies, so up to
-// kStages - 1 tasks stay in flight while one is reduced, without holding registers.
-__device__ void stream_bulk(const Params& P, long long nA, unsigned char* dsmem, const int32_t* bases, int warp,
-                            int lane) {
+// kStages - 1 tasks stay in flight while one is reduced, without holding registers. The (row, chunk)
+// of the task being reduced and of the task that refills its stage advance incrementally; the refill's
+// source is resolved before waiting on the stage, so its lookups overlap the wait and the reduction.
+__device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, const int32_t* bases,
+                            const int32_t* rows, int warp, int lane) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(dsmem + kStreamWarps * kStages * kStageBytes) + warp * kStages;
     unsigned char* bufs = dsmem + (size_t)warp * kStages * kStageBytes;
-    const long long SW = (long long)gridDim.x * kStreamWarps;
-    const long long sw = (long long)blockIdx.x * kStreamWarps + warp;
+    const uint32_t SW = gridDim.x * kStreamWarps;
+    const uint32_t sw = blockIdx.x * kStreamWarps + warp;
+    const uint32_t nch = (uint32_t)P.nchA;
+    const uint32_t dr = SW / nch, dc = SW % nch;
+    auto advance = [&](uint32_t& r, uint32_t& c) {
+        r += dr;
+        c += dc;
+        if (c >= nch) {
+            c -= nch;
+            ++r;
+        }
+    };
+    auto len_of = [&](uint32_t c) { return min(kAChunk, P.V - (int)c * kAChunk); };
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
     }
     __syncwarp();
-    int32_t cur_issue = 0, cur_proc = 0;
-    auto issue = [&](long long t, int s) {  // lane 0
-        const ATask at = a_task_at<SV_BF16, false>(P, t, cur_issue, bases);
-        const uint32_t bytes = (uint32_t)at.len * 2u;
+    int32_t cur = 0;
+    auto issue = [&](const char* src, uint32_t bytes, int s) {  // lane 0
         mbar_arrive_expect_tx(&bars[s], bytes);
-        bulk_g2s(bufs + (size_t)s * kStageBytes, at.rowp, bytes, &bars[s]);
+        bulk_g2s(bufs + (size_t)s * kStageBytes, src, bytes, &bars[s]);
     };
-    if (lane == 0)
-        for (int s = 0; s < kStages; ++s)
-            if (sw + s * SW < nA) issue(sw + s * SW, s);
+    uint32_t rp = sw / nch, cp = sw % nch;  // task being reduced
+    uint32_t ri = rp, ci = cp;              // next task to issue
+    for (int s = 0; s < kStages; ++s) {
+        if (sw + s * SW < nA) {
+            const char* src = stat_row_src<SV_BF16, false>(P, (int32_t)ri, (int32_t)ci, cur, bases, rows);
+            if (lane == 0) issue(src, (uint32_t)len_of(ci) * 2u, s);
+        }
+        advance(ri, ci);
+    }
     uint32_t parity = 0;  // bit s: parity of stage s's next completion
     int k = 0;
-    for (long long t = sw; t < nA; t += SW, ++k) {
+    for (uint32_t t = sw; t < nA; t += SW, ++k) {
         const int s = k % kStages;
-        const bool ok = mbar_wait(&bars[s], (parity >> s) & 1u, kSpinLimit);
+        const uint32_t tn = t + kStages * SW;
+        const char* nsrc = nullptr;
+        uint32_t nbytes = 0;
+        if (tn < nA) {
+            nsrc = stat_row_src<SV_BF16, false>(P, (int32_t)ri, (int32_t)ci, cur, bases, rows);
+            nbytes = (uint32_t)len_of(ci) * 2u;
+        }
+        advance(ri, ci);
+        // one verdict for the whole warp: a time-out seen by some lanes only must not split it
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[s], (parity >> s) & 1u, kSpinLimit));
         parity ^= 1u << s;
         if (!ok) {
             // a copy that never lands: report, let the copies still in flight land, stop streaming
@@ -947,14 +1220,18 @@ __device__ void stream_bulk(const Params& P, long long nA, unsigned char* dsmem,
             }
             return;
         }
-        const ATask at = a_task_at<SV_BF16, false>(P, t, cur_proc, bases);
+        ATask at;
+        at.r = (int32_t)rp;
+        at.ch = (int32_t)cp;
+        at.len = len_of(cp);
         const SegStats st = stats_bf16_smem(bufs + (size_t)s * kStageBytes, at.len, lane, P.K_hi);
         __syncwarp();
-        if (lane == 0 && t + kStages * SW < nA) {
+        if (lane == 0 && tn < nA) {
             fence_proxy_async_smem();  // this stage's reads come before the copy that overwrites it
-            issue(t + kStages * SW, s);
+            issue(nsrc, nbytes, s);
         }
         a_finish<false>(P, at, st, lane);
+        advance(rp, cp);
     }
 }
 
@@ -962,14 +1239,15 @@ __device__ void stream_bulk(const Params& P, long long nA, unsigned char* dsmem,
 // The kernel
 // ------------------------------------------------------------------------------------------------
 template <int DT, bool VEC, bool GREEDY>
-__global__ void __launch_bounds__(kThreads, 2) k_verify(const Params P) {
+__global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ Params P) {
     constexpr bool kBulk = DT == SV_BF16 && VEC && !GREEDY;
     extern __shared__ __align__(128) unsigned char dsmem[];
-    __shared__ float2 tab[64];
+    __shared__ float tab[128];
     __shared__ int s_bad;
     __shared__ int32_t s_base[kBaseCache];
+    __shared__ int32_t s_row[GREEDY ? 1 : kRowCache];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (!GREEDY) fill_exp2_table(tab);
+    if (!GREEDY) fill_exp2_table(P, tab);
     if (tid == 0) s_bad = __ldg(P.offs) != 0;
     __syncthreads();
     // every CTA checks the whole CSR structure before any row is read (and caches small batches' row
@@ -978,8 +1256,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const Params P) {
     const bool cache = P.B <= kBaseCache;
     for (int32_t b = tid; b < P.B; b += kThreads) {
         const int32_t o0 = __ldg(P.offs + b), o1 = __ldg(P.offs + b + 1), g = __ldg(P.gammas + b);
-        bad |= !(g >= 0 && g <= P.max_gamma && o0 >= 0 && o1 - o0 == g);
-        if (cache) s_base[b] = GREEDY ? o0 + b : 2 * o0 + b;
+        const bool ok = g >= 0 && g <= P.max_gamma && o0 >= 0 && o1 - o0 == g;
+        bad |= !ok;
+        const int32_t sb = GREEDY ? o0 + b : 2 * o0 + b;
+        if (cache) s_base[b] = sb;
+        if (!GREEDY && ok)  // row map entries that fit (it is used only when every row fits)
+            for (int32_t j = 0; j <= 2 * g && sb + j < kRowCache; ++j)
+                s_row[sb + j] = j <= g ? o0 + b + j : (int32_t)(0x80000000u | (uint32_t)(o0 + j - g - 1));
     }
     const int32_t* bases = cache ? s_base : nullptr;
     if (__syncthreads_or(bad) || s_bad) {
@@ -990,39 +1273,44 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const Params P) {
         return;
     }
     const int32_t oB = __ldg(P.offs + P.B);
-    const long long nA = (long long)(GREEDY ? oB + P.B : 2 * oB + P.B) * P.nchA;
+    // the host bounds rows * nchA and B * nS below 2^31
+    const uint32_t nA = (uint32_t)(GREEDY ? oB + P.B : 2 * oB + P.B) * (uint32_t)P.nchA;
     const uint32_t nStot = GREEDY ? 0u : (uint32_t)P.B * (uint32_t)P.nS;
+    const int32_t* rows = !GREEDY && 2 * oB + P.B <= kRowCache ? s_row : nullptr;
 
-    // Statistics. Bulk-copy path: kStreamWarps warps per CTA stream while the others start sampling at
-    // once. Other paths: every warp streams its strided tasks from registers first.
+    // Statistics. Bulk-copy path: the upper kStreamWarps warps of the CTA stream while the lower ones
+    // take tickets at once (the lower warps are the ones a partition's scheduler favours, so decisions
+    // and sampler work are not starved by the streamers). Other paths: every warp streams its strided
+    // tasks from registers first.
     if (kBulk) {
-        if (warp < kStreamWarps) stream_bulk(P, nA, dsmem, bases, warp, lane);
+        if (warp >= kWarps - kStreamWarps) stream_bulk(P, nA, dsmem, bases, rows, warp - (kWarps - kStreamWarps), lane);
     } else {
-        const long long W = (long long)gridDim.x * kWarps;
+        const uint32_t W = gridDim.x * kWarps;
         int32_t cur = 0;
-        for (long long a = (long long)blockIdx.x * kWarps + warp; a < nA; a += W) {
-            const ATask at = a_task_at<DT, GREEDY>(P, a, cur, bases);
+        for (uint32_t a = blockIdx.x * kWarps + warp; a < nA; a += W) {
+            const ATask at = a_task_at<DT, GREEDY>(P, a, cur, bases, rows);
             const SegStats st = seg_stats<DT, VEC, GREEDY>(at.rowp, at.len, lane, P.K_hi);
             a_finish<GREEDY>(P, at, st, lane);
         }
     }
-    // Tickets in sequence order. Greedy: one ticket per sequence, its decision. Sampling: nS sampler
-    // tasks per sequence; the holder of a sequence's first ticket first waits for the sequence's
-    // statistics, decides and publishes it; the others wait for that ready flag. Waits are bounded.
-    // Only warps whose statistics tasks are done ever wait, so every awaited count is completed by warps
-    // that never wait.
-    const uint32_t ntick = GREEDY ? (uint32_t)P.B : nStot;
+    // Tickets: first the B decisions (each polls its sequence's partial words, decides and, sampling,
+    // writes the sequence's sampler work), then the nS sampler tasks of every sequence in sequence
+    // order (each polls its sequence's sampler work; the holder of a sequence's last task then polls the
+    // task records and runs the find). A warp claims a ticket only when it is free to work on it, so a
+    // claimed ticket is never held up behind its holder's other work. Waits are bounded. Every awaited
+    // word is produced by a statistics task (done by warps that never wait before finishing them) or by
+    // a ticket claimed earlier than the waiter's, whose holder waits only on earlier tickets.
+    const uint32_t ntick = (uint32_t)P.B + nStot;
     while (true) {
         uint32_t cl = 0;
         if (lane == 0) cl = atomicAdd(&P.ctr->claim, 1u);
         cl = __shfl_sync(0xFFFFFFFFu, cl, 0);
         if (cl >= ntick) break;
-        if (GREEDY) {
-            lead_decide<DT, true>(P, (int32_t)cl, tab, lane);
+        if (cl < (uint32_t)P.B) {
+            lead_decide<DT, GREEDY>(P, (int32_t)cl, tab, lane);
             continue;
         }
-        if (cl % (uint32_t)P.nS == 0u) lead_decide<DT, false>(P, (int32_t)(cl / (uint32_t)P.nS), tab, lane);
-        s_task<DT, VEC>(P, cl, tab, lane);
+        if (!GREEDY) s_task<DT, VEC>(P, cl - (uint32_t)P.B, tab, lane);
     }
 }
 
@@ -1075,20 +1363,17 @@ cudaError_t launch_verify(const Params& P, const Layout& L, void* ws, int dtype,
 Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const size_t nchA = ((size_t)V + kAChunk - 1) / kAChunk;
-    const size_t nsub = ((size_t)V + kSub - 1) / kSub;
     const size_t nS = ((size_t)V + kSTask - 1) / kSTask;
     Layout L;
     // the first four regions are cleared before every call, with one memset
     L.counters = 0;
-    L.s_done = up(L.counters + sizeof(Counters));
-    L.seq_ready = up(L.s_done + (size_t)B * sizeof(uint32_t));
-    L.partials = up(L.seq_ready + (size_t)B * kFlagStride * sizeof(uint32_t));
-    L.tasks = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchA * sizeof(PartialWord));
+    L.partials = up(L.counters + sizeof(Counters));
+    L.taskw = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchA * sizeof(PartialWord));
+    L.recw = up(L.taskw + (size_t)B * kTaskWords * sizeof(Word));
+    L.groupw = up(L.recw + (size_t)B * nS * kRecWords * sizeof(Word));
+    L.status = up(L.groupw + (size_t)B * nS * kGroups * kGroupWords * sizeof(Word));
     L.zero_begin = 0;
-    L.zero_end = L.tasks;
-    L.subs = up(L.tasks + (size_t)B * sizeof(SeqTask));
-    L.stot = up(L.subs + (size_t)B * nsub * sizeof(double2));
-    L.status = up(L.stot + (size_t)B * nS * sizeof(double2));
+    L.zero_end = L.status;
     L.total = up(L.status + sizeof(uint32_t));
     return L;
 }
