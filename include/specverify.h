@@ -57,7 +57,7 @@ typedef enum {
     SV_ERR_BAD_OFFSETS = 4, /* device: seq_offsets / gammas inconsistent or gamma > max_gamma */
     SV_ERR_NONFINITE = 5,   /* device: NaN or +inf logit in a row the step reads */
     SV_ERR_EMPTY_ROW = 6,   /* device: a row whose logits are all -inf */
-    SV_ERR_TIMEOUT = 7,     /* device: a bounded wait gave up (reserved; no path waits today) */
+    SV_ERR_TIMEOUT = 7,     /* device: a bounded wait between warps of the launch gave up */
     SV_ERR_WORKSPACE = 8    /* workspace NULL or smaller than spec_verify_workspace_size() */
 } sv_status;
 

@@ -181,22 +181,28 @@ struct ExpConst {
 // relative error below about 1e-9. Tang's method: t = d K carried as t_hi + t_lo, j = rint(64 t),
 // 2^t = 2^(j >> 6) * 2^((j & 63) / 64) * e^y with |y| <= ln2/128 and e^y - 1 from its Taylor series.
 // tab holds 2^(i/64) split in floats: tab[i] (high part) and tab[64 + i] (low part), i = 0..63.
-// EXACT_D: l - m is exact in float (bf16 logits); otherwise its rounding error is carried too.
+// TWOSUM: l - m is carried as float-float. For bf16 logits l - m rounds in float only when the two
+// exponents are more than 16 apart; with |m| >= 2^-4 that needs |l| >= 2^12 (a zero weight) or a
+// logit within 2^-16 |m| of zero (a single rare column, error below 1e-7 of its weight), so callers
+// may drop the correction for such rows (kNeedTwoSum); rows whose maximum is near zero (log-softmax
+// inputs) need it for every column.
 // Arguments at or below d_min K, including -inf logits, give exactly 0 (2^-126 and below only).
-template <bool EXACT_D>
+constexpr float kNeedTwoSum = 0.0625f;
+template <bool TWOSUM = true>
 __device__ __forceinline__ ff2 exp2_ff2(float2 l, float2 m, const ExpConst& C, const float* tab) {
     float2 d = sub2(l, m);
     float2 dl = make_float2(0.f, 0.f);
-    if (!EXACT_D) {  // TwoSum error of l - m; zero where the clamp below applies (incl. -inf)
+    if (TWOSUM) {
         const float2 bb = sub2(d, l);
         dl = add2(sub2(l, sub2(d, bb)), sub2(make_float2(-m.x, -m.y), bb));
+        // zero where the clamp below applies (including -inf logits, whose TwoSum error is NaN)
         dl = make_float2(d.x > C.d_min ? dl.x : 0.f, d.y > C.d_min ? dl.y : 0.f);
     }
     d = make_float2(fmaxf(d.x, C.d_min), fmaxf(d.y, C.d_min));
     const float2 nt = mul2(d, f2(C.nK_hi));          // -t_hi
     float2 tl = fma2(d, f2(C.K_hi), nt);              // exact rounding error of d * K_hi
     tl = fma2(d, f2(C.K_lo), tl);
-    if (!EXACT_D) tl = fma2(dl, f2(C.K_hi), tl);
+    if (TWOSUM) tl = fma2(dl, f2(C.K_hi), tl);
     // j = rint(64 t_hi) lands in the low mantissa bits of jm (adding 1.5 * 2^23 rounds to an integer)
     const float2 jm = fma2(nt, f2(-64.f), f2(12582912.f));
     const uint32_t b0 = __float_as_uint(jm.x), b1 = __float_as_uint(jm.y);

@@ -61,7 +61,7 @@ constexpr int kGroupWords = 2;
 
 // Counters of one call (zeroed before the kernel by the launch sequence).
 struct Counters {
-    uint32_t claim;  // tickets claimed: the B decisions first, then the sampler tasks in sequence order
+    uint32_t claim;  // sampler tasks claimed, in sequence-major order
     uint32_t pad[31];
 };
 

@@ -524,7 +524,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     bool acc = true;
     if (lane < g) {
         // p(x) and q(x) from the precise exponential of the exact logit gaps, over the fp32 normalisers
-        const ff2 e = exp2_ff2<DT == SV_BF16>(make_float2(lt, ld), make_float2(my_m0, dm), exp_const(P), tab);
+        const ff2 e = exp2_ff2(make_float2(lt, ld), make_float2(my_m0, dm), exp_const(P), tab);
         const float px = div_fma(e.hi.x + e.lo.x, my_s0);
         const float qx = div_fma(e.hi.y + e.lo.y, ds);
         acc = u_acc * qx < px;
@@ -626,10 +626,10 @@ __device__ __forceinline__ ff resid_weight(float hp, float lp, float hq, float l
 
 // Weight of one column in the find's element search: the precise p weight, or the residual weight of
 // a selected column (float-float); 0 at or past k_hi.
-template <int DT, bool EXACT_D>
+template <int DT>
 __device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& tk, const ExpConst& EC, bool resid,
                                             ff rho, const float* tab) {
-    const ff2 e = exp2_ff2<EXACT_D>(make_float2(lp, lq), make_float2(tk.m_p, tk.m_q), EC, tab);
+    const ff2 e = exp2_ff2(make_float2(lp, lq), make_float2(tk.m_p, tk.m_q), EC, tab);
     if (!resid) return ff_norm(e.hi.x, e.lo.x);
     const bool sel = e.hi.x > tk.rho * e.hi.y;  // the selection rule of sel_mask
     return resid_weight(e.hi.x, e.lo.x, e.hi.y, e.lo.y, sel ? 1.f : 0.f, rho);
@@ -644,7 +644,6 @@ template <int DT, bool VEC>
 __device__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t prow, size_t qrow, bool resid, ff rho,
                                  int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, const float* tab, int lane) {
     const ExpConst EC = exp_const(P);
-    constexpr bool kExact = DT == SV_BF16;
     // a unit spans at most kSTask columns: NB passes; bf16 issues every pass's loads first
     constexpr int NB = kSTask / kScanBlock;
     constexpr bool kAhead = DT == SV_BF16;
@@ -676,8 +675,8 @@ __device__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t pro
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float2 lpv = col2<DT>(cp, e), lqv = resid ? col2<DT>(cq, e) : f2(0.f);
-            const ff w0 = column_weight<DT, kExact>(lpv.x, lqv.x, tk, EC, resid, rho, tab);
-            const ff w1 = column_weight<DT, kExact>(lpv.y, lqv.y, tk, EC, resid, rho, tab);
+            const ff w0 = column_weight<DT>(lpv.x, lqv.x, tk, EC, resid, rho, tab);
+            const ff w1 = column_weight<DT>(lpv.y, lqv.y, tk, EC, resid, rho, tab);
             if (k0 + 2 * e < k_hi && w0.hi > 0.f) {
                 tot = ff_add(tot, w0);
                 lastp = k0 + 2 * e;
@@ -702,7 +701,7 @@ __device__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t pro
             if (lane < kScanPerLane && kj < k_hi) {
                 const float lpj = logit_at<DT>(P.target, prow * (size_t)P.V + kj);
                 const float lqj = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + kj) : 0.f;
-                w = column_weight<DT, kExact>(lpj, lqj, tk, EC, resid, rho, tab);
+                w = column_weight<DT>(lpj, lqj, tk, EC, resid, rho, tab);
                 if (!(w.hi > 0.f)) w = ff{0.f, 0.f};
             }
             const ff c = ff_add(pre, warp_inscan_ff(w, lane));  // lanes >= 16 add zeros
@@ -760,7 +759,7 @@ __device__ int32_t group_search(const Params& P, int32_t b, int unit, const Task
         if (k < P.V) {
             const float lpk = logit_at<DT>(P.target, prow * (size_t)P.V + k);
             const float lqk = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + k) : 0.f;
-            cw[e] = column_weight<DT, DT == SV_BF16>(lpk, lqk, tk, EC, resid, rho, tab);
+            cw[e] = column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab);
             if (!(cw[e].hi > 0.f)) cw[e] = ff{0.f, 0.f};
         }
         tot = ff_add(tot, cw[e]);
@@ -989,12 +988,97 @@ __device__ __forceinline__ float2 pair8(const Cols8& c, int e) {
     return make_float2(__uint_as_float(c.w[2 * e]), __uint_as_float(c.w[2 * e + 1]));
 }
 
-// Sampler task c: sequence b = c / nS, columns [i * kSTask, (i + 1) * kSTask) for i = c % nS. The warp
-// reads the sequence's sampler work (polled); lane L then walks its 32 consecutive columns
-// [32 L, 32 L + 32) of the task in 4 steps of 8 (one 16-byte load per row; a bf16 task's loads are
-// all issued before the first step), accumulating the p and q weights and their selected parts. It
-// stores the selected sums of each group of kGroupLanes lanes, then the warp's sums as the record. The warp holding the
-// last task of a sequence then runs its find.
+// The accumulation of one sampler task: sequence b, columns [i * kSTask, (i + 1) * kSTask). Lane L
+// walks its 32 consecutive columns [32 L, 32 L + 32) in 4 steps of 8 (one 16-byte load per row; a
+// bf16 task's loads are all issued before the first step), accumulating the p and q weights and their
+// selected parts. It stores the selected sums of each group of kGroupLanes lanes, then the warp's sums
+// as the task's record. TWOSUM: carry the rounding of l - m (see exp2_ff2).
+template <int DT, bool VEC, bool TWOSUM>
+__device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, const TaskInfo& tk, size_t prow,
+                                             size_t qrow, const float* tab, int lane) {
+    const bool resid = tk.mode == kModeResidual;
+    const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
+    const int32_t cbase = i * kSTask;
+    const ExpConst EC = exp_const(P);
+    // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
+    float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
+    float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
+    // a ring of D steps in flight: bf16 loads the whole task at once, fp32 two steps ahead
+    constexpr int kSteps = kSTask / 256;
+    constexpr int D = DT == SV_BF16 ? kSteps : 2;
+    Cols8 rp[D], rq[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        rp[d] = load_cols8<DT, VEC>(P.target, prow, P.V, cbase + 32 * lane + 8 * d);
+        if (resid) rq[d] = load_cols8<DT, VEC>(P.draft, qrow, P.V, cbase + 32 * lane + 8 * d);
+    }
+#pragma unroll 1
+    for (int e = 0; e < kSteps; ++e) {
+        const Cols8 cp = rp[0], cq = rq[0];
+#pragma unroll
+        for (int d = 0; d + 1 < D; ++d) {
+            rp[d] = rp[d + 1];
+            rq[d] = rq[d + 1];
+        }
+        if (e + D < kSteps) {
+            const int32_t k1 = cbase + 32 * lane + 8 * (e + D);
+            rp[D - 1] = load_cols8<DT, VEC>(P.target, prow, P.V, k1);
+            if (resid) rq[D - 1] = load_cols8<DT, VEC>(P.draft, qrow, P.V, k1);
+        }
+        if (resid) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
+                const ff2 eq = exp2_ff2<TWOSUM>(pair8<DT>(cq, h), mq, EC, tab);
+                const float2 mk = sel_mask(ep, eq, tk.rho);
+                const float2 hp = grid_hi(ep.hi), hq = grid_hi(eq.hi);
+                const float2 lp = add2(sub2(ep.hi, hp), ep.lo), lq = add2(sub2(eq.hi, hq), eq.lo);
+                Ph = add2(Ph, hp);
+                Pl = add2(Pl, lp);
+                Qh = add2(Qh, hq);
+                Ql = add2(Ql, lq);
+                Ah = fma2(mk, hp, Ah);
+                Al = fma2(mk, lp, Al);
+                Bh = fma2(mk, hq, Bh);
+                Bl = fma2(mk, lq, Bl);
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
+                const float2 hp = grid_hi(ep.hi);
+                Ph = add2(Ph, hp);
+                Pl = add2(Pl, add2(sub2(ep.hi, hp), ep.lo));
+            }
+        }
+    }
+    // the group words first (read by the find only, which polls them): sums over kGroupLanes lanes
+    ff ga = resid ? lane_ff(Ah, Al) : lane_ff(Ph, Pl), gb = resid ? lane_ff(Bh, Bl) : ff{0.f, 0.f};
+#pragma unroll
+    for (int o = 1; o < kGroupLanes; o <<= 1) {
+        ga = ff_add(ga, ff{__shfl_xor_sync(0xFFFFFFFFu, ga.hi, o), __shfl_xor_sync(0xFFFFFFFFu, ga.lo, o)});
+        gb = ff_add(gb, ff{__shfl_xor_sync(0xFFFFFFFFu, gb.hi, o), __shfl_xor_sync(0xFFFFFFFFu, gb.lo, o)});
+    }
+    if (lane % kGroupLanes == 0) {
+        Word* gw = P.groupw + (((size_t)b * P.nS + i) * kGroups + lane / kGroupLanes) * kGroupWords;
+        st_word(gw, pack_ff(ga));
+        st_word(gw + 1, pack_ff(gb));
+    }
+    const ff sp = warp_sum_ff(lane_ff(Ph, Pl));
+    ff mine = sp;  // record word `lane` (lanes 0-3)
+    if (resid) {
+        const ff sq = warp_sum_ff(lane_ff(Qh, Ql)), sa = warp_sum_ff(lane_ff(Ah, Al));
+        const ff sb = warp_sum_ff(lane_ff(Bh, Bl));
+        mine = lane == 1 ? sq : lane == 2 ? sa : lane == 3 ? sb : sp;
+    } else if (lane == 1 || lane == 3) {
+        mine = ff{0.f, 0.f};
+    }
+    if (lane < kRecWords) st_word(P.recw + ((size_t)b * P.nS + i) * kRecWords + lane, pack_ff(mine));
+}
+
+// Sampler task c: sequence b = c / nS, task i = c % nS. The warp reads the sequence's sampler work
+// (polled), accumulates and stores the task; the warp holding the last task of a sequence then runs
+// its find.
 template <int DT, bool VEC>
 __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) {
     // c / nS by a multiply-high with floor(2^64 / nS) + 1: exact for c, nS < 2^32 (no MUFU reciprocal)
@@ -1003,87 +1087,12 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
     const int32_t o0 = __ldg(P.offs + b);
     TaskInfo tk;
     if (!get_task(P, b, lane, tk) || tk.mode == kModeNone) return;
-    const bool resid = tk.mode == kModeResidual;
     const size_t prow = (size_t)(o0 + b + tk.n), qrow = (size_t)(o0 + tk.n);
-    {
-        const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
-        const int32_t cbase = i * kSTask;
-        const ExpConst EC = exp_const(P);
-        // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
-        float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
-        float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
-        // a ring of D steps in flight: bf16 loads the whole task at once, fp32 two steps ahead
-        constexpr int kSteps = kSTask / 256;
-        constexpr int D = DT == SV_BF16 ? kSteps : 2;
-        Cols8 rp[D], rq[D];
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-            rp[d] = load_cols8<DT, VEC>(P.target, prow, P.V, cbase + 32 * lane + 8 * d);
-            if (resid) rq[d] = load_cols8<DT, VEC>(P.draft, qrow, P.V, cbase + 32 * lane + 8 * d);
-        }
-#pragma unroll 1
-        for (int e = 0; e < kSteps; ++e) {
-            const Cols8 cp = rp[0], cq = rq[0];
-#pragma unroll
-            for (int d = 0; d + 1 < D; ++d) {
-                rp[d] = rp[d + 1];
-                rq[d] = rq[d + 1];
-            }
-            if (e + D < kSteps) {
-                const int32_t k1 = cbase + 32 * lane + 8 * (e + D);
-                rp[D - 1] = load_cols8<DT, VEC>(P.target, prow, P.V, k1);
-                if (resid) rq[D - 1] = load_cols8<DT, VEC>(P.draft, qrow, P.V, k1);
-            }
-            if (resid) {
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const ff2 ep = exp2_ff2<DT == SV_BF16>(pair8<DT>(cp, h), mp, EC, tab);
-                    const ff2 eq = exp2_ff2<DT == SV_BF16>(pair8<DT>(cq, h), mq, EC, tab);
-                    const float2 mk = sel_mask(ep, eq, tk.rho);
-                    const float2 hp = grid_hi(ep.hi), hq = grid_hi(eq.hi);
-                    const float2 lp = add2(sub2(ep.hi, hp), ep.lo), lq = add2(sub2(eq.hi, hq), eq.lo);
-                    Ph = add2(Ph, hp);
-                    Pl = add2(Pl, lp);
-                    Qh = add2(Qh, hq);
-                    Ql = add2(Ql, lq);
-                    Ah = fma2(mk, hp, Ah);
-                    Al = fma2(mk, lp, Al);
-                    Bh = fma2(mk, hq, Bh);
-                    Bl = fma2(mk, lq, Bl);
-                }
-            } else {
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const ff2 ep = exp2_ff2<DT == SV_BF16>(pair8<DT>(cp, h), mp, EC, tab);
-                    const float2 hp = grid_hi(ep.hi);
-                    Ph = add2(Ph, hp);
-                    Pl = add2(Pl, add2(sub2(ep.hi, hp), ep.lo));
-                }
-            }
-        }
-        // the group words first (read by the find only, which polls them): sums over kGroupLanes lanes
-        ff ga = resid ? lane_ff(Ah, Al) : lane_ff(Ph, Pl), gb = resid ? lane_ff(Bh, Bl) : ff{0.f, 0.f};
-#pragma unroll
-        for (int o = 1; o < kGroupLanes; o <<= 1) {
-            ga = ff_add(ga, ff{__shfl_xor_sync(0xFFFFFFFFu, ga.hi, o), __shfl_xor_sync(0xFFFFFFFFu, ga.lo, o)});
-            gb = ff_add(gb, ff{__shfl_xor_sync(0xFFFFFFFFu, gb.hi, o), __shfl_xor_sync(0xFFFFFFFFu, gb.lo, o)});
-        }
-        if (lane % kGroupLanes == 0) {
-            Word* gw = P.groupw + (((size_t)b * P.nS + i) * kGroups + lane / kGroupLanes) * kGroupWords;
-            st_word(gw, pack_ff(ga));
-            st_word(gw + 1, pack_ff(gb));
-        }
-        const ff sp = warp_sum_ff(lane_ff(Ph, Pl));
-        ff mine = sp;  // record word `lane` (lanes 0-3)
-        if (resid) {
-            const ff sq = warp_sum_ff(lane_ff(Qh, Ql)), sa = warp_sum_ff(lane_ff(Ah, Al));
-            const ff sb = warp_sum_ff(lane_ff(Bh, Bl));
-            mine = lane == 1 ? sq : lane == 2 ? sa : lane == 3 ? sb : sp;
-        } else if (lane == 1 || lane == 3) {
-            mine = ff{0.f, 0.f};
-        }
-        if (lane < kRecWords) st_word(P.recw + ((size_t)b * P.nS + i) * kRecWords + lane, pack_ff(mine));
-    }
+    // rows whose maximum is near zero carry the rounding of l - m (see exp2_ff2)
+    if (fabsf(tk.m_p) < kNeedTwoSum || (tk.mode == kModeResidual && fabsf(tk.m_q) < kNeedTwoSum))
+        s_accumulate<DT, VEC, true>(P, b, i, tk, prow, qrow, tab, lane);
+    else
+        s_accumulate<DT, VEC, false>(P, b, i, tk, prow, qrow, tab, lane);
     if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0 + b + tk.n, tab, lane);
 }
 
@@ -1148,7 +1157,7 @@ __device__ __forceinline__ void a_finish(const Params& P, const ATask& at, const
     }
 }
 
-// Decision of sequence b, run by the warp holding its ticket; it polls the partial words itself.
+// Decision of sequence b, run by its decider warp; it polls the partial words itself.
 template <int DT, bool GREEDY>
 __device__ void lead_decide(const Params& P, int32_t b, const float* tab, int lane) {
     const int32_t o0 = __ldg(P.offs + b), g = __ldg(P.gammas + b);
@@ -1293,24 +1302,30 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
             a_finish<GREEDY>(P, at, st, lane);
         }
     }
-    // Tickets: first the B decisions (each polls its sequence's partial words, decides and, sampling,
-    // writes the sequence's sampler work), then the nS sampler tasks of every sequence in sequence
-    // order (each polls its sequence's sampler work; the holder of a sequence's last task then polls the
-    // task records and runs the find). A warp claims a ticket only when it is free to work on it, so a
-    // claimed ticket is never held up behind its holder's other work. Waits are bounded. Every awaited
-    // word is produced by a statistics task (done by warps that never wait before finishing them) or by
-    // a ticket claimed earlier than the waiter's, whose holder waits only on earlier tickets.
-    const uint32_t ntick = (uint32_t)P.B + nStot;
-    while (true) {
-        uint32_t cl = 0;
-        if (lane == 0) cl = atomicAdd(&P.ctr->claim, 1u);
-        cl = __shfl_sync(0xFFFFFFFFu, cl, 0);
-        if (cl >= ntick) break;
-        if (cl < (uint32_t)P.B) {
-            lead_decide<DT, GREEDY>(P, (int32_t)cl, tab, lane);
-            continue;
+    // Work after the statistics:
+    //   decisions, assigned statically: decider slot d (the non-streamer warps on the bulk-copy path,
+    //     every warp otherwise) decides sequences d, d + ND, ... (each polls its sequence's partial
+    //     words and, sampling, writes the sequence's sampler work);
+    //   sampler tasks, claimed one at a time from a counter in sequence-major order by whichever warp
+    //     is free (streamers join when their stream ends); the warp that claims a sequence's last task
+    //     runs its find after the task.
+    // Waits are bounded. A decision waits only on statistics tasks, which are done by warps that never
+    // wait before finishing them. A sampler task waits on its decision, and a find on tasks of its own
+    // sequence claimed before its own; a warp claims only when free, so every awaited word is produced
+    // by a running warp that is not (transitively) waiting on the waiter.
+    const bool streamer = kBulk && warp >= kWarps - kStreamWarps;
+    const uint32_t ND = kBulk ? gridDim.x * (kWarps - kStreamWarps) : gridDim.x * kWarps;
+    const uint32_t did = kBulk ? blockIdx.x * (kWarps - kStreamWarps) + warp : blockIdx.x * kWarps + warp;
+    if (!streamer)
+        for (uint32_t b = did; b < (uint32_t)P.B; b += ND) lead_decide<DT, GREEDY>(P, (int32_t)b, tab, lane);
+    if constexpr (!GREEDY) {
+        while (true) {
+            uint32_t t = 0;
+            if (lane == 0) t = atomicAdd(&P.ctr->claim, 1u);
+            t = __shfl_sync(0xFFFFFFFFu, t, 0);
+            if (t >= nStot) break;
+            s_task<DT, VEC>(P, t, tab, lane);
         }
-        if (!GREEDY) s_task<DT, VEC>(P, cl - (uint32_t)P.B, tab, lane);
     }
 }
 

@@ -209,3 +209,20 @@ def test_statistical_losslessness_on_gpu():
     assert abs(rate - beta) < 5 * np.sqrt(beta * (1 - beta) / N)
     r = parity.run_oracle(b, 2024, 0)
     assert np.array_equal(g["n"], r.num_accepted) and np.array_equal(g["tokens"], r.tokens)
+
+
+@pytest.mark.parametrize("name", ["b8_g4_v32000_t0.7", "b64_g5_v128256"])
+def test_rows_with_maximum_near_zero(name):
+    """Rows shifted so their maximum is -2^-20 (as log-probabilities of a confident model are): l - m
+    rounds in float for nearly every column of such rows, so the sampler carries its rounding error."""
+    b0 = synth.make_batch(name)
+
+    def shifted_bf16(bits):
+        x = synth.bf16_bits_to_f32(bits)
+        return synth.to_bf16_bits((x - x.max(1, keepdims=True) - np.float32(2.0 ** -20)).astype(np.float32))
+
+    b = synth.Batch(b0.workload, shifted_bf16(b0.target), shifted_bf16(b0.draft), b0.draft_tokens,
+                    b0.seq_offsets, b0.gammas)
+    m = synth.bf16_bits_to_f32(b.target).max(1)
+    assert np.all(np.abs(m) < 2.0 ** -19)  # these rows take the carried-rounding path
+    parity.assert_parity(b, 31, 2)
