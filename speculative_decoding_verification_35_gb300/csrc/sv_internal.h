@@ -17,7 +17,9 @@ constexpr int kSTask = 1024;                // vocabulary columns of one sampler
 constexpr int kScanBlock = 512;             // columns the find's element scan covers per pass
 constexpr int kScanPerLane = kScanBlock / 32;  // 16 consecutive columns per lane
 constexpr int kStreamWarps = 4;             // statistics streamers per CTA on the bulk-copy path
-constexpr int kStages = 3;                  // bulk-copy stages per streamer
+constexpr int kStages = 2;                  // bulk-copy stages per streamer (64 KB in flight per CTA:
+                                            // enough for the HBM rate, short enough that other requests
+                                            // and instruction fetches are not queued far behind)
 constexpr int kStageBytes = kAChunk * 2;    // one bf16 statistics task
 constexpr int kTmaSmemBytes = kStreamWarps * kStages * (kStageBytes + 8);
 constexpr int kBaseCache = 1024;            // batches up to this size keep their row bases in shared memory
