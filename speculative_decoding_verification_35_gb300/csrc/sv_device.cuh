@@ -225,6 +225,13 @@ __device__ __forceinline__ ff2 exp2_ff2(float2 l, float2 m, const ExpConst& C, c
     return ff2{mul2(h, sc), mul2(lo, sc)};
 }
 
+// 1.0f where a > b, else 0.0f (one instruction; false for NaN operands, like a > b)
+__device__ __forceinline__ float gt_mask(float a, float b) {
+    float r;
+    asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 // Split of a weight w in [0, 1] into a part on the 2^-20 grid (hi) and the rest (lo, |lo| <= 2^-21):
 // sums of up to 16 grid parts are exact in float, so an accumulator only needs plain adds.
 __device__ __forceinline__ float2 grid_hi(float2 w) { return add2(add2(w, f2(12.f)), f2(-12.f)); }

@@ -614,7 +614,8 @@ __device__ __forceinline__ float2 col2(const Cols16& c, int e) {
 // Residual selection of two columns: p > q, judged on the approximate normaliser ratio rho. The same
 // rule (same float operations) is applied by every step that sums or scans the residual.
 __device__ __forceinline__ float2 sel_mask(const ff2& ep, const ff2& eq, float rho) {
-    return make_float2(ep.hi.x > rho * eq.hi.x ? 1.f : 0.f, ep.hi.y > rho * eq.hi.y ? 1.f : 0.f);
+    const float2 rq = mul2(f2(rho), eq.hi);
+    return make_float2(gt_mask(ep.hi.x, rq.x), gt_mask(ep.hi.y, rq.y));
 }
 
 // Residual weight of a selected column, max(0, e_p - rho e_q) in float-float; 0 when not selected.
@@ -641,7 +642,7 @@ __device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& 
 // a 16-lane prefix picks the column. Returns the first column whose running sum exceeds `rem`, or the
 // last column of positive weight when the crossing is lost to rounding (or `tail_rule` asks for it).
 template <int DT, bool VEC>
-__device__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t prow, size_t qrow, bool resid, ff rho,
+__device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t prow, size_t qrow, bool resid, ff rho,
                                  int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, const float* tab, int lane) {
     const ExpConst EC = exp_const(P);
     // a unit spans at most kSTask columns: NB passes; bf16 issues every pass's loads first
@@ -722,7 +723,7 @@ __device__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t pro
 // after the tasks before. Rounding that loses the crossing (or tail_rule) picks the last group, then
 // column, of positive weight. Returns -1 when nothing in the task has positive weight, -2 on a time-out.
 template <int DT, bool VEC>
-__device__ int32_t group_search(const Params& P, int32_t b, int unit, const TaskInfo& tk, size_t prow, size_t qrow,
+__device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int unit, const TaskInfo& tk, size_t prow, size_t qrow,
                                 bool resid, ff rho, ff rem, bool tail_rule, const float* tab, int lane) {
     static_assert(kGroupCols == 4 * 32, "four columns per lane");
     const Word* gw = P.groupw + (((size_t)b * P.nS + unit) * kGroups + (lane % kGroups)) * kGroupWords;
@@ -1003,28 +1004,8 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
     // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
     float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
     float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
-    // a ring of D steps in flight: bf16 loads the whole task at once, fp32 two steps ahead
-    constexpr int kSteps = kSTask / 256;
-    constexpr int D = DT == SV_BF16 ? kSteps : 2;
-    Cols8 rp[D], rq[D];
-#pragma unroll
-    for (int d = 0; d < D; ++d) {
-        rp[d] = load_cols8<DT, VEC>(P.target, prow, P.V, cbase + 32 * lane + 8 * d);
-        if (resid) rq[d] = load_cols8<DT, VEC>(P.draft, qrow, P.V, cbase + 32 * lane + 8 * d);
-    }
-#pragma unroll 1
-    for (int e = 0; e < kSteps; ++e) {
-        const Cols8 cp = rp[0], cq = rq[0];
-#pragma unroll
-        for (int d = 0; d + 1 < D; ++d) {
-            rp[d] = rp[d + 1];
-            rq[d] = rq[d + 1];
-        }
-        if (e + D < kSteps) {
-            const int32_t k1 = cbase + 32 * lane + 8 * (e + D);
-            rp[D - 1] = load_cols8<DT, VEC>(P.target, prow, P.V, k1);
-            if (resid) rq[D - 1] = load_cols8<DT, VEC>(P.draft, qrow, P.V, k1);
-        }
+    // one step: 8 consecutive columns of the lane (4 pairs) of the p row, and of the q row for a residual
+    auto step = [&](const Cols8& cp, const Cols8& cq) {
         if (resid) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -1051,6 +1032,32 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
                 Pl = add2(Pl, add2(sub2(ep.hi, hp), ep.lo));
             }
         }
+    };
+    // a ring of D steps in flight: bf16 loads the whole task at once, fp32 two steps ahead. The step
+    // loop stays rolled: under the statistics stream, instruction fetches are slow, and this loop's
+    // code must stay small enough to remain cached.
+    constexpr int kSteps = kSTask / 256;
+    constexpr int D = DT == SV_BF16 ? kSteps : 2;
+    Cols8 rp[D], rq[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        rp[d] = load_cols8<DT, VEC>(P.target, prow, P.V, cbase + 32 * lane + 8 * d);
+        if (resid) rq[d] = load_cols8<DT, VEC>(P.draft, qrow, P.V, cbase + 32 * lane + 8 * d);
+    }
+#pragma unroll 1
+    for (int e = 0; e < kSteps; ++e) {
+        const Cols8 cp = rp[0], cq = rq[0];
+#pragma unroll
+        for (int d = 0; d + 1 < D; ++d) {
+            rp[d] = rp[d + 1];
+            rq[d] = rq[d + 1];
+        }
+        if (e + D < kSteps) {
+            const int32_t k1 = cbase + 32 * lane + 8 * (e + D);
+            rp[D - 1] = load_cols8<DT, VEC>(P.target, prow, P.V, k1);
+            if (resid) rq[D - 1] = load_cols8<DT, VEC>(P.draft, qrow, P.V, k1);
+        }
+        step(cp, cq);
     }
     // the group words first (read by the find only, which polls them): sums over kGroupLanes lanes
     ff ga = resid ? lane_ff(Ah, Al) : lane_ff(Ph, Pl), gb = resid ? lane_ff(Bh, Bl) : ff{0.f, 0.f};
@@ -1288,9 +1295,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     const int32_t* rows = !GREEDY && 2 * oB + P.B <= kRowCache ? s_row : nullptr;
 
     // Statistics. Bulk-copy path: the upper kStreamWarps warps of the CTA stream while the lower ones
-    // take tickets at once (the lower warps are the ones a partition's scheduler favours, so decisions
-    // and sampler work are not starved by the streamers). Other paths: every warp streams its strided
-    // tasks from registers first.
+    // decide and take sampler tasks at once. Other paths: every warp streams its strided tasks from
+    // registers first.
     if (kBulk) {
         if (warp >= kWarps - kStreamWarps) stream_bulk(P, nA, dsmem, bases, rows, warp - (kWarps - kStreamWarps), lane);
     } else {
