@@ -7,24 +7,32 @@
 //   p_i = softmax(l_target_i / T), q_i = softmax(l_draft_i / T); accept x_i while u_i q_i(x_i) < p_i(x_i);
 //   draw the first rejected slot from norm(max(0, p - q)), or a bonus token from p_gamma.
 //
-// Every warp of the grid is an independent worker that repeatedly takes one task:
+// Work items and who runs them (bf16 rows with 16-byte alignment take the bulk-copy path):
 //   statistics task (row r, 4096-column chunk c), in sequence-major order, statically strided over the
-//     warps: one streaming pass over the logits (16 x 16-byte loads in flight per lane) computing the
-//     raw max, the fp32 sum of exp((l - max) / T) and, greedy, the first argmax. This pass moves almost
-//     all HBM traffic. The warp that finishes the last statistics task of a sequence runs its decision.
-//   decision (one warp, one sequence): merge the chunk partials of each row, evaluate
-//     u_i * q_i(x_i) < p_i(x_i) in fp64 for every slot, find the first rejection with a ballot, write
-//     the accepted tokens and publish the sequence's sampler work (a per-sequence ready flag).
-//   sampler task (sequence b, 2048 columns), claimed in sequence order in preference to statistics work:
-//     the draw's weights (max(0, p - q), or p for a bonus) in float-float precision, summed per
-//     512-column sub-chunk. The rows were streamed moments earlier, so these reads hit L2. The warp that
-//     finishes the last sampler task of a sequence runs its find.
-//   find (one warp, one sequence): exact normalisers, then the inverse CDF in fp64 over the sub-chunk
-//     sums and over the 512 columns of the crossing sub-chunk.
-// Precision: the accept test tolerates fp32 statistics (its decision moves by ~1e-7 of p/q); the
-// inverse CDF over ~1e5 tokens does not, hence the float-float sampler with exact normalisers.
-// Waits: a warp out of statistics work waits for published sampler work with a bounded spin; the launch
-// is cooperative, so every CTA is resident and every awaited task is held by a running warp.
+//     streamer warps (the upper 4 warps of every CTA; every warp on the other paths): the chunk arrives
+//     by a 1-D bulk copy into a shared-memory ring (two stages per streamer, evict-first in L2), and
+//     the warp reduces it to the raw max and the fp32 sum of 2^((l - max) K) (greedy: first argmax).
+//     One 64-bit partial word per task. This pass moves all the algorithmic HBM traffic.
+//   decision (one warp per sequence, the lower warps of the CTAs by static slot): polls the sequence's
+//     partial words, merges each row (fp32 online rescaling), evaluates u q(x) < p(x) for every slot with
+//     a float-float exponential of the exact logit gap, takes the first rejection with a ballot, writes
+//     the accepted tokens and publishes the draw (mode, slot, row maxima, approximate normaliser ratio,
+//     uniform) as self-validating task words.
+//   sampler task (sequence b, 1024 columns), claimed from a counter in sequence-major order by any free
+//     warp: the draw's weights max(0, p - q) (or p for a bonus) in float-float precision, stored as four
+//     per-task sums and per-128-column group sums.
+//   find (run by the warp that claimed the sequence's last sampler task): exact normalisers from the
+//     task sums, the crossing task, the crossing group from its group sums, then the crossing column among
+//     the group's 128 columns recomputed with the same float-float weights.
+// Handoff: every word passed between warps is written once per call with one relaxed store into a
+// region zeroed before the call and is non-zero once written, so readers poll the words themselves
+// (bounded back-off); no fences, flags or counters order them.
+// Precision: the accept test tolerates fp32 statistics (its decision moves by ~1e-7 of p/q, inside the
+// 1e-6 band); the inverse CDF over ~1e5 tokens does not: a token boundary shifted by e is hit by the
+// uniform with probability ~(tokens of positive weight) x e, so every weight carries ~1e-9 relative
+// precision and the normalisers are exact sums of them.
+// Waits: every wait is bounded (then SV_ERR_TIMEOUT); the launch is cooperative, so every awaited word is
+// produced by a resident warp that is not waiting on the waiter.
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
