@@ -388,9 +388,20 @@ template <int DT, bool GREEDY>
 __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float* tab) {
     const int32_t t0 = o0 + b;
     const int nrows = stat_rows<GREEDY>(g);
-    const int32_t sbase = stat_base<GREEDY>(P, b);
+    const int32_t sbase = GREEDY ? o0 + b : 2 * o0 + b;
     const int nch = P.nchA;
     const float K = P.K_hi;
+    // Partial words of a block (8 rows from j0, the 32 chunks from c0), one row per register; rows past
+    // the sequence and chunks past the row read as 1 (never polled). The first block's loads are issued
+    // before anything else, and each next block's right after the current block's words are in.
+    auto load_block = [&](int j0, int c0, PartialWord (&q)[8]) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            q[k] = j0 + k < nrows && c0 + lane < nch
+                       ? ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c0 + lane) : 1ull;
+    };
+    PartialWord qn[8];
+    load_block(0, 0, qn);
     int32_t x = 0;
     uint32_t err = 0;
     float lt = 0.f, ld = 0.f, u_acc = 0.f, u_draw = 0.f;
@@ -423,7 +434,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 v[k] = j0 + k < nrows && c < nch;
-                q[k] = v[k] ? ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c) : 1ull;
+                q[k] = qn[k];
             }
             // words still 0 are statistics tasks in flight: poll them (bounded back-off)
             uint32_t spins = 0, ns = 64;
@@ -439,6 +450,10 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     if (q[k] == 0) q[k] = ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c);
+            }
+            {  // the next block's loads, in flight while this block is merged and reduced
+                const int nc0 = c0 + 32 < nch ? c0 + 32 : 0, nj0 = c0 + 32 < nch ? j0 : j0 + 8;
+                if (nj0 < nrows) load_block(nj0, nc0, qn);
             }
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -1174,8 +1189,16 @@ __device__ __forceinline__ void a_finish(const Params& P, const ATask& at, const
 
 // Decision of sequence b, run by its decider warp; it polls the partial words itself.
 template <int DT, bool GREEDY>
-__device__ void lead_decide(const Params& P, int32_t b, const float* tab, int lane) {
-    const int32_t o0 = __ldg(P.offs + b), g = __ldg(P.gammas + b);
+__device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, const float* tab, int lane) {
+    int32_t o0, g;
+    if (bases) {  // from the validated offsets cached in shared memory: no dependent global load
+        const int32_t s0 = bases[b], s1 = bases[b + 1];
+        o0 = GREEDY ? s0 - b : (s0 - b) >> 1;
+        g = GREEDY ? s1 - s0 - 1 : (s1 - s0 - 1) >> 1;
+    } else {
+        o0 = __ldg(P.offs + b);
+        g = __ldg(P.gammas + b);
+    }
     decide<DT, GREEDY>(P, b, g, o0, lane, tab);
 }
 
@@ -1275,9 +1298,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     if (tid == 0) s_bad = __ldg(P.offs) != 0;
     __syncthreads();
     // every CTA checks the whole CSR structure before any row is read (and caches small batches' row
-    // bases for the statistics tasks)
+    // bases, b = 0..B, for the statistics tasks and the decisions)
     int bad = 0;
-    const bool cache = P.B <= kBaseCache;
+    const bool cache = P.B < kBaseCache;
+    if (cache && tid == 0) {  // the end of the last sequence's rows
+        const int32_t oB = __ldg(P.offs + P.B);
+        s_base[P.B] = GREEDY ? oB + P.B : 2 * oB + P.B;
+    }
     for (int32_t b = tid; b < P.B; b += kThreads) {
         const int32_t o0 = __ldg(P.offs + b), o1 = __ldg(P.offs + b + 1), g = __ldg(P.gammas + b);
         const bool ok = g >= 0 && g <= P.max_gamma && o0 >= 0 && o1 - o0 == g;
@@ -1331,7 +1358,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     const uint32_t ND = kBulk ? gridDim.x * (kWarps - kStreamWarps) : gridDim.x * kWarps;
     const uint32_t did = kBulk ? blockIdx.x * (kWarps - kStreamWarps) + warp : blockIdx.x * kWarps + warp;
     if (!streamer)
-        for (uint32_t b = did; b < (uint32_t)P.B; b += ND) lead_decide<DT, GREEDY>(P, (int32_t)b, tab, lane);
+        for (uint32_t b = did; b < (uint32_t)P.B; b += ND) lead_decide<DT, GREEDY>(P, (int32_t)b, bases, tab, lane);
     if constexpr (!GREEDY) {
         while (true) {
             uint32_t t = 0;
