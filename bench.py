@@ -284,6 +284,28 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_e2e = float(t.item())
 
+    # post-verify update (spec_verify_commit) on the last call's outputs: the device-side append of the
+    # emitted tokens and the next input token, stream-ordered launches, no host sync between them
+    n_commit = 200
+    cap = 8 * n_commit
+    hist = torch.zeros((b.B, cap), dtype=torch.int32, device=dev)
+    lens = torch.zeros(b.B, dtype=torch.int32, device=dev)
+    nxt = torch.zeros(b.B, dtype=torch.int32, device=dev)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        call.commit(dev_buf["seq_offsets"], hist, cap, lens, nxt, stream=stream)  # warm
+        lens.zero_()
+        c0.record(stream)
+        for _ in range(n_commit):
+            if call.commit(dev_buf["seq_offsets"], hist, cap, lens, nxt, stream=stream) != sv.SV_OK:
+                raise RuntimeError("spec_verify_commit failed")
+        c1.record(stream)
+    stream.synchronize()
+    us_commit = c0.elapsed_time(c1) / n_commit * 1e3
+    if call.status_bits():
+        raise RuntimeError("device status bits set by the post-verify update")
+
     rows = b.verified_rows()
     value = rows * world / (ms * 1e-3)
     e2e_value = rows * world / (ms_e2e * 1e-3)
@@ -316,6 +338,9 @@ def main():
                     "steps": n_e2e, "ms_per_step": ms_e2e},
             "gpu_launches": args.steps * kernels_per_step,
             "clocks": clocks,
+            "post_verify_update": {"us_per_call": us_commit, "calls": n_commit, "B": b.B,
+                                   "launch": "spec_verify_commit, stream-ordered after the verify steps, "
+                                             "one kernel per call, no host sync"},
         }
         if world == 1 and args.cpu_seconds > 0:
             rate, cores, sample = cpu_oracle_rate(b, args.cpu_seconds)

@@ -58,7 +58,8 @@ typedef enum {
     SV_ERR_NONFINITE = 5,   /* device: NaN or +inf logit in a row the step reads */
     SV_ERR_EMPTY_ROW = 6,   /* device: a row whose logits are all -inf */
     SV_ERR_TIMEOUT = 7,     /* device: a bounded wait between warps of the launch gave up */
-    SV_ERR_WORKSPACE = 8    /* workspace NULL or smaller than spec_verify_workspace_size() */
+    SV_ERR_WORKSPACE = 8,   /* workspace NULL or smaller than spec_verify_workspace_size() */
+    SV_ERR_CAPACITY = 9     /* device (spec_verify_commit): a sequence's history would overflow */
 } sv_status;
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -135,6 +136,34 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_
                         int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
                         uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
                         uint32_t* device_status, const sv_debug* debug, void* cuda_stream);
+
+/*
+ * Post-verify update on the device ("Accelerating Sonar through speculation", §"MTP scheduling": once
+ * the drafts are verified, a kernel shifts the target's input tokens and inserts the next target token,
+ * so the host does not have to wait for the accepted length before the next step is issued). Enqueued
+ * on `cuda_stream` after spec_verify_ex on the same stream, it consumes that call's outputs on the
+ * device; nothing is copied to the host and the host does not synchronise.
+ *
+ *   for every sequence b with n = out_num_accepted[b] >= 0 and L = lengths[b]:
+ *     history[b * capacity + L + j] = out_tokens[seq_offsets[b] + b + j]   for j = 0..n
+ *     lengths[b] = L + n + 1;  next_tokens[b] = out_tokens[seq_offsets[b] + b + n]
+ *   (the n accepted drafts and the drawn token are appended; the drawn token is the next step's input
+ *   token, at position lengths[b] - 1).
+ *   A sequence with n < 0 (it failed verification) is left unchanged and gets next_tokens[b] = -1.
+ *   A sequence with n > seq_offsets[b+1] - seq_offsets[b] (inconsistent outputs) or with L < 0 or
+ *   L + n + 1 > capacity is left unchanged, gets next_tokens[b] = -1, and sets bit
+ *   (1u << SV_ERR_BAD_OFFSETS) or (1u << SV_ERR_CAPACITY) of *device_status (if not NULL).
+ *
+ * Arguments: out_tokens int32[seq_offsets[B] + B], out_num_accepted int32[B] and seq_offsets
+ * int32[B + 1] as spec_verify_ex wrote / read them; history int32[B * capacity], one row of capacity
+ * tokens per sequence; lengths int32[B] (read and updated); next_tokens int32[B] (written). All are
+ * DEVICE pointers owned by the caller, 4-byte aligned. Returns SV_ERR_INVALID_ARG for B < 0,
+ * capacity < 1 or a NULL / misaligned pointer (B > 0), SV_ERR_CUDA if the launch fails, else SV_OK
+ * (asynchronously: device-side findings go to *device_status).
+ */
+int spec_verify_commit(const int32_t* out_tokens, const int32_t* out_num_accepted, const int32_t* seq_offsets,
+                       int32_t B, int32_t* history, int32_t capacity, int32_t* lengths, int32_t* next_tokens,
+                       uint32_t* device_status, void* cuda_stream);
 
 /* Map a device status word (OR of 1u << code) to one status code, by the priority above. */
 int spec_verify_status_from_bits(uint32_t bits);

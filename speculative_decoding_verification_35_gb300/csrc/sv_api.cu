@@ -18,7 +18,7 @@ size_t spec_verify_workspace_size(int32_t B, int32_t V, int32_t max_gamma) {
 
 int spec_verify_status_from_bits(uint32_t bits) {
     static const int order[] = {SV_ERR_BAD_OFFSETS, SV_ERR_BAD_TOKEN, SV_ERR_NONFINITE, SV_ERR_EMPTY_ROW,
-                                SV_ERR_TIMEOUT};
+                                SV_ERR_TIMEOUT, SV_ERR_CAPACITY};
     for (int c : order)
         if (bits & (1u << c)) return c;
     for (int c = 1; c < 32; ++c)
@@ -37,6 +37,7 @@ const char* spec_verify_status_string(int status) {
         case SV_ERR_EMPTY_ROW: return "SV_ERR_EMPTY_ROW: a row whose logits are all -inf";
         case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a bounded device wait gave up";
         case SV_ERR_WORKSPACE: return "SV_ERR_WORKSPACE: workspace missing, too small or not 256-byte aligned";
+        case SV_ERR_CAPACITY: return "SV_ERR_CAPACITY: a sequence's token history would overflow its capacity";
         default: return "unknown status";
     }
 }

@@ -13,13 +13,13 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_CUDA, SV_ERR_BAD_TOKEN, SV_ERR_BAD_OFFSETS = 0, 1, 2, 3, 4
-SV_ERR_NONFINITE, SV_ERR_EMPTY_ROW, SV_ERR_TIMEOUT, SV_ERR_WORKSPACE = 5, 6, 7, 8
+SV_ERR_NONFINITE, SV_ERR_EMPTY_ROW, SV_ERR_TIMEOUT, SV_ERR_WORKSPACE, SV_ERR_CAPACITY = 5, 6, 7, 8, 9
 SV_F32, SV_BF16 = 0, 1
 SV_MAX_GAMMA = 31
 
 # every exported symbol of the C ABI, in header order
 EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
-           "spec_verify_status_from_bits", "spec_verify_status_string")
+           "spec_verify_commit", "spec_verify_status_from_bits", "spec_verify_status_string")
 
 
 class SvDebug(ctypes.Structure):
@@ -42,6 +42,8 @@ def _load():
     L.spec_verify_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
                                       vp, ctypes.POINTER(SvDebug), vp]
     L.spec_verify_noalloc.restype = ctypes.c_int
+    L.spec_verify_commit.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp]
+    L.spec_verify_commit.restype = ctypes.c_int
     L.spec_verify_status_from_bits.argtypes = [ctypes.c_uint32]
     L.spec_verify_status_from_bits.restype = ctypes.c_int
     L.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -82,6 +84,13 @@ def spec_verify_noalloc(target_logits, draft_logits, dtype, draft_tokens, seq_of
                                    max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
                                    device_status, ctypes.byref(debug) if debug is not None else None,
                                    cuda_stream)
+
+
+def spec_verify_commit(out_tokens, out_num_accepted, seq_offsets, B, history, capacity, lengths, next_tokens,
+                       device_status, cuda_stream) -> int:
+    """Post-verify update on the device. Pointer arguments are device addresses (int or None)."""
+    return lib.spec_verify_commit(out_tokens, out_num_accepted, seq_offsets, B, history, capacity, lengths,
+                                  next_tokens, device_status, cuda_stream)
 
 
 def spec_verify_status_from_bits(bits: int) -> int:
@@ -143,6 +152,13 @@ class Call:
                               _ptr(seq_offsets), _ptr(gammas), self.B, self.V, self.max_gamma, temperature,
                               seed, step, _ptr(self.out_tokens), _ptr(self.out_n), _ptr(self.status),
                               _ptr(self.workspace), self.ws_bytes, self.dbg_struct, st.cuda_stream)
+
+    def commit(self, seq_offsets, history, capacity, lengths, next_tokens, stream=None) -> int:
+        """Enqueue spec_verify_commit on this call's outputs (same stream, no host sync)."""
+        import torch
+        st = stream if stream is not None else torch.cuda.current_stream()
+        return spec_verify_commit(_ptr(self.out_tokens), _ptr(self.out_n), _ptr(seq_offsets), self.B, _ptr(history),
+                                  capacity, _ptr(lengths), _ptr(next_tokens), _ptr(self.status), st.cuda_stream)
 
     def status_bits(self) -> int:
         return int(self.status.item()) & 0xFFFFFFFF

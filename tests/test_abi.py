@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
-                          "spec_verify_status_from_bits", "spec_verify_status_string"}
+                          "spec_verify_commit", "spec_verify_status_from_bits", "spec_verify_status_string"}
 
 
 def test_library_exports_every_declared_symbol(libpath):
@@ -93,5 +93,24 @@ def test_status_helpers(libpath):
     assert sv.spec_verify_status_from_bits((1 << 5) | (1 << 3)) == sv.SV_ERR_BAD_TOKEN
     assert sv.spec_verify_status_from_bits((1 << 5) | (1 << 4)) == sv.SV_ERR_BAD_OFFSETS
     assert sv.spec_verify_status_from_bits(1 << 6) == sv.SV_ERR_EMPTY_ROW
-    for code in range(9):
+    assert sv.spec_verify_status_from_bits(1 << 9) == sv.SV_ERR_CAPACITY
+    for code in range(10):
         assert sv.spec_verify_status_string(code).startswith("SV_")
+
+
+def test_commit_host_side_checks_without_gpu(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    fake = 1 << 20  # never dereferenced: every call below returns before any CUDA call
+    args = dict(out_tokens=fake, out_num_accepted=fake, seq_offsets=fake, B=4, history=fake, capacity=16,
+                lengths=fake, next_tokens=fake, device_status=None, cuda_stream=None)
+
+    def call(**kw):
+        a = dict(args); a.update(kw)
+        return sv.spec_verify_commit(**a)
+
+    assert call(B=-1) == sv.SV_ERR_INVALID_ARG
+    assert call(capacity=0) == sv.SV_ERR_INVALID_ARG
+    assert call(history=None) == sv.SV_ERR_INVALID_ARG
+    assert call(lengths=fake + 2) == sv.SV_ERR_INVALID_ARG
+    assert call(device_status=fake + 1) == sv.SV_ERR_INVALID_ARG
+    assert call(B=0) == sv.SV_OK
