@@ -306,6 +306,39 @@ def main():
     if call.status_bits():
         raise RuntimeError("device status bits set by the post-verify update")
 
+    # the same steps with the update fused into the verify launch (spec_verify_fused), from a CUDA graph of
+    # G steps like the timed region above; the history grows by at most max_gamma + 1 tokens per step
+    n_fused = G * max(1, min(args.steps, 1000) // G)
+    fcap = (mg + 1) * (n_fused + G + 1)
+    fhist = torch.zeros((b.B, fcap), dtype=torch.int32, device=dev)
+    flens = torch.zeros(b.B, dtype=torch.int32, device=dev)
+    fnext = torch.zeros(b.B, dtype=torch.int32, device=dev)
+
+    def one_fused(i):
+        c = copies[i % ncopy]
+        rc = call.run_fused(c["target"], c["draft"], c["draft_tokens"], c["seq_offsets"], c["gammas"], w.temperature,
+                            seed, i, fhist, fcap, flens, fnext, stream=stream, clear_status=False)
+        if rc != sv.SV_OK:
+            raise RuntimeError(sv.spec_verify_status_string(rc))
+
+    fgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(fgraph, stream=stream):
+        for i in range(G):
+            one_fused(i)
+    fgraph.replay()  # warm (G steps of history)
+    stream.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(n_fused // G):
+            fgraph.replay()
+    f1.record(stream)
+    stream.synchronize()
+    ms_fused = f0.elapsed_time(f1) / n_fused
+    if call.status_bits():
+        raise RuntimeError("device status bits set by the fused steps")
+
     rows = b.verified_rows()
     value = rows * world / (ms * 1e-3)
     e2e_value = rows * world / (ms_e2e * 1e-3)
@@ -340,7 +373,10 @@ def main():
             "clocks": clocks,
             "post_verify_update": {"us_per_call": us_commit, "calls": n_commit, "B": b.B,
                                    "launch": "spec_verify_commit, stream-ordered after the verify steps, "
-                                             "one kernel per call, no host sync"},
+                                             "one kernel per call, no host sync",
+                                   "fused_ms_per_step": ms_fused, "fused_steps": n_fused,
+                                   "fused_extra_us_per_step": (ms_fused - ms) * 1e3,
+                                   "fused_launch": f"spec_verify_fused from a CUDA graph of {G} steps"},
         }
         if world == 1 and args.cpu_seconds > 0:
             rate, cores, sample = cpu_oracle_rate(b, args.cpu_seconds)

@@ -165,6 +165,21 @@ int spec_verify_commit(const int32_t* out_tokens, const int32_t* out_num_accepte
                        int32_t B, int32_t* history, int32_t capacity, int32_t* lengths, int32_t* next_tokens,
                        uint32_t* device_status, void* cuda_stream);
 
+/*
+ * The verify step with the post-verify update fused into it: spec_verify_ex on the same arguments
+ * (without debug output) followed by the update spec_verify_commit describes, done inside the verify
+ * launch by the warp that writes each sequence's final token, so no second kernel is launched. History,
+ * lengths and next tokens follow spec_verify_commit; a sequence that fails verification keeps its
+ * history and length and gets next token -1. Returns SV_ERR_INVALID_ARG for capacity < 1 or a NULL /
+ * misaligned history, lengths or next_tokens (B > 0), else as spec_verify_ex.
+ */
+int spec_verify_fused(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                      int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed, uint64_t step,
+                      int32_t* out_tokens, int32_t* out_num_accepted, uint32_t* device_status, void* workspace,
+                      size_t workspace_bytes, int32_t* history, int32_t capacity, int32_t* lengths,
+                      int32_t* next_tokens, void* cuda_stream);
+
 /* Map a device status word (OR of 1u << code) to one status code, by the priority above. */
 int spec_verify_status_from_bits(uint32_t bits);
 

@@ -42,12 +42,21 @@ const char* spec_verify_status_string(int status) {
     }
 }
 
-int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype,
-                   const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
-                   int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
-                   uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
-                   uint32_t* device_status, void* workspace, size_t workspace_bytes,
-                   const sv_debug* debug, void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+struct CommitBufs {
+    int32_t* history;
+    int32_t capacity;
+    int32_t* lengths;
+    int32_t* next_tokens;
+};
+
+int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dtype, const int32_t* draft_tokens,
+                const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, int32_t max_gamma,
+                float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                uint32_t* device_status, void* workspace, size_t workspace_bytes, const sv_debug* debug,
+                const CommitBufs* commit, void* cuda_stream) {
     if (B < 0 || V < 1 || max_gamma < 0 || max_gamma > SV_MAX_GAMMA) return SV_ERR_INVALID_ARG;
     if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
     if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
@@ -106,8 +115,47 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
     P.recw = (Word*)(ws + L.recw);
     P.groupw = (Word*)(ws + L.groupw);
     P.ctr = (Counters*)(ws + L.counters);
+    if (commit) {
+        P.hist = commit->history;
+        P.cap = commit->capacity;
+        P.lens = commit->lengths;
+        P.next = commit->next_tokens;
+    }
     const cudaError_t e = launch_verify(P, L, workspace, (int)dtype, vec, greedy, (cudaStream_t)cuda_stream);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                   const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                   int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
+                   uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                   uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                   const sv_debug* debug, void* cuda_stream) {
+    return verify_impl(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                       temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
+                       workspace_bytes, debug, nullptr, cuda_stream);
+}
+
+int spec_verify_fused(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                      int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed, uint64_t step,
+                      int32_t* out_tokens, int32_t* out_num_accepted, uint32_t* device_status, void* workspace,
+                      size_t workspace_bytes, int32_t* history, int32_t capacity, int32_t* lengths,
+                      int32_t* next_tokens, void* cuda_stream) {
+    if (capacity < 1) return SV_ERR_INVALID_ARG;
+    if (B > 0) {
+        const void* ptrs[] = {history, lengths, next_tokens};
+        for (const void* p : ptrs)
+            if (!p || (uintptr_t)p % 4) return SV_ERR_INVALID_ARG;
+        if (max_gamma > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;  // the appended drafts
+    }
+    const CommitBufs c{history, capacity, lengths, next_tokens};
+    return verify_impl(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                       temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
+                       workspace_bytes, nullptr, &c, cuda_stream);
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,

@@ -91,6 +91,11 @@ struct Params {
     Word* recw;             // [B * nS * kRecWords]
     Word* groupw;           // [B * nS * kGroups * kGroupWords]
     Counters* ctr;
+    // fused post-verify update (spec_verify_fused); hist == nullptr: none
+    int32_t* hist;
+    int32_t cap;
+    int32_t* lens;
+    int32_t* next;
     float2 exp2_tab[64];  // 2^(j/64), j = 0..63, as (hi, lo) floats, built on the host
 };
 

@@ -337,6 +337,32 @@ __device__ __forceinline__ SegStats seg_stats(const char* rowp, int len, int lan
 }
 
 // ------------------------------------------------------------------------------------------------
+// Fused post-verify update (spec_verify_fused; "Accelerating Sonar through speculation",
+// §"MTP scheduling"): run by the one warp that writes a sequence's final token, after writing it. It
+// appends the n accepted drafts and the drawn token to the sequence's history at its length, advances
+// the length and writes the next input token; a failed sequence (n < 0) gets next token -1, and one
+// whose history would overflow is left as it is with next token -1 and SV_ERR_CAPACITY.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void commit_seq(const Params& P, int32_t b, int32_t n, int32_t o0, int32_t drawn, int lane) {
+    if (!P.hist) return;
+    const int32_t L = n >= 0 ? P.lens[b] : 0;
+    if (n < 0 || L < 0 || (int64_t)L + n + 1 > P.cap) {
+        if (lane == 0) {
+            P.next[b] = -1;
+            if (n >= 0) atomicOr(P.status, 1u << SV_ERR_CAPACITY);
+        }
+        return;
+    }
+    int32_t* h = P.hist + (size_t)b * (size_t)P.cap + (size_t)L;
+    if (lane < n) h[lane] = __ldg(P.tokens + o0 + lane);  // the accepted drafts
+    if (lane == n) h[n] = drawn;
+    if (lane == 0) {
+        P.lens[b] = L + n + 1;
+        P.next[b] = drawn;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
 // Sampler work of a sequence (see kTaskWords)
 // ------------------------------------------------------------------------------------------------
 struct TaskInfo {
@@ -528,6 +554,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         }
         if (!GREEDY) put_task(P, b, lane, kModeNone, 0, 0.f, 0.f, 1.f, 0.f);
         for (int32_t j = lane; j <= g; j += 32) P.out_tokens[t0 + j] = -1;
+        commit_seq(P, b, -1, o0, -1, lane);
         return;
     }
     if (GREEDY) {
@@ -537,6 +564,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         const int n = mism ? __ffs(mism) - 1 : g;
         if (lane <= g) P.out_tokens[t0 + lane] = lane < n ? x : (lane == n ? a : -1);
         if (lane == 0) P.out_n[b] = n;
+        commit_seq(P, b, n, o0, __shfl_sync(0xFFFFFFFFu, a, n), lane);
         return;
     }
     // the draft row of slot `lane` is statistics row g + 1 + lane: lane (g+1+lane) & 31, register >> 5
@@ -874,10 +902,16 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
     ff lp{0.f, 0.f}, lq{0.f, 0.f}, la{0.f, 0.f}, lb{0.f, 0.f};
     ff ka[4], kb[4];  // the lane's first four tasks, kept for the crossing search
     const int nchunk = (per + 3) / 4;  // the same on every lane
-    if (!__all_sync(0xFFFFFFFFu, poll4(s0, lp, lq, la, lb, ka, kb))) return;
+    if (!__all_sync(0xFFFFFFFFu, poll4(s0, lp, lq, la, lb, ka, kb))) {
+        commit_seq(P, b, -1, 0, -1, lane);  // timed out (reported in the status word)
+        return;
+    }
     for (int q = 1; q < nchunk; ++q) {
         ff va[4], vb[4];
-        if (!__all_sync(0xFFFFFFFFu, poll4(s0 + 4 * q, lp, lq, la, lb, va, vb))) return;
+        if (!__all_sync(0xFFFFFFFFu, poll4(s0 + 4 * q, lp, lq, la, lb, va, vb))) {
+            commit_seq(P, b, -1, 0, -1, lane);
+            return;
+        }
     }
     const ff sp = warp_sum_ff(lp);
     bool resid = tk.mode == kModeResidual;
@@ -969,6 +1003,7 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
         P.out_tokens[out_pos] = token;
         if (P.dbg.seq_mass) P.dbg.seq_mass[b] = ((double)S.hi + (double)S.lo) / ((double)sp.hi + (double)sp.lo);
     }
+    commit_seq(P, b, token >= 0 ? tk.n : -1, out_pos - b - tk.n, token, lane);
 }
 
 // 8 consecutive columns k0 .. k0 + 7 of `row`, packed (bf16: 4 words; fp32: 8 words); -inf past V.
@@ -1318,7 +1353,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     const int32_t* bases = cache ? s_base : nullptr;
     if (__syncthreads_or(bad) || s_bad) {
         if (blockIdx.x == 0) {
-            for (int32_t b = tid; b < P.B; b += kThreads) P.out_n[b] = -1;
+            for (int32_t b = tid; b < P.B; b += kThreads) {
+                P.out_n[b] = -1;
+                if (P.hist) P.next[b] = -1;
+            }
             if (tid == 0) atomicOr(P.status, 1u << SV_ERR_BAD_OFFSETS);
         }
         return;

@@ -19,7 +19,7 @@ SV_MAX_GAMMA = 31
 
 # every exported symbol of the C ABI, in header order
 EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
-           "spec_verify_commit", "spec_verify_status_from_bits", "spec_verify_status_string")
+           "spec_verify_commit", "spec_verify_fused", "spec_verify_status_from_bits", "spec_verify_status_string")
 
 
 class SvDebug(ctypes.Structure):
@@ -44,6 +44,9 @@ def _load():
     L.spec_verify_noalloc.restype = ctypes.c_int
     L.spec_verify_commit.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, vp, vp]
     L.spec_verify_commit.restype = ctypes.c_int
+    L.spec_verify_fused.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp, vp, sz,
+                                    vp, i32, vp, vp, vp]
+    L.spec_verify_fused.restype = ctypes.c_int
     L.spec_verify_status_from_bits.argtypes = [ctypes.c_uint32]
     L.spec_verify_status_from_bits.restype = ctypes.c_int
     L.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -91,6 +94,16 @@ def spec_verify_commit(out_tokens, out_num_accepted, seq_offsets, B, history, ca
     """Post-verify update on the device. Pointer arguments are device addresses (int or None)."""
     return lib.spec_verify_commit(out_tokens, out_num_accepted, seq_offsets, B, history, capacity, lengths,
                                   next_tokens, device_status, cuda_stream)
+
+
+def spec_verify_fused(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                      temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
+                      workspace_bytes, history, capacity, lengths, next_tokens, cuda_stream) -> int:
+    """Verify step with the post-verify update fused in. Pointer arguments are device addresses."""
+    return lib.spec_verify_fused(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V,
+                                 max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
+                                 device_status, workspace, workspace_bytes, history, capacity, lengths,
+                                 next_tokens, cuda_stream)
 
 
 def spec_verify_status_from_bits(bits: int) -> int:
@@ -159,6 +172,19 @@ class Call:
         st = stream if stream is not None else torch.cuda.current_stream()
         return spec_verify_commit(_ptr(self.out_tokens), _ptr(self.out_n), _ptr(seq_offsets), self.B, _ptr(history),
                                   capacity, _ptr(lengths), _ptr(next_tokens), _ptr(self.status), st.cuda_stream)
+
+    def run_fused(self, target, draft, draft_tokens, seq_offsets, gammas, temperature, seed, step, history,
+                  capacity, lengths, next_tokens, stream=None, clear_status=True) -> int:
+        """Enqueue spec_verify_fused (verify + post-verify update in one launch) on the given stream."""
+        import torch
+        if clear_status:
+            self.status.zero_()
+        st = stream if stream is not None else torch.cuda.current_stream()
+        return spec_verify_fused(_ptr(target), _ptr(draft), dtype_code(target), _ptr(draft_tokens),
+                                 _ptr(seq_offsets), _ptr(gammas), self.B, self.V, self.max_gamma, temperature,
+                                 seed, step, _ptr(self.out_tokens), _ptr(self.out_n), _ptr(self.status),
+                                 _ptr(self.workspace), self.ws_bytes, _ptr(history), capacity, _ptr(lengths),
+                                 _ptr(next_tokens), st.cuda_stream)
 
     def status_bits(self) -> int:
         return int(self.status.item()) & 0xFFFFFFFF

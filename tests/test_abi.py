@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
-                          "spec_verify_commit", "spec_verify_status_from_bits", "spec_verify_status_string"}
+                          "spec_verify_commit", "spec_verify_fused", "spec_verify_status_from_bits",
+                          "spec_verify_status_string"}
 
 
 def test_library_exports_every_declared_symbol(libpath):
@@ -114,3 +115,22 @@ def test_commit_host_side_checks_without_gpu(libpath):
     assert call(lengths=fake + 2) == sv.SV_ERR_INVALID_ARG
     assert call(device_status=fake + 1) == sv.SV_ERR_INVALID_ARG
     assert call(B=0) == sv.SV_OK
+
+
+def test_fused_host_side_checks_without_gpu(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    fake = 1 << 20  # never dereferenced: every call below fails its host checks first
+    args = dict(target_logits=fake, draft_logits=fake, dtype=sv.SV_BF16, draft_tokens=fake, seq_offsets=fake,
+                gammas=fake, B=4, V=100, max_gamma=4, temperature=1.0, seed=1, step=0, out_tokens=fake,
+                out_num_accepted=fake, device_status=None, workspace=fake, workspace_bytes=1 << 30, history=fake,
+                capacity=64, lengths=fake, next_tokens=fake, cuda_stream=None)
+
+    def call(**kw):
+        a = dict(args); a.update(kw)
+        return sv.spec_verify_fused(**a)
+
+    assert call(capacity=0) == sv.SV_ERR_INVALID_ARG
+    assert call(history=None) == sv.SV_ERR_INVALID_ARG
+    assert call(next_tokens=fake + 2) == sv.SV_ERR_INVALID_ARG
+    assert call(temperature=-1.0) == sv.SV_ERR_INVALID_ARG
+    assert call(workspace=None) == sv.SV_ERR_WORKSPACE

@@ -80,3 +80,51 @@ def test_verify_then_commit_over_steps_without_host_sync(name):
     assert np.array_equal(hist.cpu().numpy(), rh)
     assert np.array_equal(lens.cpu().numpy(), rl)
     assert np.array_equal(nxt.cpu().numpy(), rn)
+
+
+@pytest.mark.parametrize("name", ["b64_g5_v128256", "b8_g4_v32000_greedy", "ragged_b128_v129280", "b1_g4_v1024_f32"])
+def test_fused_update_matches_oracle_over_steps(name):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    b = synth.make_batch(name)
+    d = parity.to_device(b)
+    cap = 48
+    call = sv.Call(b.B, b.V, int(b.gammas.max()), b.R_t, b.R_d)
+    hist = torch.zeros((b.B, cap), dtype=torch.int32, device="cuda")
+    lens = torch.zeros(b.B, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(b.B, dtype=torch.int32, device="cuda")
+    rh, rl = np.zeros((b.B, cap), np.int32), np.zeros(b.B, np.int32)
+    for step in range(3):
+        assert call.run_fused(d["target"], d["draft"], d["draft_tokens"], d["seq_offsets"], d["gammas"],
+                              b.temperature, 1234, step, hist, cap, lens, nxt) == sv.SV_OK
+        torch.cuda.synchronize()
+        r = parity.run_oracle(b, 1234, step)
+        assert np.array_equal(call.out_n.cpu().numpy(), r.num_accepted)
+        assert np.array_equal(call.out_tokens.cpu().numpy(), r.tokens)
+        rh, rl, rn, rs = commit(r.tokens, r.num_accepted, b.seq_offsets, rh, cap, rl)
+        assert call.status_bits() == rs == 0
+        assert np.array_equal(hist.cpu().numpy(), rh)
+        assert np.array_equal(lens.cpu().numpy(), rl)
+        assert np.array_equal(nxt.cpu().numpy(), rn)
+
+
+def test_fused_update_overflow_and_failed_sequences():
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    b = synth.make_batch("ragged_b128_v129280", B=9, V=3001)
+    b.draft_tokens[int(b.seq_offsets[2])] = b.V + 5  # sequence 2 fails verification (bad token)
+    d = parity.to_device(b)
+    cap = 8
+    call = sv.Call(b.B, b.V, int(b.gammas.max()), b.R_t, b.R_d)
+    lens0 = np.array([0, 7, 0, 3, 8, 1, 2, 6, 0], np.int32)  # some cannot take n + 1 more tokens
+    hist = torch.full((b.B, cap), 77, dtype=torch.int32, device="cuda")
+    lens = torch.from_numpy(lens0.copy()).cuda()
+    nxt = torch.zeros(b.B, dtype=torch.int32, device="cuda")
+    assert call.run_fused(d["target"], d["draft"], d["draft_tokens"], d["seq_offsets"], d["gammas"], b.temperature,
+                          7, 0, hist, cap, lens, nxt) == sv.SV_OK
+    torch.cuda.synchronize()
+    r = parity.run_oracle(b, 7, 0)
+    rh, rl, rn, rs = commit(r.tokens, r.num_accepted, b.seq_offsets, np.full((b.B, cap), 77, np.int32), cap, lens0)
+    assert rn[2] == -1 and rs & (1 << sv.SV_ERR_CAPACITY)
+    assert call.status_bits() == rs | r.status
+    assert np.array_equal(hist.cpu().numpy(), rh)
+    assert np.array_equal(lens.cpu().numpy(), rl)
+    assert np.array_equal(nxt.cpu().numpy(), rn)
