@@ -68,8 +68,8 @@ def lib():
             L.oracle_verify.restype = ctypes.c_uint32
             L.oracle_draw_bracket.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                               ctypes.c_int32, ctypes.c_double, ctypes.c_double,
-                                              ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
-                                              ctypes.c_void_p]
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p]
             L.oracle_draw_bracket.restype = ctypes.c_int32
             _lib = L
     return _lib
@@ -131,7 +131,8 @@ def verify(target, draft, draft_tokens, seq_offsets, gammas, V, temperature, see
     """Verify a CSR-packed batch on host arrays.
 
     target/draft: numpy arrays of float32 logits, or uint16 arrays holding raw bf16 bits, with
-    shapes [R_t, V] / [R_d, V]. Returns a ``Result`` with tokens, counts and debug values.
+    shapes [R_t, V] / [R_d, V]. draft None with temperature > 0: the drafts are point masses (an
+    n-gram drafter's). Returns a ``Result`` with tokens, counts and debug values.
     """
     target = np.ascontiguousarray(target)
     dtype = BF16 if target.dtype == np.uint16 else F32
@@ -158,8 +159,9 @@ def verify(target, draft, draft_tokens, seq_offsets, gammas, V, temperature, see
     return res
 
 
-def draw_bracket(trow, drow, V, temperature, u, k_query):
-    """(token, C_{k-1}/S, C_k/S, S) of one inverse-CDF draw; see ``oracle_draw_bracket``."""
+def draw_bracket(trow, drow, V, temperature, u, k_query, x_excl=-1):
+    """(token, C_{k-1}/S, C_k/S, S) of one inverse-CDF draw; see ``oracle_draw_bracket``
+    (x_excl >= 0 with drow None: the residual of a point-mass draft at x_excl)."""
     trow = np.ascontiguousarray(trow)
     dtype = BF16 if trow.dtype == np.uint16 else F32
     if dtype == F32:
@@ -168,5 +170,5 @@ def draw_bracket(trow, drow, V, temperature, u, k_query):
         drow = np.ascontiguousarray(drow).astype(trow.dtype, copy=False)
     lo = np.zeros(1); hi = np.zeros(1); S = np.zeros(1)
     tok = lib().oracle_draw_bracket(_ptr(trow), _ptr(drow), dtype, V, float(temperature), float(u),
-                                    int(k_query), _ptr(lo), _ptr(hi), _ptr(S))
+                                    int(x_excl), int(k_query), _ptr(lo), _ptr(hi), _ptr(S))
     return tok, float(lo[0]), float(hi[0]), float(S[0])

@@ -31,6 +31,10 @@
  *   - the residual normaliser S is the direct sum of max(0, p - q) (equal to 1 - beta in exact
  *     arithmetic); if it is exactly 0 the draw falls back to p.
  *   - greedy (T == 0): argmax of the raw target logits, lowest index on ties.
+ *   - drafts without a draft distribution (an n-gram drafter, [velog] §"drafter types": the tokens
+ *     that followed an earlier occurrence of the last n tokens): no draft rows are given (draft NULL
+ *     with T > 0), and q_i is the point mass at x_i. The rule above is applied unchanged: accept iff
+ *     u < p(x), residual p with x removed.
  *   - uniform u = (Philox4x32-10(ctr, key).x0 >> 8) * 2^-24 with key = (lo32 seed, hi32 seed),
  *     ctr = (lo32 step, hi32 step, seq, (slot << 8) | purpose); purpose 0 = accept test of
  *     slot i, purpose 1 = residual/bonus draw at the emitting slot.
@@ -280,7 +284,13 @@ static void verify_one(job_t* J, int32_t b, double* prow, double* qrow, double* 
         int e = row_softmax(J->target, J->dtype, (size_t)(t0 + i), V, J->T, prow + (size_t)i * V, &lse);
         if (e) { fail_seq(J, b, e); return; }
         if (J->dbg && J->dbg->row_lse) J->dbg->row_lse[t0 + i] = lse;
-        if (i < g) {
+        if (i < g && !J->draft) { /* point-mass draft: q_i = 1 at x_i, 0 elsewhere */
+            double* qi = qrow + (size_t)i * V;
+            for (int32_t k = 0; k < V; ++k) qi[k] = 0.0;
+            qi[x[i]] = 1.0;
+            if (J->dbg && J->dbg->p_x) J->dbg->p_x[d0 + i] = prow[(size_t)i * V + x[i]];
+            if (J->dbg && J->dbg->q_x) J->dbg->q_x[d0 + i] = 1.0;
+        } else if (i < g) {
             e = row_softmax(J->draft, J->dtype, (size_t)(d0 + i), V, J->T, qrow + (size_t)i * V, &lse);
             if (e) { fail_seq(J, b, e); return; }
             if (J->dbg && J->dbg->row_lse) J->dbg->row_lse[R_t + d0 + i] = lse;
@@ -330,9 +340,8 @@ uint32_t oracle_verify(const void* target, const void* draft, int dtype, const i
     for (int32_t b = 0; b < B; ++b)
         if (gammas[b] < 0 || seq_offsets[b + 1] - seq_offsets[b] != gammas[b]) return 1u << OR_ERR_BAD_OFFSETS;
     if (B == 0) return 0;
-    /* draft rows are read only in sampling mode, and only when some sequence has gamma > 0 */
-    if (seq_offsets[B] > 0 && (!draft_tokens || (temperature > 0.0 && !draft)))
-        return 1u << OR_ERR_INVALID_ARG;
+    /* draft rows are read only in sampling mode; without them the drafts are point masses */
+    if (seq_offsets[B] > 0 && !draft_tokens) return 1u << OR_ERR_INVALID_ARG;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > B) nthreads = B;
     job_t* jobs = (job_t*)calloc((size_t)nthreads, sizeof(job_t));
@@ -360,11 +369,13 @@ uint32_t oracle_verify(const void* target, const void* draft, int dtype, const i
 /*
  * Inverse-CDF bracket of one token for a single draw, used to classify a disagreement as lying
  * inside the decision band. trow/drow point at one target / draft row (drow NULL: draw from p
- * alone, as for the bonus token). Returns the drawn token for uniform u and writes the running
+ * alone, as for the bonus token, or, with x_excl >= 0, from the residual of a point-mass draft at
+ * x_excl: p with x_excl removed). Returns the drawn token for uniform u and writes the running
  * sums C_{k-1}/S and C_k/S of token k_query and the normaliser S.
  */
 int32_t oracle_draw_bracket(const void* trow, const void* drow, int dtype, int32_t V, double T,
-                            double u, int32_t k_query, double* c_lo, double* c_hi, double* S_out) {
+                            double u, int32_t x_excl, int32_t k_query, double* c_lo, double* c_hi,
+                            double* S_out) {
     double* p = (double*)malloc(sizeof(double) * (size_t)V);
     double* q = (double*)malloc(sizeof(double) * (size_t)V);
     double* w = (double*)malloc(sizeof(double) * (size_t)V);
@@ -374,8 +385,10 @@ int32_t oracle_draw_bracket(const void* trow, const void* drow, int dtype, int32
     if (drow) {
         if (row_softmax(drow, dtype, 0, V, T, q, NULL)) goto done;
         for (int32_t k = 0; k < V; ++k) { w[k] = p[k] > q[k] ? p[k] - q[k] : 0.0; S += w[k]; }
+    } else if (x_excl >= 0 && x_excl < V) { /* point mass at x_excl: max(0, p - q) */
+        for (int32_t k = 0; k < V; ++k) { w[k] = k == x_excl ? 0.0 : p[k]; S += w[k]; }
     }
-    if (!drow || S == 0.0) {
+    if ((!drow && !(x_excl >= 0 && x_excl < V)) || S == 0.0) {
         S = 0.0;
         for (int32_t k = 0; k < V; ++k) { w[k] = p[k]; S += w[k]; }
     }

@@ -65,7 +65,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     const float K_hi = (float)K64;
     if (!greedy && !std::isfinite(K_hi)) return SV_ERR_INVALID_ARG;
     if (!target_logits || !seq_offsets || !gammas || !out_tokens || !out_num_accepted) return SV_ERR_INVALID_ARG;
-    if (max_gamma > 0 && (!draft_tokens || (!greedy && !draft_logits))) return SV_ERR_INVALID_ARG;
+    if (max_gamma > 0 && !draft_tokens) return SV_ERR_INVALID_ARG;  // no draft logits: point-mass drafts
     const size_t esz = dtype == SV_BF16 ? 2 : 4;
     if ((uintptr_t)target_logits % esz || (draft_logits && (uintptr_t)draft_logits % esz)) return SV_ERR_INVALID_ARG;
     if ((uintptr_t)seq_offsets % 4 || (uintptr_t)gammas % 4 || (uintptr_t)out_tokens % 4 ||
@@ -79,7 +79,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     const Layout L = workspace_layout(B, V, max_gamma);
     if (!workspace || workspace_bytes < L.total || (uintptr_t)workspace % 256) return SV_ERR_WORKSPACE;
 
-    const bool uses_draft = !greedy && max_gamma > 0;
+    const bool uses_draft = !greedy && max_gamma > 0 && draft_logits;
     const bool vec = (uintptr_t)target_logits % 16 == 0 && (!uses_draft || (uintptr_t)draft_logits % 16 == 0) &&
                      ((size_t)V * esz) % 16 == 0;
     char* ws = (char*)workspace;
@@ -92,6 +92,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.B = B;
     P.V = V;
     P.max_gamma = max_gamma;
+    P.pm = !greedy && !draft_logits;
     P.nchA = (V + kAChunk - 1) / kAChunk;
     P.nS = (V + kSTask - 1) / kSTask;
     P.nS_recip = P.nS >= 2 ? ~0ull / (unsigned long long)P.nS + 1ull : 0ull;

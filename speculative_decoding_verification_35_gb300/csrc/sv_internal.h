@@ -26,7 +26,8 @@ constexpr int kBaseCache = 1024;            // batches up to this size keep thei
 constexpr int kRowCache = 2048;             // sampling batches with up to this many statistics rows keep a
                                             // row map (target or draft, row index) in shared memory
 
-enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2 };
+// kModeResidualPM: the residual of a point-mass draft (no draft rows): p with the draft column removed
+enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2, kModeResidualPM = 3 };
 
 // Data handed between warps of one launch is written as 64-bit words, each exactly once per call with
 // one relaxed store, into a region zeroed before the call, and each non-zero once written. A reader
@@ -41,7 +42,9 @@ typedef Word PartialWord;
 
 // A sequence's sampler work, written by its decision as kTaskWords words:
 //   w0 = (0x80000000 | mode << 8 | n) << 32 | bits(m_p)   mode kMode*, n the emitting slot
-//   w1 = bits(rho) << 32 | bits(m_q)                      rho = approximate s_p / s_q (> 0)
+//   w1 = bits(rho) << 32 | bits(m_q)                      rho = approximate s_p / s_q (> 0);
+//                                                         kModeResidualPM: (x + 1) << 32, x the
+//                                                         draft token (the column the draw removes)
 //   w2 = 0x80000000 << 32 | bits(u)                       u the draw's uniform
 // m_p, m_q are the raw-logit maxima of the draw's target and draft rows.
 constexpr int kTaskWords = 4;
@@ -50,7 +53,9 @@ constexpr uint32_t kWordMark = 0x80000000u;
 // A sampler task's record, kRecWords words: word k = bits(lo) << 32 | (bits(hi) | 0x80000000) of a
 // non-negative float-float sum over the task's columns of the weights 2^((l - m) K):
 //   k = 0: all p weights, 1: all q weights, 2: p weights of the selected columns, 3: q weights of the
-//   selected columns (a bonus draw stores its p total as 0 and 2, zeros as 1 and 3).
+//   selected columns (a bonus draw stores its p total as 0 and 2, zeros as 1 and 3; the residual of a
+//   point-mass draft stores its p total as 0, the total without the removed column as 2, zeros as 1
+//   and 3).
 constexpr int kRecWords = 4;
 // Per group of kGroupLanes lanes of a sampler task (lane L covers the task's columns [32 L, 32 L + 32),
 // so group G covers [128 G, 128 G + 128)): two words, the group's selected p weights and selected q
@@ -74,6 +79,7 @@ struct Params {
     const int32_t* offs;
     const int32_t* gammas;
     int32_t B, V, max_gamma;
+    int32_t pm;        // point-mass drafts: sampling without draft rows (q_i = 1 at x_i)
     int32_t nchA;      // statistics chunks per row
     int32_t nS;        // sampler tasks per sequence
     unsigned long long nS_recip;  // floor(2^64 / nS) + 1 (nS >= 2): c / nS = high 64 bits of c * nS_recip

@@ -133,12 +133,12 @@ __device__ __forceinline__ ff exclusive_of(ff incl, int lane) {
 // CSR helpers (the offsets are validated by every CTA before any row is read).
 // ------------------------------------------------------------------------------------------------
 template <bool GREEDY>
-__device__ __forceinline__ int32_t stat_rows(int32_t g) { return GREEDY ? g + 1 : 2 * g + 1; }
+__device__ __forceinline__ int32_t stat_rows(const Params& P, int32_t g) { return GREEDY || P.pm ? g + 1 : 2 * g + 1; }
 
 template <bool GREEDY>
 __device__ __forceinline__ int32_t stat_base(const Params& P, int32_t b) {
     const int32_t o = __ldg(P.offs + b);
-    return GREEDY ? o + b : 2 * o + b;
+    return GREEDY || P.pm ? o + b : 2 * o + b;
 }
 
 template <int DT>
@@ -368,6 +368,7 @@ __device__ __forceinline__ void commit_seq(const Params& P, int32_t b, int32_t n
 struct TaskInfo {
     int32_t mode, n;
     float m_p, m_q, rho, u;
+    int32_t xcl;  // kModeResidualPM: the column the draw removes (the draft token); else -1
 };
 
 // Written by the decision (lanes 0-2 store one word each).
@@ -401,6 +402,11 @@ __device__ __forceinline__ bool get_task(const Params& P, int32_t b, int lane, T
     t.m_q = __uint_as_float((uint32_t)w1);
     t.rho = __uint_as_float((uint32_t)(w1 >> 32));
     t.u = __uint_as_float((uint32_t)w2);
+    t.xcl = -1;
+    if (t.mode == kModeResidualPM) {
+        t.xcl = (int32_t)(w1 >> 32) - 1;
+        t.rho = 1.f;
+    }
     return true;
 }
 
@@ -413,8 +419,8 @@ __device__ __forceinline__ bool get_task(const Params& P, int32_t b, int lane, T
 template <int DT, bool GREEDY>
 __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float* tab) {
     const int32_t t0 = o0 + b;
-    const int nrows = stat_rows<GREEDY>(g);
-    const int32_t sbase = GREEDY ? o0 + b : 2 * o0 + b;
+    const int nrows = stat_rows<GREEDY>(P, g);
+    const int32_t sbase = GREEDY || P.pm ? o0 + b : 2 * o0 + b;
     const int nch = P.nchA;
     const float K = P.K_hi;
     // Partial words of a block (8 rows from j0, the 32 chunks from c0), one row per register; rows past
@@ -436,7 +442,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         if (x < 0 || x >= P.V) err |= 1u << SV_ERR_BAD_TOKEN;
         else if (!GREEDY) {
             lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
-            ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
+            if (!P.pm) ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
         }
     }
     if (!GREEDY) {
@@ -568,16 +574,17 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         return;
     }
     // the draft row of slot `lane` is statistics row g + 1 + lane: lane (g+1+lane) & 31, register >> 5
+    // (point-mass drafts have no draft rows: q(x) = 1)
     const int jd = g + 1 + lane;
     const float dm0 = __shfl_sync(0xFFFFFFFFu, my_m0, jd & 31), dm1 = __shfl_sync(0xFFFFFFFFu, my_m1, jd & 31);
     const float ds0 = __shfl_sync(0xFFFFFFFFu, my_s0, jd & 31), ds1 = __shfl_sync(0xFFFFFFFFu, my_s1, jd & 31);
-    const float dm = (jd >> 5) ? dm1 : dm0, ds = (jd >> 5) ? ds1 : ds0;
+    const float dm = P.pm ? 0.f : (jd >> 5) ? dm1 : dm0, ds = P.pm ? 1.f : (jd >> 5) ? ds1 : ds0;
     bool acc = true;
     if (lane < g) {
         // p(x) and q(x) from the precise exponential of the exact logit gaps, over the fp32 normalisers
         const ff2 e = exp2_ff2(make_float2(lt, ld), make_float2(my_m0, dm), exp_const(P), tab);
         const float px = div_fma(e.hi.x + e.lo.x, my_s0);
-        const float qx = div_fma(e.hi.y + e.lo.y, ds);
+        const float qx = P.pm ? 1.f : div_fma(e.hi.y + e.lo.y, ds);
         acc = u_acc * qx < px;
         if (P.dbg.p_x) P.dbg.p_x[o0 + lane] = (double)px;
         if (P.dbg.q_x) P.dbg.q_x[o0 + lane] = (double)qx;
@@ -601,8 +608,13 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     const float pm = __shfl_sync(0xFFFFFFFFu, my_m0, n), ps = __shfl_sync(0xFFFFFFFFu, my_s0, n);
     const float qm = __shfl_sync(0xFFFFFFFFu, dm, n), qs = __shfl_sync(0xFFFFFFFFu, ds, n);
     const float un = __shfl_sync(0xFFFFFFFFu, u_draw, n);
-    put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, pm, n < g ? qm : 0.f,
-             n < g ? div_fma(ps, qs) : 1.f, un);
+    const int32_t xn = __shfl_sync(0xFFFFFFFFu, x, n < g ? n : 0);
+    if (P.pm)  // the residual of a point-mass draft removes column x_n; rho's word carries x_n + 1
+        put_task(P, b, lane, n < g ? kModeResidualPM : kModeBonus, n, pm, 0.f,
+                 n < g ? __int_as_float(xn + 1) : 1.f, un);
+    else
+        put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, pm, n < g ? qm : 0.f,
+                 n < g ? div_fma(ps, qs) : 1.f, un);
     if (lane == 0) P.out_n[b] = n;
 }
 
@@ -680,9 +692,9 @@ __device__ __forceinline__ ff resid_weight(float hp, float lp, float hq, float l
 // a selected column (float-float); 0 at or past k_hi.
 template <int DT>
 __device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& tk, const ExpConst& EC, bool resid,
-                                            ff rho, const float* tab) {
+                                            ff rho, const float* tab, int32_t k, int32_t xcl) {
     const ff2 e = exp2_ff2(make_float2(lp, lq), make_float2(tk.m_p, tk.m_q), EC, tab);
-    if (!resid) return ff_norm(e.hi.x, e.lo.x);
+    if (!resid) return k == xcl ? ff{0.f, 0.f} : ff_norm(e.hi.x, e.lo.x);
     const bool sel = e.hi.x > tk.rho * e.hi.y;  // the selection rule of sel_mask
     return resid_weight(e.hi.x, e.lo.x, e.hi.y, e.lo.y, sel ? 1.f : 0.f, rho);
 }
@@ -694,7 +706,8 @@ __device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& 
 // last column of positive weight when the crossing is lost to rounding (or `tail_rule` asks for it).
 template <int DT, bool VEC>
 __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t prow, size_t qrow, bool resid, ff rho,
-                                 int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, const float* tab, int lane) {
+                                 int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, int32_t xcl, const float* tab,
+                                 int lane) {
     const ExpConst EC = exp_const(P);
     // a unit spans at most kSTask columns: NB passes; bf16 issues every pass's loads first
     constexpr int NB = kSTask / kScanBlock;
@@ -727,8 +740,8 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float2 lpv = col2<DT>(cp, e), lqv = resid ? col2<DT>(cq, e) : f2(0.f);
-            const ff w0 = column_weight<DT>(lpv.x, lqv.x, tk, EC, resid, rho, tab);
-            const ff w1 = column_weight<DT>(lpv.y, lqv.y, tk, EC, resid, rho, tab);
+            const ff w0 = column_weight<DT>(lpv.x, lqv.x, tk, EC, resid, rho, tab, k0 + 2 * e, xcl);
+            const ff w1 = column_weight<DT>(lpv.y, lqv.y, tk, EC, resid, rho, tab, k0 + 2 * e + 1, xcl);
             if (k0 + 2 * e < k_hi && w0.hi > 0.f) {
                 tot = ff_add(tot, w0);
                 lastp = k0 + 2 * e;
@@ -753,7 +766,7 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
             if (lane < kScanPerLane && kj < k_hi) {
                 const float lpj = logit_at<DT>(P.target, prow * (size_t)P.V + kj);
                 const float lqj = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + kj) : 0.f;
-                w = column_weight<DT>(lpj, lqj, tk, EC, resid, rho, tab);
+                w = column_weight<DT>(lpj, lqj, tk, EC, resid, rho, tab, kj, xcl);
                 if (!(w.hi > 0.f)) w = ff{0.f, 0.f};
             }
             const ff c = ff_add(pre, warp_inscan_ff(w, lane));  // lanes >= 16 add zeros
@@ -811,7 +824,7 @@ __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int uni
         if (k < P.V) {
             const float lpk = logit_at<DT>(P.target, prow * (size_t)P.V + k);
             const float lqk = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + k) : 0.f;
-            cw[e] = column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab);
+            cw[e] = column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab, k, tk.xcl);
             if (!(cw[e].hi > 0.f)) cw[e] = ff{0.f, 0.f};
         }
         tot = ff_add(tot, cw[e]);
@@ -924,7 +937,7 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
     ff incl = warp_inscan_ff(W, lane);
     ff S = shfl_ff(incl, 31);
     bool by_p = false;
-    if (resid && !(S.hi > 0.f)) {  // residual mass 0 (only through rounding): draw from p
+    if ((resid || tk.mode == kModeResidualPM) && !(S.hi > 0.f)) {  // residual mass 0: draw from p
         resid = false;
         by_p = true;
         W = lp;
@@ -995,7 +1008,8 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
         if (!by_p) token = group_search<DT, VEC>(P, b, unit, tk, prow, qrow, resid, rho, rem, tail_rule, tab, lane);
         if (by_p || token == -1) {
             const int32_t k_lo = unit * kSTask, k_hi = min(P.V, k_lo + kSTask);
-            token = scan_elements<DT, VEC>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule, tab, lane);
+            token = scan_elements<DT, VEC>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule,
+                                           by_p ? -1 : tk.xcl, tab, lane);
         }
         if (token == -2) token = -1;  // time-out (reported in the status word)
     }
@@ -1059,11 +1073,14 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
     const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
     const int32_t cbase = i * kSTask;
     const ExpConst EC = exp_const(P);
+    // the residual of a point-mass draft removes one column: the task holding it selects all but it
+    const bool excl = tk.xcl >= cbase && tk.xcl < cbase + kSTask;
     // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
     float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
     float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
-    // one step: 8 consecutive columns of the lane (4 pairs) of the p row, and of the q row for a residual
-    auto step = [&](const Cols8& cp, const Cols8& cq) {
+    // one step: 8 consecutive columns k, k + 1, ... of the lane (4 pairs) of the p row, and of the q row
+    // for a residual
+    auto step = [&](const Cols8& cp, const Cols8& cq, int32_t k) {
         if (resid) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -1080,6 +1097,17 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
                 Al = fma2(mk, lp, Al);
                 Bh = fma2(mk, hq, Bh);
                 Bl = fma2(mk, lq, Bl);
+            }
+        } else if (excl) {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
+                const float2 mk = make_float2(k + 2 * h == tk.xcl ? 0.f : 1.f, k + 2 * h + 1 == tk.xcl ? 0.f : 1.f);
+                const float2 hp = grid_hi(ep.hi), lp = add2(sub2(ep.hi, hp), ep.lo);
+                Ph = add2(Ph, hp);
+                Pl = add2(Pl, lp);
+                Ah = fma2(mk, hp, Ah);
+                Al = fma2(mk, lp, Al);
             }
         } else {
 #pragma unroll
@@ -1115,10 +1143,11 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
             rp[D - 1] = load_cols8<DT, VEC>(P.target, prow, P.V, k1);
             if (resid) rq[D - 1] = load_cols8<DT, VEC>(P.draft, qrow, P.V, k1);
         }
-        step(cp, cq);
+        step(cp, cq, cbase + 32 * lane + 8 * e);
     }
     // the group words first (read by the find only, which polls them): sums over kGroupLanes lanes
-    ff ga = resid ? lane_ff(Ah, Al) : lane_ff(Ph, Pl), gb = resid ? lane_ff(Bh, Bl) : ff{0.f, 0.f};
+    const bool sel = resid || excl;  // the selected sums differ from the p sums
+    ff ga = sel ? lane_ff(Ah, Al) : lane_ff(Ph, Pl), gb = resid ? lane_ff(Bh, Bl) : ff{0.f, 0.f};
 #pragma unroll
     for (int o = 1; o < kGroupLanes; o <<= 1) {
         ga = ff_add(ga, ff{__shfl_xor_sync(0xFFFFFFFFu, ga.hi, o), __shfl_xor_sync(0xFFFFFFFFu, ga.lo, o)});
@@ -1135,6 +1164,9 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
         const ff sq = warp_sum_ff(lane_ff(Qh, Ql)), sa = warp_sum_ff(lane_ff(Ah, Al));
         const ff sb = warp_sum_ff(lane_ff(Bh, Bl));
         mine = lane == 1 ? sq : lane == 2 ? sa : lane == 3 ? sb : sp;
+    } else if (excl) {
+        const ff sa = warp_sum_ff(lane_ff(Ah, Al));
+        mine = lane == 2 ? sa : (lane == 1 || lane == 3) ? ff{0.f, 0.f} : sp;
     } else if (lane == 1 || lane == 3) {
         mine = ff{0.f, 0.f};
     }
@@ -1180,7 +1212,7 @@ __device__ __forceinline__ const char* stat_row_src(const Params& P, int32_t r, 
     const size_t esz = DT == SV_BF16 ? 2 : 4;
     size_t row = (size_t)r;
     bool draft = false;
-    if (!GREEDY) {
+    if (!GREEDY && !P.pm) {  // greedy and point-mass batches stream target rows only: row = r
         if (rows) {
             const int32_t v = rows[r];
             draft = v < 0;
@@ -1228,8 +1260,8 @@ __device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, co
     int32_t o0, g;
     if (bases) {  // from the validated offsets cached in shared memory: no dependent global load
         const int32_t s0 = bases[b], s1 = bases[b + 1];
-        o0 = GREEDY ? s0 - b : (s0 - b) >> 1;
-        g = GREEDY ? s1 - s0 - 1 : (s1 - s0 - 1) >> 1;
+        o0 = GREEDY || P.pm ? s0 - b : (s0 - b) >> 1;
+        g = GREEDY || P.pm ? s1 - s0 - 1 : (s1 - s0 - 1) >> 1;
     } else {
         o0 = __ldg(P.offs + b);
         g = __ldg(P.gammas + b);
@@ -1338,15 +1370,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     const bool cache = P.B < kBaseCache;
     if (cache && tid == 0) {  // the end of the last sequence's rows
         const int32_t oB = __ldg(P.offs + P.B);
-        s_base[P.B] = GREEDY ? oB + P.B : 2 * oB + P.B;
+        s_base[P.B] = GREEDY || P.pm ? oB + P.B : 2 * oB + P.B;
     }
     for (int32_t b = tid; b < P.B; b += kThreads) {
         const int32_t o0 = __ldg(P.offs + b), o1 = __ldg(P.offs + b + 1), g = __ldg(P.gammas + b);
         const bool ok = g >= 0 && g <= P.max_gamma && o0 >= 0 && o1 - o0 == g;
         bad |= !ok;
-        const int32_t sb = GREEDY ? o0 + b : 2 * o0 + b;
+        const int32_t sb = GREEDY || P.pm ? o0 + b : 2 * o0 + b;
         if (cache) s_base[b] = sb;
-        if (!GREEDY && ok)  // row map entries that fit (it is used only when every row fits)
+        if (!GREEDY && !P.pm && ok)  // row map entries that fit (it is used only when every row fits)
             for (int32_t j = 0; j <= 2 * g && sb + j < kRowCache; ++j)
                 s_row[sb + j] = j <= g ? o0 + b + j : (int32_t)(0x80000000u | (uint32_t)(o0 + j - g - 1));
     }
@@ -1363,9 +1395,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     }
     const int32_t oB = __ldg(P.offs + P.B);
     // the host bounds rows * nchA and B * nS below 2^31
-    const uint32_t nA = (uint32_t)(GREEDY ? oB + P.B : 2 * oB + P.B) * (uint32_t)P.nchA;
+    const uint32_t nA = (uint32_t)(GREEDY || P.pm ? oB + P.B : 2 * oB + P.B) * (uint32_t)P.nchA;
     const uint32_t nStot = GREEDY ? 0u : (uint32_t)P.B * (uint32_t)P.nS;
-    const int32_t* rows = !GREEDY && 2 * oB + P.B <= kRowCache ? s_row : nullptr;
+    const int32_t* rows = !GREEDY && !P.pm && 2 * oB + P.B <= kRowCache ? s_row : nullptr;
 
     // Statistics. Bulk-copy path: the upper kStreamWarps warps of the CTA stream while the lower ones
     // decide and take sampler tasks at once. Other paths: every warp streams its strided tasks from

@@ -7,6 +7,11 @@ distribution with the Gumbel-max trick (argmax of l/T + Gumbel noise), which sam
 exactly by a different route than the verify step's inverse CDF. Greedy workloads take the draft's
 argmax as its token. All randomness comes from numpy's PCG64 with per-workload seeds.
 
+Point-mass workloads stand in for a drafter without a draft distribution (an n-gram drafter, velog
+"6-1편. Speculative Decoding", §"drafter types": it proposes the tokens that followed an earlier occurrence
+of the last n tokens). Each draft slot gets a planted next token whose target logit is raised by `boost`;
+the drafter proposes it with probability `hit`, else a uniform token. No draft rows exist.
+
 No dataset is used: the pages measure nothing on the verify step itself, and these synthetic batches
 stand in for the decode batches the pages describe (draft model proposes gamma tokens, target scores
 gamma + 1 positions; "Accelerating Sonar through speculation", §"Speculative decoding" steps 2-4).
@@ -36,6 +41,9 @@ class Workload:
     gamma_hi: int = 8
     seed: int = 0
     tags: tuple = field(default_factory=tuple)
+    point_mass: bool = False     # drafts without a draft distribution (q = point mass), no draft rows
+    boost: float = 0.0           # point mass: raise of the planted token's target logit
+    hit: float = 0.0             # point mass: probability that the draft is the planted token
 
     @property
     def greedy(self) -> bool:
@@ -51,6 +59,8 @@ WORKLOADS = {
         Workload("b64_g5_v128256", 64, 128256, BF16, 1.0, 5, 2.5, 1.1, 1.0, (0.3, 1.0, 2.0), seed=3000),
         Workload("b256_g3_v152064_t0.8", 256, 152064, BF16, 0.8, 3, 2.0, 1.05, 1.0, (0.8,), seed=4000),
         Workload("ragged_b128_v129280", 128, 129280, BF16, 1.0, None, 2.0, 1.1, 1.0, (1.0,), seed=5000),
+        Workload("pointmass_b64_g5_v128256", 64, 128256, BF16, 1.0, 5, 2.5, 1.1, 0.0, (0.0,), seed=6000,
+                 point_mass=True, boost=9.0, hit=0.8),
     ]
 }
 
@@ -110,12 +120,12 @@ class Batch:
     def algorithmic_bytes(self) -> int:
         """Bytes the verify step must move at least: every logit it needs read once, plus the
         small index arrays and outputs."""
-        rows = self.R_t if self.workload.greedy else self.R_t + self.R_d
+        rows = self.verified_rows()
         return (rows * self.V * self.elem_bytes + 4 * self.R_d + 4 * (self.B + 1) + 4 * self.B
                 + 4 * self.R_t + 4 * self.B)
 
     def verified_rows(self) -> int:
-        return self.R_t if self.workload.greedy else self.R_t + self.R_d
+        return self.R_t if self.workload.greedy or self.draft is None else self.R_t + self.R_d
 
 
 def _rows(rng, n, V, sigma, zipf_s):
@@ -151,6 +161,13 @@ def make_batch(name_or_w, B: int | None = None, V: int | None = None, gammas=Non
         d0 = int(offs[b])
         t0 = d0 + b
         t64 = _rows(rng, g + 1, V, w.target_sigma, w.zipf_s)
+        if w.point_mass:
+            planted = tok_rng.integers(0, min(V, 1024), size=g)
+            t64[np.arange(g), planted] += w.boost
+            guess = np.where(tok_rng.random(size=g) < w.hit, planted, tok_rng.integers(0, V, size=g))
+            tokens[d0:d0 + g] = guess
+            target[t0:t0 + g + 1] = to_bf16_bits(t64) if w.dtype == BF16 else t64.astype(np.float32)
+            continue
         sig = w.draft_sigmas[b % len(w.draft_sigmas)]
         d64 = w.draft_scale * t64[:g] + rng.normal(0.0, sig, size=(g, V))
         if w.dtype == BF16:
@@ -167,4 +184,4 @@ def make_batch(name_or_w, B: int | None = None, V: int | None = None, gammas=Non
             else:
                 gum = -np.log(-np.log(tok_rng.random(size=(g, V)) + 1e-300) + 1e-300)
                 tokens[d0:d0 + g] = np.argmax(dl / w.temperature + gum, axis=1)
-    return Batch(w, target, draft if R_d else None, tokens, offs, gammas)
+    return Batch(w, target, draft if R_d and not w.point_mass else None, tokens, offs, gammas)

@@ -83,8 +83,9 @@ def compare(b, g, r, seed, step):
         n = nr
         kg = int(g["tokens"][t0 + n])
         u = oracle.uniform(seed, step, s, n, 1)
-        drow = b.draft[d0 + n] if n < gm else None
-        tok, lo, hi, S = oracle.draw_bracket(b.target[t0 + n], drow, b.V, T, u, kg)
+        drow = b.draft[d0 + n] if n < gm and b.draft is not None else None
+        x_excl = int(b.draft_tokens[d0 + n]) if n < gm and b.draft is None else -1  # point-mass draft
+        tok, lo, hi, S = oracle.draw_bracket(b.target[t0 + n], drow, b.V, T, u, kg, x_excl)
         dist = 0.0 if lo <= u < hi else min(abs(u - lo), abs(u - hi))
         (band if dist < BAND else bad).append((s, "draw", n, u, kg, tok, lo, hi))
     return dict(draws=draws, band=band, bad=bad)

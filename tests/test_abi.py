@@ -79,7 +79,8 @@ def test_host_side_checks_without_gpu(libpath):
     assert call(max_gamma=32) == sv.SV_ERR_INVALID_ARG
     assert call(dtype=7) == sv.SV_ERR_INVALID_ARG
     assert call(target_logits=None) == sv.SV_ERR_INVALID_ARG
-    assert call(draft_logits=None) == sv.SV_ERR_INVALID_ARG
+    # draft_logits NULL at T > 0 is valid (point-mass drafts), but never without draft tokens
+    assert call(draft_logits=None, draft_tokens=None) == sv.SV_ERR_INVALID_ARG
     assert call(draft_tokens=None) == sv.SV_ERR_INVALID_ARG
     assert call(target_logits=fake + 1) == sv.SV_ERR_INVALID_ARG
     assert call(workspace=None) == sv.SV_ERR_WORKSPACE

@@ -226,3 +226,24 @@ def test_rows_with_maximum_near_zero(name):
     m = synth.bf16_bits_to_f32(b.target).max(1)
     assert np.all(np.abs(m) < 2.0 ** -19)  # these rows take the carried-rounding path
     parity.assert_parity(b, 31, 2)
+
+
+@pytest.mark.parametrize("name,B,V,f32", [("pointmass_b64_g5_v128256", None, None, False),
+                                          ("pointmass_b64_g5_v128256", 7, 20001, False),
+                                          ("pointmass_b64_g5_v128256", 5, 3000, True)])
+def test_point_mass_drafts(name, B, V, f32):
+    """Drafts without a draft distribution (an n-gram drafter's): no draft rows, q = point mass."""
+    b = synth.make_batch(name, B=B, V=V)
+    if f32:
+        b.target = synth.bf16_bits_to_f32(b.target)
+    assert b.draft is None
+    d = parity.to_device(b)
+    for step in range(3 if B is None else 5):
+        g = parity.run_gpu(b, 1234, step, dev_in=d)
+        parity.assert_parity(b, 1234, step, g=g)
+
+
+def test_point_mass_gamma_zero_and_max():
+    b = synth.make_batch("pointmass_b64_g5_v128256", B=5, V=4000, gammas=[0, 31, 3, 0, 31])
+    for step in range(3):
+        parity.assert_parity(b, 9, step)
