@@ -180,6 +180,27 @@ int spec_verify_fused(const void* target_logits, const void* draft_logits, sv_dt
                       size_t workspace_bytes, int32_t* history, int32_t capacity, int32_t* lengths,
                       int32_t* next_tokens, void* cuda_stream);
 
+/*
+ * N-gram drafter (velog "6-1편. Speculative Decoding", §"drafter types", N-gram: no draft model; the
+ * tokens that followed an earlier occurrence of the most recent n tokens are reused as the guess). For
+ * every sequence b, with L = lengths[b] tokens history[b * capacity + 0 .. L-1]:
+ *   for n = n_max down to n_min (the first n that matches): the largest s with s + n < L and
+ *   history[s .. s+n-1] == history[L-n .. L-1]; the draft is the tokens history[s+n .. s+n+gamma-1],
+ *   gamma = min(gamma_max, L - (s + n)), and match_pos[b] = s + n. No match: gamma 0, match_pos = L.
+ * Outputs, CSR-packed as spec_verify_ex reads them: gammas[b], seq_offsets[0..B] (prefix sums of the
+ * gammas) and draft_tokens[seq_offsets[b] .. seq_offsets[b+1]-1]. Such drafts have no draft
+ * distribution: verify them with draft_logits NULL (point-mass drafts).
+ * Arguments: history int32[B * capacity] and lengths int32[B] as spec_verify_commit maintains them
+ * (1 <= capacity <= 32768); 1 <= n_min <= n_max; 0 <= gamma_max <= SV_MAX_GAMMA; draft_tokens
+ * int32[B * gamma_max]; gammas and match_pos int32[B]; seq_offsets int32[B + 1]. All DEVICE pointers
+ * owned by the caller, 4-byte aligned. A length outside [0, capacity] gives that sequence no draft and
+ * sets (1u << SV_ERR_INVALID_ARG) in *device_status (if not NULL). Two launches on cuda_stream; returns
+ * SV_ERR_INVALID_ARG for bad scalars or pointers, SV_ERR_CUDA if a launch fails, else SV_OK.
+ */
+int spec_draft_ngram(const int32_t* history, int32_t capacity, const int32_t* lengths, int32_t B, int32_t n_min,
+                     int32_t n_max, int32_t gamma_max, int32_t* draft_tokens, int32_t* gammas,
+                     int32_t* seq_offsets, int32_t* match_pos, uint32_t* device_status, void* cuda_stream);
+
 /* Map a device status word (OR of 1u << code) to one status code, by the priority above. */
 int spec_verify_status_from_bits(uint32_t bits);
 

@@ -29,8 +29,8 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
-                          "spec_verify_commit", "spec_verify_fused", "spec_verify_status_from_bits",
-                          "spec_verify_status_string"}
+                          "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram",
+                          "spec_verify_status_from_bits", "spec_verify_status_string"}
 
 
 def test_library_exports_every_declared_symbol(libpath):
@@ -135,3 +135,23 @@ def test_fused_host_side_checks_without_gpu(libpath):
     assert call(next_tokens=fake + 2) == sv.SV_ERR_INVALID_ARG
     assert call(temperature=-1.0) == sv.SV_ERR_INVALID_ARG
     assert call(workspace=None) == sv.SV_ERR_WORKSPACE
+
+
+def test_ngram_host_side_checks_without_gpu(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    fake = 1 << 20  # never dereferenced: every call below returns before any CUDA call
+    args = dict(history=fake, capacity=1024, lengths=fake, B=4, n_min=1, n_max=3, gamma_max=5, draft_tokens=fake,
+                gammas=fake, seq_offsets=fake, match_pos=fake, device_status=None, cuda_stream=None)
+
+    def call(**kw):
+        a = dict(args); a.update(kw)
+        return sv.spec_draft_ngram(**a)
+
+    assert call(B=-1) == sv.SV_ERR_INVALID_ARG
+    assert call(capacity=0) == sv.SV_ERR_INVALID_ARG
+    assert call(capacity=32769) == sv.SV_ERR_INVALID_ARG
+    assert call(n_min=0) == sv.SV_ERR_INVALID_ARG
+    assert call(n_max=0) == sv.SV_ERR_INVALID_ARG
+    assert call(gamma_max=32) == sv.SV_ERR_INVALID_ARG
+    assert call(history=None) == sv.SV_ERR_INVALID_ARG
+    assert call(seq_offsets=fake + 2) == sv.SV_ERR_INVALID_ARG
