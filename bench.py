@@ -339,6 +339,36 @@ def main():
     if call.status_bits():
         raise RuntimeError("device status bits set by the fused steps")
 
+    # n-gram drafter (spec_draft_ngram) on synthetic histories of 2000 tokens with repeats, B sequences
+    ng_cap, ng_len, ng_g = 4096, 2000, max(mg, 1)
+    ng_rng = np.random.default_rng(77)
+    ng_hist = ng_rng.integers(0, 500, size=(b.B, ng_cap)).astype(np.int32)
+    for r in range(b.B):  # plant a repeat of the last 4 tokens 300 tokens earlier
+        ng_hist[r, ng_len - 300:ng_len - 296] = ng_hist[r, ng_len - 4:ng_len]
+    ng_h = torch.from_numpy(ng_hist).to(dev)
+    ng_L = torch.full((b.B,), ng_len, dtype=torch.int32, device=dev)
+    ng_t = torch.zeros(b.B * ng_g, dtype=torch.int32, device=dev)
+    ng_gam = torch.zeros(b.B, dtype=torch.int32, device=dev)
+    ng_off = torch.zeros(b.B + 1, dtype=torch.int32, device=dev)
+    ng_pos = torch.zeros(b.B, dtype=torch.int32, device=dev)
+
+    def ngram_call():
+        if sv.spec_draft_ngram(ng_h.data_ptr(), ng_cap, ng_L.data_ptr(), b.B, 1, 4, ng_g, ng_t.data_ptr(),
+                               ng_gam.data_ptr(), ng_off.data_ptr(), ng_pos.data_ptr(), call.status.data_ptr(),
+                               stream.cuda_stream) != sv.SV_OK:
+            raise RuntimeError("spec_draft_ngram failed")
+
+    ngram_call()
+    n0 = torch.cuda.Event(enable_timing=True)
+    n1 = torch.cuda.Event(enable_timing=True)
+    n_ng = 100
+    n0.record(stream)
+    for _ in range(n_ng):
+        ngram_call()
+    n1.record(stream)
+    stream.synchronize()
+    us_ngram = n0.elapsed_time(n1) / n_ng * 1e3
+
     rows = b.verified_rows()
     value = rows * world / (ms * 1e-3)
     e2e_value = rows * world / (ms_e2e * 1e-3)
@@ -377,6 +407,9 @@ def main():
                                    "fused_ms_per_step": ms_fused, "fused_steps": n_fused,
                                    "fused_extra_us_per_step": (ms_fused - ms) * 1e3,
                                    "fused_launch": f"spec_verify_fused from a CUDA graph of {G} steps"},
+            "ngram_drafter": {"us_per_call": us_ngram, "calls": n_ng, "B": b.B, "history_tokens": ng_len,
+                              "n": "4..1", "gamma_max": ng_g,
+                              "launch": "spec_draft_ngram: search (one CTA per sequence) + pack (one CTA)"},
         }
         if world == 1 and args.cpu_seconds > 0:
             rate, cores, sample = cpu_oracle_rate(b, args.cpu_seconds)
