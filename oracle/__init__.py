@@ -71,6 +71,12 @@ def lib():
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                                               ctypes.c_void_p, ctypes.c_void_p]
             L.oracle_draw_bracket.restype = ctypes.c_int32
+            L.oracle_tree_probs.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int32] * 2 + [ctypes.c_void_p] * 4
+            L.oracle_tree_probs.restype = ctypes.c_int32
+            L.oracle_verify_tree.argtypes = [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 4 + \
+                [ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_uint64, ctypes.c_uint64] + \
+                [ctypes.c_void_p] * 3
+            L.oracle_verify_tree.restype = ctypes.c_uint32
             _lib = L
     return _lib
 
@@ -172,3 +178,39 @@ def draw_bracket(trow, drow, V, temperature, u, k_query, x_excl=-1):
     tok = lib().oracle_draw_bracket(_ptr(trow), _ptr(drow), dtype, V, float(temperature), float(u),
                                     int(x_excl), int(k_query), _ptr(lo), _ptr(hi), _ptr(S))
     return tok, float(lo[0]), float(hi[0]), float(S[0])
+
+
+def tree_probs(p, parents, x, u_acc, u_smp):
+    """The tree rule on fp64 probabilities (see ``oracle_tree_probs``): p [gamma+1, V], parents/x of
+    the gamma non-root nodes, u_acc/u_smp indexed by slot / node. Returns (n, tokens, path)."""
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    g = p.shape[0] - 1
+    V = p.shape[1]
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(max(g, 1))
+    xs = np.ascontiguousarray(x, dtype=np.int32).reshape(max(g, 1))
+    ua = np.ascontiguousarray(u_acc, dtype=np.float64).reshape(max(g, 1))
+    us = np.ascontiguousarray(u_smp, dtype=np.float64).reshape(g + 1)
+    out = np.zeros(g + 1, dtype=np.int32)
+    path = np.zeros(max(g, 1), dtype=np.int32)
+    n = lib().oracle_tree_probs(_ptr(p), _ptr(par), _ptr(xs), g, V, _ptr(ua), _ptr(us), _ptr(out), _ptr(path))
+    return n, out, path[:g]
+
+
+def verify_tree(target, draft_tokens, seq_offsets, gammas, parents, V, temperature, seed, step):
+    """Verify token trees (see ``oracle_verify_tree``). Returns (tokens, num_accepted, path, status)."""
+    target = np.ascontiguousarray(target)
+    dtype = BF16 if target.dtype == np.uint16 else F32
+    if dtype == F32:
+        target = target.astype(np.float32, copy=False)
+    offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+    gam = np.ascontiguousarray(gammas, dtype=np.int32)
+    tok = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    par = np.ascontiguousarray(parents, dtype=np.int32)
+    B = len(gam)
+    R_d = int(offs[-1]) if B else 0
+    out = np.full(R_d + B, -7, dtype=np.int32)
+    n = np.full(B, -7, dtype=np.int32)
+    path = np.full(max(R_d, 1), -7, dtype=np.int32)
+    st = lib().oracle_verify_tree(_ptr(target), dtype, _ptr(tok), _ptr(offs), _ptr(gam), _ptr(par), B, V,
+                                  float(temperature), seed, step, _ptr(out), _ptr(n), _ptr(path))
+    return out, n, path[:R_d], int(st)

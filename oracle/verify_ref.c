@@ -404,3 +404,138 @@ done:
     free(p); free(q); free(w);
     return tok;
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* Token-tree verification (point-mass candidates)                                            */
+/* ------------------------------------------------------------------------------------------ */
+/*
+ * Reading (the pages sketch tree drafts -- EAGLE's top-K candidates, "Accelerating Sonar through
+ * speculation", §"EAGLE" -- but give no rule): the tree's candidates are tokens without a draft
+ * distribution, so each is a point mass, and [velog] §2-1/§2-2 is applied to the children of the
+ * current node in index order, each rejection removing its token from p:
+ *   cur = root; E = {} (removed tokens), P_E = their p mass;
+ *   for each child c of cur: x = token[c]; if x in E: rejected;
+ *     else accept iff u_c * (1 - P_E) < p_cur(x)   (p restricted to the tokens not removed);
+ *     accepted: emit x, cur = c, E = {}; rejected: E += {x}.
+ *   No child accepted (or a leaf): draw from p_cur with E removed (E empty: p itself) and stop.
+ * The first emitted token is then distributed exactly as p_root. Nodes are numbered 0 (root) ..
+ * gamma; node j >= 1 is draft slot j - 1 with parent parents[j - 1] < j. Uniforms: u_c is the accept
+ * uniform of slot c - 1, the final draw uses the draw uniform of slot cur -- for a chain (parents[i]
+ * = i) this is exactly the linear rule with point-mass drafts.
+ */
+static int32_t tree_probs(const double* p, const int32_t* parent, const int32_t* x, int32_t gamma, int32_t V,
+                          const double* u_acc, const double* u_smp, int32_t* out, int32_t* path) {
+    double* w = (double*)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    char* removed = (char*)calloc((size_t)(V > 0 ? V : 1), 1);
+    int32_t cur = 0, n = 0;
+    for (;;) {
+        const double* pc = p + (size_t)cur * V;
+        double PE = 0.0;
+        int32_t next = -1;
+        for (int32_t c = 1; c <= gamma; ++c) {
+            if (parent[c - 1] != cur) continue;
+            const int32_t xc = x[c - 1];
+            if (removed[xc]) continue;
+            if (u_acc[c - 1] * (1.0 - PE) < pc[xc]) { next = c; break; }
+            removed[xc] = 1;
+            PE += pc[xc];
+        }
+        if (next >= 0) {
+            out[n] = x[next - 1];
+            if (path) path[n] = next;
+            ++n;
+            memset(removed, 0, (size_t)V);
+            cur = next;
+            continue;
+        }
+        double S = 0.0;
+        for (int32_t k = 0; k < V; ++k) { w[k] = removed[k] ? 0.0 : pc[k]; S += w[k]; }
+        if (S == 0.0) for (int32_t k = 0; k < V; ++k) { w[k] = pc[k]; S += w[k]; } /* (reading R6) */
+        out[n] = invcdf(w, V, S, u_smp[cur]);
+        break;
+    }
+    for (int32_t j = n + 1; j <= gamma; ++j) out[j] = -1;
+    if (path) for (int32_t j = n; j < gamma; ++j) path[j] = -1;
+    free(w);
+    free(removed);
+    return n;
+}
+
+/* The tree rule on given probabilities (test helper): p [gamma+1, V] (row j: node j), parent/x of the
+ * gamma non-root nodes, uniforms by slot. Returns n; out [gamma+1] tokens, path [gamma] nodes. */
+int32_t oracle_tree_probs(const double* p, const int32_t* parent, const int32_t* x, int32_t gamma, int32_t V,
+                          const double* u_acc, const double* u_smp, int32_t* out, int32_t* path) {
+    return tree_probs(p, parent, x, gamma, V, u_acc, u_smp, out, path);
+}
+
+/*
+ * Verify a batch of token trees: sequence b has gammas[b] + 1 nodes, node j the target row
+ * seq_offsets[b] + b + j, non-root node j the draft slot seq_offsets[b] + j - 1 (token draft_tokens[.],
+ * parent parents[.] in [0, j)). Outputs as oracle_verify (out_tokens: the accepted path's tokens, then
+ * the drawn one) plus out_path [R_d]: the accepted nodes. Greedy (T == 0): the first child whose token
+ * is the argmax of the current row is taken; else that argmax is emitted. A bad parent fails the
+ * sequence with OR_ERR_BAD_OFFSETS; tokens and non-finite / empty rows as oracle_verify.
+ */
+uint32_t oracle_verify_tree(const void* target, int dtype, const int32_t* draft_tokens, const int32_t* seq_offsets,
+                            const int32_t* gammas, const int32_t* parents, int32_t B, int32_t V, double T,
+                            uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                            int32_t* out_path) {
+    if (B < 0 || V <= 0 || !(T >= 0.0) || isinf(T) || !target || !seq_offsets || !gammas || !out_tokens ||
+        !out_num_accepted)
+        return 1u << OR_ERR_INVALID_ARG;
+    if (seq_offsets[0] != 0) return 1u << OR_ERR_BAD_OFFSETS;
+    for (int32_t b = 0; b < B; ++b)
+        if (gammas[b] < 0 || seq_offsets[b + 1] - seq_offsets[b] != gammas[b]) return 1u << OR_ERR_BAD_OFFSETS;
+    uint32_t status = 0;
+    int32_t gmax = 0;
+    for (int32_t b = 0; b < B; ++b) gmax = gammas[b] > gmax ? gammas[b] : gmax;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V * (size_t)(gmax + 1));
+    double* ua = (double*)malloc(sizeof(double) * (size_t)(gmax + 1));
+    double* us = (double*)malloc(sizeof(double) * (size_t)(gmax + 1));
+    int32_t* arg = (int32_t*)malloc(sizeof(int32_t) * (size_t)(gmax + 1));
+    for (int32_t b = 0; b < B; ++b) {
+        const int32_t g = gammas[b], d0 = seq_offsets[b], t0 = d0 + b;
+        int code = 0;
+        for (int32_t i = 0; i < g && !code; ++i) {
+            if (draft_tokens[d0 + i] < 0 || draft_tokens[d0 + i] >= V) code = OR_ERR_BAD_TOKEN;
+            else if (parents[d0 + i] < 0 || parents[d0 + i] > i) code = OR_ERR_BAD_OFFSETS;
+        }
+        for (int32_t j = 0; j <= g && !code; ++j)
+            code = T == 0.0 ? row_argmax(target, dtype, (size_t)(t0 + j), V, &arg[j])
+                            : row_softmax(target, dtype, (size_t)(t0 + j), V, T, p + (size_t)j * V, NULL);
+        if (code) {
+            for (int32_t j = 0; j <= g; ++j) out_tokens[t0 + j] = -1;
+            if (out_path) for (int32_t j = 0; j < g; ++j) out_path[d0 + j] = -1;
+            out_num_accepted[b] = -1;
+            status |= 1u << code;
+            continue;
+        }
+        int32_t n = 0;
+        if (T == 0.0) {
+            int32_t cur = 0;
+            for (;;) {
+                int32_t next = -1;
+                for (int32_t c = 1; c <= g && next < 0; ++c)
+                    if (parents[d0 + c - 1] == cur && draft_tokens[d0 + c - 1] == arg[cur]) next = c;
+                if (next < 0) break;
+                out_tokens[t0 + n] = arg[cur];
+                if (out_path) out_path[d0 + n] = next;
+                ++n;
+                cur = next;
+            }
+            out_tokens[t0 + n] = arg[cur];
+            for (int32_t j = n + 1; j <= g; ++j) out_tokens[t0 + j] = -1;
+            if (out_path) for (int32_t j = n; j < g; ++j) out_path[d0 + j] = -1;
+        } else {
+            for (int32_t j = 0; j <= g; ++j) {
+                ua[j] = oracle_uniform(seed, step, (uint32_t)b, (uint32_t)j, 0);
+                us[j] = oracle_uniform(seed, step, (uint32_t)b, (uint32_t)j, 1);
+            }
+            n = tree_probs(p, parents + d0, draft_tokens + d0, g, V, ua, us, out_tokens + t0,
+                           out_path ? out_path + d0 : NULL);
+        }
+        out_num_accepted[b] = n;
+    }
+    free(p); free(ua); free(us); free(arg);
+    return status;
+}
