@@ -201,6 +201,35 @@ int spec_draft_ngram(const int32_t* history, int32_t capacity, const int32_t* le
                      int32_t n_max, int32_t gamma_max, int32_t* draft_tokens, int32_t* gammas,
                      int32_t* seq_offsets, int32_t* match_pos, uint32_t* device_status, void* cuda_stream);
 
+/*
+ * Token-tree verification with point-mass candidates. The pages sketch tree drafts (EAGLE's top-K
+ * candidates: "Accelerating Sonar through speculation", §"EAGLE") but give no rule; the reading here
+ * applies velog "6-1편. Speculative Decoding" §2-1/§2-2 to the children of the current node, each a point
+ * mass:
+ *   cur = root; at node cur its children are tried in index order; child c with token x is accepted iff
+ *   u_c * (1 - P_E) < p_cur(x), where P_E is the p_cur mass of the distinct tokens rejected before it
+ *   (a repeated token is rejected); the first accepted child's token is emitted and the walk moves to
+ *   it; if no child is accepted (or cur is a leaf), the last token is drawn from p_cur with the rejected
+ *   tokens removed (if that leaves no mass, from p_cur), and the walk stops. The emitted tokens are then
+ *   distributed exactly as sampling from the target. Greedy (T == 0): the first child whose token is the
+ *   argmax of the current row is taken; else that argmax is emitted.
+ * Layout: the CSR of spec_verify_ex with gamma_b = the number of non-root nodes of tree b (<= 31):
+ *   node 0 is the root, node j >= 1 is draft slot seq_offsets[b] + j - 1 with token draft_tokens[.] and
+ *   parent parents[.] in [0, j); target row seq_offsets[b] + b + j holds the logits after the path to
+ *   node j. Uniforms: the accept test of node j uses slot j - 1 (purpose 0), the final draw at node cur
+ *   uses slot cur (purpose 1): a chain (parents of slot i = i) verifies exactly as spec_verify_ex with
+ *   point-mass drafts (draft_logits NULL).
+ * Outputs: out_tokens[seq_offsets[b] + b + j] for j <= n: the accepted path's tokens, then the drawn
+ * one (-1 after); out_num_accepted[b] = n; out_path (nullable, int32[R_d]) [seq_offsets[b] + j] = the
+ * j-th accepted node for j < n, -1 after. A parent outside [0, j) fails its sequence
+ * (SV_ERR_BAD_OFFSETS); other errors as spec_verify_ex. Workspace: spec_verify_workspace_size.
+ */
+int spec_verify_tree(const void* target_logits, sv_dtype dtype, const int32_t* draft_tokens, const int32_t* parents,
+                     const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, int32_t max_gamma,
+                     float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                     int32_t* out_path, uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                     void* cuda_stream);
+
 /* Map a device status word (OR of 1u << code) to one status code, by the priority above. */
 int spec_verify_status_from_bits(uint32_t bits);
 

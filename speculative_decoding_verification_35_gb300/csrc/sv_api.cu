@@ -56,7 +56,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
                 const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, int32_t max_gamma,
                 float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
                 uint32_t* device_status, void* workspace, size_t workspace_bytes, const sv_debug* debug,
-                const CommitBufs* commit, void* cuda_stream) {
+                const CommitBufs* commit, const int32_t* parents, int32_t* out_path, void* cuda_stream) {
     if (B < 0 || V < 1 || max_gamma < 0 || max_gamma > SV_MAX_GAMMA) return SV_ERR_INVALID_ARG;
     if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
     if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
@@ -115,7 +115,10 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.taskw = (Word*)(ws + L.taskw);
     P.recw = (Word*)(ws + L.recw);
     P.groupw = (Word*)(ws + L.groupw);
+    P.remw = (Word*)(ws + L.remw);
     P.ctr = (Counters*)(ws + L.counters);
+    P.parents = parents;
+    P.out_path = out_path;
     if (commit) {
         P.hist = commit->history;
         P.cap = commit->capacity;
@@ -137,7 +140,7 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
                    const sv_debug* debug, void* cuda_stream) {
     return verify_impl(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
                        temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
-                       workspace_bytes, debug, nullptr, cuda_stream);
+                       workspace_bytes, debug, nullptr, nullptr, nullptr, cuda_stream);
 }
 
 int spec_verify_fused(const void* target_logits, const void* draft_logits, sv_dtype dtype,
@@ -156,7 +159,20 @@ int spec_verify_fused(const void* target_logits, const void* draft_logits, sv_dt
     const CommitBufs c{history, capacity, lengths, next_tokens};
     return verify_impl(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
                        temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
-                       workspace_bytes, nullptr, &c, cuda_stream);
+                       workspace_bytes, nullptr, &c, nullptr, nullptr, cuda_stream);
+}
+
+int spec_verify_tree(const void* target_logits, sv_dtype dtype, const int32_t* draft_tokens, const int32_t* parents,
+                     const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, int32_t max_gamma,
+                     float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
+                     int32_t* out_path, uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                     void* cuda_stream) {
+    if (max_gamma > 0 && (!parents || (uintptr_t)parents % 4)) return SV_ERR_INVALID_ARG;
+    if (out_path && (uintptr_t)out_path % 4) return SV_ERR_INVALID_ARG;
+    // max_gamma 0: every tree is a root alone, which the linear path handles identically (a draw from p)
+    return verify_impl(target_logits, nullptr, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                       temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
+                       workspace_bytes, nullptr, nullptr, max_gamma > 0 ? parents : nullptr, out_path, cuda_stream);
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,

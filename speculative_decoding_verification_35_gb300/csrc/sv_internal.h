@@ -26,8 +26,10 @@ constexpr int kBaseCache = 1024;            // batches up to this size keep thei
 constexpr int kRowCache = 2048;             // sampling batches with up to this many statistics rows keep a
                                             // row map (target or draft, row index) in shared memory
 
-// kModeResidualPM: the residual of a point-mass draft (no draft rows): p with the draft column removed
-enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2, kModeResidualPM = 3 };
+// kModeResidualPM: the residual of a point-mass draft (no draft rows): p with the draft column removed.
+// kModeResidualSet: a token-tree node whose candidates were all rejected: p with their tokens removed.
+enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2, kModeResidualPM = 3, kModeResidualSet = 4 };
+constexpr int kMaxRemoved = 32;  // removed-token words per sequence (a node has at most 31 children)
 
 // Data handed between warps of one launch is written as 64-bit words, each exactly once per call with
 // one relaxed store, into a region zeroed before the call, and each non-zero once written. A reader
@@ -44,8 +46,11 @@ typedef Word PartialWord;
 //   w0 = (0x80000000 | mode << 8 | n) << 32 | bits(m_p)   mode kMode*, n the emitting slot
 //   w1 = bits(rho) << 32 | bits(m_q)                      rho = approximate s_p / s_q (> 0);
 //                                                         kModeResidualPM: (x + 1) << 32, x the
-//                                                         draft token (the column the draw removes)
-//   w2 = 0x80000000 << 32 | bits(u)                       u the draw's uniform
+//                                                         draft token (the column the draw removes);
+//                                                         kModeResidualSet: k << 32, k removed tokens
+//                                                         in the sequence's removed-token words
+//   w2 = (0x80000000 | npos) << 32 | bits(u)              u the draw's uniform, npos the output slot
+//                                                         of the drawn token (n, except in a tree)
 // m_p, m_q are the raw-logit maxima of the draw's target and draft rows.
 constexpr int kTaskWords = 4;
 constexpr uint32_t kWordMark = 0x80000000u;
@@ -96,6 +101,9 @@ struct Params {
     Word* taskw;            // [B * kTaskWords]
     Word* recw;             // [B * nS * kRecWords]
     Word* groupw;           // [B * nS * kGroups * kGroupWords]
+    Word* remw;             // [B * kMaxRemoved] removed tokens of a tree draw: 0x80000000 << 32 | token
+    const int32_t* parents; // token trees: parent node of each non-root node (nullptr: linear drafts)
+    int32_t* out_path;      // token trees: the accepted nodes (nullable)
     Counters* ctr;
     // fused post-verify update (spec_verify_fused); hist == nullptr: none
     int32_t* hist;
@@ -106,7 +114,7 @@ struct Params {
 };
 
 struct Layout {
-    size_t counters, partials, taskw, recw, groupw, status;
+    size_t counters, partials, taskw, recw, groupw, remw, status;
     size_t zero_begin, zero_end;  // byte range the launch sequence clears
     size_t total;
 };

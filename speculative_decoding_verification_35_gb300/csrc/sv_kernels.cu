@@ -366,18 +366,20 @@ __device__ __forceinline__ void commit_seq(const Params& P, int32_t b, int32_t n
 // Sampler work of a sequence (see kTaskWords)
 // ------------------------------------------------------------------------------------------------
 struct TaskInfo {
-    int32_t mode, n;
+    int32_t mode, n;  // n: the node (slot) whose target row the draw takes
+    int32_t npos;     // the output slot of the drawn token (n itself, except in a token tree)
     float m_p, m_q, rho, u;
     int32_t xcl;  // kModeResidualPM: the column the draw removes (the draft token); else -1
+    int32_t nrm;  // tokens the draw removes: 1 (kModeResidualPM), k (kModeResidualSet), else 0
 };
 
 // Written by the decision (lanes 0-2 store one word each).
 __device__ __forceinline__ void put_task(const Params& P, int32_t b, int lane, int32_t mode, int32_t n, float m_p,
-                                         float m_q, float rho, float u) {
+                                         float m_q, float rho, float u, int32_t npos) {
     Word w = 0;
     if (lane == 0) w = pack_words(kWordMark | (uint32_t)mode << 8 | (uint32_t)n, __float_as_uint(m_p));
     if (lane == 1) w = pack_words(__float_as_uint(rho), __float_as_uint(m_q));
-    if (lane == 2) w = pack_words(kWordMark, __float_as_uint(u));
+    if (lane == 2) w = pack_words(kWordMark | (uint32_t)npos, __float_as_uint(u));
     if (lane < 3) st_word(P.taskw + (size_t)b * kTaskWords + lane, w);
 }
 
@@ -402,12 +404,127 @@ __device__ __forceinline__ bool get_task(const Params& P, int32_t b, int lane, T
     t.m_q = __uint_as_float((uint32_t)w1);
     t.rho = __uint_as_float((uint32_t)(w1 >> 32));
     t.u = __uint_as_float((uint32_t)w2);
+    t.npos = (int32_t)((w2 >> 32) & 0xFFu);
     t.xcl = -1;
+    t.nrm = 0;
     if (t.mode == kModeResidualPM) {
         t.xcl = (int32_t)(w1 >> 32) - 1;
+        t.nrm = 1;
+        t.rho = 1.f;
+    } else if (t.mode == kModeResidualSet) {
+        t.nrm = (int32_t)(w1 >> 32);
         t.rho = 1.f;
     }
     return true;
+}
+
+// The tokens a draw removes, one per lane (lanes 0 .. tk.nrm - 1, -1 elsewhere): the draft token of a
+// point-mass residual, or a tree draw's removed-token words (polled, bounded). False on time-out.
+__device__ __forceinline__ bool removed_tokens(const Params& P, int32_t b, const TaskInfo& tk, int lane, int32_t& tok) {
+    tok = -1;
+    if (tk.mode == kModeResidualPM) {
+        tok = lane == 0 ? tk.xcl : -1;
+        return true;
+    }
+    if (tk.mode != kModeResidualSet) return true;
+    const Word* w = P.remw + (size_t)b * kMaxRemoved;
+    Word v = lane < tk.nrm ? ld_word(w + lane) : (Word)kWordMark << 32;
+    uint32_t spins = 0, ns = 32;
+    while (__any_sync(0xFFFFFFFFu, v == 0)) {
+        if (++spins > kSpinLimit) {
+            if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(ns);
+        ns = ns < 256 ? 2 * ns : 256;
+        if (v == 0) v = ld_word(w + lane);
+    }
+    if (lane < tk.nrm) tok = (int32_t)(uint32_t)v;
+    return true;
+}
+
+// Bits of the columns [base, base + width) (width <= 32, base per lane) that are among the removed
+// tokens held by lanes 0 .. nrm - 1 (nrm warp-uniform).
+__device__ __forceinline__ uint32_t removed_bits(int32_t tok, int32_t nrm, int32_t base, int width) {
+    uint32_t bits = 0;
+    for (int i = 0; i < nrm; ++i) {
+        const int32_t d = __shfl_sync(0xFFFFFFFFu, tok, i) - base;
+        if (d >= 0 && d < width) bits |= 1u << d;
+    }
+    return bits;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Token trees (spec_verify_tree): the walk from the root, after the decision has the row statistics.
+// Slot i of sequence b is node i + 1, with token x and parent par (per lane); a tree's rows are its nodes
+// (at most 32), so row j's statistics sit on lane j.
+// ------------------------------------------------------------------------------------------------
+// Greedy: at node cur, the first child whose token is cur's argmax (a: the argmax of row `lane`).
+__device__ __noinline__ void tree_greedy(const Params& P, int32_t b, int32_t g, int32_t o0, int32_t x, int32_t par,
+                                         int32_t a, int lane) {
+    const int32_t t0 = o0 + b;
+    const int apar = __shfl_sync(0xFFFFFFFFu, a, par & 31);
+    int cur = 0, n = 0, mytok = -1, mynode = -1;
+    while (true) {
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, lane < g && par == cur && x == apar);
+        if (!hit) break;
+        const int c = __ffs(hit) - 1;
+        const int xc = __shfl_sync(0xFFFFFFFFu, x, c);
+        if (lane == n) { mytok = xc; mynode = c + 1; }
+        ++n;
+        cur = c + 1;
+    }
+    const int ac = __shfl_sync(0xFFFFFFFFu, a, cur);
+    if (lane <= g) P.out_tokens[t0 + lane] = lane < n ? mytok : (lane == n ? ac : -1);
+    if (P.out_path && lane < g) P.out_path[o0 + lane] = lane < n ? mynode : -1;
+    if (lane == 0) P.out_n[b] = n;
+}
+
+// Sampled, point-mass candidates: at node cur, its children (slots whose parent is cur) are tried in
+// slot order, each accepted iff u (1 - P_E) < p_cur(x), P_E the p mass of the distinct tokens rejected
+// before it (a repeated token is rejected outright). The first accepted child is emitted and becomes cur;
+// if none is, the draw takes p_cur without those tokens (their words written before the sampler work).
+// px: p_par(x) of slot `lane`; m_row: the raw maximum of row `lane`.
+__device__ __noinline__ void tree_sampled(const Params& P, int32_t b, int32_t g, int32_t o0, int32_t x, int32_t par,
+                                          float px, float u_acc, float u_draw, float m_row, int lane) {
+    const int32_t t0 = o0 + b;
+    int cur = 0, n = 0, mytok = -1, mynode = -1;
+    uint32_t removed = 0;  // slots holding the tokens the final draw removes
+    while (true) {
+        const bool child = lane < g && par == cur;
+        const uint32_t cm = __ballot_sync(0xFFFFFFFFu, child);
+        if (!cm) break;  // a leaf: the draw takes p_cur
+        const uint32_t same = __match_any_sync(0xFFFFFFFFu, child ? x : -1 - lane);
+        const bool first = child && !(same & cm & ((1u << lane) - 1u));
+        const float pv = first ? px : 0.f;
+        float incl = pv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const bool accept = first && u_acc * (1.f - (incl - pv)) < px;
+        const uint32_t am = __ballot_sync(0xFFFFFFFFu, accept);
+        if (!am) {
+            removed = __ballot_sync(0xFFFFFFFFu, first);
+            break;
+        }
+        const int c = __ffs(am) - 1;
+        const int xc = __shfl_sync(0xFFFFFFFFu, x, c);
+        if (lane == n) { mytok = xc; mynode = c + 1; }
+        ++n;
+        cur = c + 1;
+    }
+    if (lane <= g && lane != n) P.out_tokens[t0 + lane] = lane < n ? mytok : -1;
+    if (P.out_path && lane < g) P.out_path[o0 + lane] = lane < n ? mynode : -1;
+    const int nrm = __popc(removed);
+    if ((removed >> lane) & 1u)
+        st_word(P.remw + (size_t)b * kMaxRemoved + __popc(removed & ((1u << lane) - 1u)),
+                pack_words(kWordMark, (uint32_t)x));
+    const float pm = __shfl_sync(0xFFFFFFFFu, m_row, cur);
+    const float un = __shfl_sync(0xFFFFFFFFu, u_draw, cur);
+    put_task(P, b, lane, nrm ? kModeResidualSet : kModeBonus, cur, pm, 0.f, nrm ? __int_as_float(nrm) : 1.f, un, n);
+    if (lane == 0) P.out_n[b] = n;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -437,11 +554,20 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     int32_t x = 0;
     uint32_t err = 0;
     float lt = 0.f, ld = 0.f, u_acc = 0.f, u_draw = 0.f;
+    // the node whose target row tests slot `lane`: its parent in a token tree, the slot itself otherwise
+    int32_t par = lane;
     if (lane < g) {
         x = __ldg(P.tokens + o0 + lane);
+        if (P.parents) {
+            par = __ldg(P.parents + o0 + lane);
+            if (par < 0 || par > lane) {
+                err |= 1u << SV_ERR_BAD_OFFSETS;
+                par = lane;
+            }
+        }
         if (x < 0 || x >= P.V) err |= 1u << SV_ERR_BAD_TOKEN;
         else if (!GREEDY) {
-            lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
+            lt = logit_at<DT>(P.target, (size_t)(t0 + par) * P.V + x);
             if (!P.pm) ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
         }
     }
@@ -558,14 +684,19 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
             atomicOr(P.status, err);
             P.out_n[b] = -1;
         }
-        if (!GREEDY) put_task(P, b, lane, kModeNone, 0, 0.f, 0.f, 1.f, 0.f);
+        if (!GREEDY) put_task(P, b, lane, kModeNone, 0, 0.f, 0.f, 1.f, 0.f, 0);
         for (int32_t j = lane; j <= g; j += 32) P.out_tokens[t0 + j] = -1;
+        if (P.out_path && lane < g) P.out_path[o0 + lane] = -1;
         commit_seq(P, b, -1, o0, -1, lane);
         return;
     }
     if (GREEDY) {
         const int a = my_a0;  // argmax of target row `lane` (lane <= g <= 31)
         if (lane <= g && P.dbg.row_argmax) P.dbg.row_argmax[t0 + lane] = a;
+        if (P.parents) {  // token tree (out of line: the linear path's code stays small)
+            tree_greedy(P, b, g, o0, x, par, a, lane);
+            return;
+        }
         const uint32_t mism = __ballot_sync(0xFFFFFFFFu, lane < g && x != a);
         const int n = mism ? __ffs(mism) - 1 : g;
         if (lane <= g) P.out_tokens[t0 + lane] = lane < n ? x : (lane == n ? a : -1);
@@ -580,10 +711,14 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     const float ds0 = __shfl_sync(0xFFFFFFFFu, my_s0, jd & 31), ds1 = __shfl_sync(0xFFFFFFFFu, my_s1, jd & 31);
     const float dm = P.pm ? 0.f : (jd >> 5) ? dm1 : dm0, ds = P.pm ? 1.f : (jd >> 5) ? ds1 : ds0;
     bool acc = true;
+    float px = 0.f;
+    // the statistics of the row that tests slot `lane` (rows 0..31 sit on lanes 0..31 here: a tree's
+    // rows are its nodes, at most 32)
+    const float mpar = __shfl_sync(0xFFFFFFFFu, my_m0, par & 31), spar = __shfl_sync(0xFFFFFFFFu, my_s0, par & 31);
     if (lane < g) {
         // p(x) and q(x) from the precise exponential of the exact logit gaps, over the fp32 normalisers
-        const ff2 e = exp2_ff2(make_float2(lt, ld), make_float2(my_m0, dm), exp_const(P), tab);
-        const float px = div_fma(e.hi.x + e.lo.x, my_s0);
+        const ff2 e = exp2_ff2(make_float2(lt, ld), make_float2(mpar, dm), exp_const(P), tab);
+        px = div_fma(e.hi.x + e.lo.x, spar);
         const float qx = P.pm ? 1.f : div_fma(e.hi.y + e.lo.y, ds);
         acc = u_acc * qx < px;
         if (P.dbg.p_x) P.dbg.p_x[o0 + lane] = (double)px;
@@ -601,6 +736,10 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
             }
         }
     }
+    if (P.parents) {  // token tree (out of line: the linear path's code stays small)
+        tree_sampled(P, b, g, o0, x, par, px, u_acc, u_draw, my_m0, lane);
+        return;
+    }
     const uint32_t rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
     const int n = rej ? __ffs(rej) - 1 : g;
     if (lane <= g && lane != n) P.out_tokens[t0 + lane] = lane < n ? x : -1;
@@ -611,10 +750,10 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     const int32_t xn = __shfl_sync(0xFFFFFFFFu, x, n < g ? n : 0);
     if (P.pm)  // the residual of a point-mass draft removes column x_n; rho's word carries x_n + 1
         put_task(P, b, lane, n < g ? kModeResidualPM : kModeBonus, n, pm, 0.f,
-                 n < g ? __int_as_float(xn + 1) : 1.f, un);
+                 n < g ? __int_as_float(xn + 1) : 1.f, un, n);
     else
         put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, pm, n < g ? qm : 0.f,
-                 n < g ? div_fma(ps, qs) : 1.f, un);
+                 n < g ? div_fma(ps, qs) : 1.f, un, n);
     if (lane == 0) P.out_n[b] = n;
 }
 
@@ -692,9 +831,9 @@ __device__ __forceinline__ ff resid_weight(float hp, float lp, float hq, float l
 // a selected column (float-float); 0 at or past k_hi.
 template <int DT>
 __device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& tk, const ExpConst& EC, bool resid,
-                                            ff rho, const float* tab, int32_t k, int32_t xcl) {
+                                            ff rho, const float* tab, bool removed) {
     const ff2 e = exp2_ff2(make_float2(lp, lq), make_float2(tk.m_p, tk.m_q), EC, tab);
-    if (!resid) return k == xcl ? ff{0.f, 0.f} : ff_norm(e.hi.x, e.lo.x);
+    if (!resid) return removed ? ff{0.f, 0.f} : ff_norm(e.hi.x, e.lo.x);
     const bool sel = e.hi.x > tk.rho * e.hi.y;  // the selection rule of sel_mask
     return resid_weight(e.hi.x, e.lo.x, e.hi.y, e.lo.y, sel ? 1.f : 0.f, rho);
 }
@@ -706,8 +845,8 @@ __device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& 
 // last column of positive weight when the crossing is lost to rounding (or `tail_rule` asks for it).
 template <int DT, bool VEC>
 __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t prow, size_t qrow, bool resid, ff rho,
-                                 int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, int32_t xcl, const float* tab,
-                                 int lane) {
+                                 int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, int32_t rtok, int32_t nrm,
+                                 const float* tab, int lane) {
     const ExpConst EC = exp_const(P);
     // a unit spans at most kSTask columns: NB passes; bf16 issues every pass's loads first
     constexpr int NB = kSTask / kScanBlock;
@@ -737,11 +876,12 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
         }
         ff tot{0.f, 0.f};
         int lastp = -1;
+        const uint32_t rb = removed_bits(rtok, nrm, k0, kScanPerLane);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const float2 lpv = col2<DT>(cp, e), lqv = resid ? col2<DT>(cq, e) : f2(0.f);
-            const ff w0 = column_weight<DT>(lpv.x, lqv.x, tk, EC, resid, rho, tab, k0 + 2 * e, xcl);
-            const ff w1 = column_weight<DT>(lpv.y, lqv.y, tk, EC, resid, rho, tab, k0 + 2 * e + 1, xcl);
+            const ff w0 = column_weight<DT>(lpv.x, lqv.x, tk, EC, resid, rho, tab, (rb >> (2 * e)) & 1u);
+            const ff w1 = column_weight<DT>(lpv.y, lqv.y, tk, EC, resid, rho, tab, (rb >> (2 * e + 1)) & 1u);
             if (k0 + 2 * e < k_hi && w0.hi > 0.f) {
                 tot = ff_add(tot, w0);
                 lastp = k0 + 2 * e;
@@ -762,11 +902,12 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
             const ff pre = shfl_ff(exclusive_of(incl, lane), L);
             // lanes j < 16 take column kL + j of lane L
             const int32_t kL = base + L * kScanPerLane, kj = kL + (lane & 15);
+            const uint32_t rj = removed_bits(rtok, nrm, kj, 1);
             ff w{0.f, 0.f};
             if (lane < kScanPerLane && kj < k_hi) {
                 const float lpj = logit_at<DT>(P.target, prow * (size_t)P.V + kj);
                 const float lqj = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + kj) : 0.f;
-                w = column_weight<DT>(lpj, lqj, tk, EC, resid, rho, tab, kj, xcl);
+                w = column_weight<DT>(lpj, lqj, tk, EC, resid, rho, tab, rj != 0u);
                 if (!(w.hi > 0.f)) w = ff{0.f, 0.f};
             }
             const ff c = ff_add(pre, warp_inscan_ff(w, lane));  // lanes >= 16 add zeros
@@ -788,7 +929,7 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
 // column, of positive weight. Returns -1 when nothing in the task has positive weight, -2 on a time-out.
 template <int DT, bool VEC>
 __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int unit, const TaskInfo& tk, size_t prow, size_t qrow,
-                                bool resid, ff rho, ff rem, bool tail_rule, const float* tab, int lane) {
+                                bool resid, ff rho, ff rem, bool tail_rule, int32_t rtok, const float* tab, int lane) {
     static_assert(kGroupCols == 4 * 32, "four columns per lane");
     const Word* gw = P.groupw + (((size_t)b * P.nS + unit) * kGroups + (lane % kGroups)) * kGroupWords;
     Word wa = lane < kGroups ? ld_word(gw) : (Word)kWordMark, wb = lane < kGroups ? ld_word(gw + 1) : (Word)kWordMark;
@@ -815,6 +956,7 @@ __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int uni
     // lane j: columns k0 + 4 j .. k0 + 4 j + 3 of the group
     const ExpConst EC = exp_const(P);
     const int32_t k0 = unit * kSTask + kGroupCols * G + 4 * lane;
+    const uint32_t r4 = removed_bits(rtok, tk.nrm, k0, 4);
     ff cw[4];
     ff tot{0.f, 0.f};
 #pragma unroll
@@ -824,7 +966,7 @@ __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int uni
         if (k < P.V) {
             const float lpk = logit_at<DT>(P.target, prow * (size_t)P.V + k);
             const float lqk = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + k) : 0.f;
-            cw[e] = column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab, k, tk.xcl);
+            cw[e] = column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab, (r4 >> e) & 1u);
             if (!(cw[e].hi > 0.f)) cw[e] = ff{0.f, 0.f};
         }
         tot = ff_add(tot, cw[e]);
@@ -937,7 +1079,7 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
     ff incl = warp_inscan_ff(W, lane);
     ff S = shfl_ff(incl, 31);
     bool by_p = false;
-    if ((resid || tk.mode == kModeResidualPM) && !(S.hi > 0.f)) {  // residual mass 0: draw from p
+    if ((resid || tk.mode == kModeResidualPM || tk.mode == kModeResidualSet) && !(S.hi > 0.f)) {  // mass 0: p
         resid = false;
         by_p = true;
         W = lp;
@@ -1005,11 +1147,14 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
     if (unit >= 0) {
         const ff rem = ff_sub(target, before);
         // the groups' sums cover the residual and bonus weights; the p fallback scans the task's columns
-        if (!by_p) token = group_search<DT, VEC>(P, b, unit, tk, prow, qrow, resid, rho, rem, tail_rule, tab, lane);
+        int32_t rtok = -1;
+        if (!by_p && !removed_tokens(P, b, tk, lane, rtok)) token = -2;
+        if (!by_p && token != -2)
+            token = group_search<DT, VEC>(P, b, unit, tk, prow, qrow, resid, rho, rem, tail_rule, rtok, tab, lane);
         if (by_p || token == -1) {
             const int32_t k_lo = unit * kSTask, k_hi = min(P.V, k_lo + kSTask);
-            token = scan_elements<DT, VEC>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule,
-                                           by_p ? -1 : tk.xcl, tab, lane);
+            token = scan_elements<DT, VEC>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule, rtok,
+                                           by_p ? 0 : tk.nrm, tab, lane);
         }
         if (token == -2) token = -1;  // time-out (reported in the status word)
     }
@@ -1017,7 +1162,7 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
         P.out_tokens[out_pos] = token;
         if (P.dbg.seq_mass) P.dbg.seq_mass[b] = ((double)S.hi + (double)S.lo) / ((double)sp.hi + (double)sp.lo);
     }
-    commit_seq(P, b, token >= 0 ? tk.n : -1, out_pos - b - tk.n, token, lane);
+    commit_seq(P, b, token >= 0 ? tk.npos : -1, out_pos - b - tk.npos, token, lane);
 }
 
 // 8 consecutive columns k0 .. k0 + 7 of `row`, packed (bf16: 4 words; fp32: 8 words); -inf past V.
@@ -1073,8 +1218,15 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
     const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
     const int32_t cbase = i * kSTask;
     const ExpConst EC = exp_const(P);
-    // the residual of a point-mass draft removes one column: the task holding it selects all but it
-    const bool excl = tk.xcl >= cbase && tk.xcl < cbase + kSTask;
+    // point-mass and tree residuals remove some columns: a task holding one selects all but them
+    // (bit j of lane_rm: the lane's column cbase + 32 lane + j is removed)
+    uint32_t lane_rm = 0;
+    if (tk.nrm) {  // warp-uniform
+        int32_t rtok = -1;
+        if (!removed_tokens(P, b, tk, lane, rtok)) return;
+        lane_rm = removed_bits(rtok, tk.nrm, cbase + 32 * lane, 32);
+    }
+    const bool excl = tk.nrm && __any_sync(0xFFFFFFFFu, lane_rm != 0u);
     // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
     float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
     float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
@@ -1102,7 +1254,8 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
-                const float2 mk = make_float2(k + 2 * h == tk.xcl ? 0.f : 1.f, k + 2 * h + 1 == tk.xcl ? 0.f : 1.f);
+                const int bit = k - (cbase + 32 * lane) + 2 * h;
+                const float2 mk = make_float2((lane_rm >> bit) & 1u ? 0.f : 1.f, (lane_rm >> (bit + 1)) & 1u ? 0.f : 1.f);
                 const float2 hp = grid_hi(ep.hi), lp = add2(sub2(ep.hi, hp), ep.lo);
                 Ph = add2(Ph, hp);
                 Pl = add2(Pl, lp);
@@ -1190,7 +1343,7 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
         s_accumulate<DT, VEC, true>(P, b, i, tk, prow, qrow, tab, lane);
     else
         s_accumulate<DT, VEC, false>(P, b, i, tk, prow, qrow, tab, lane);
-    if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0 + b + tk.n, tab, lane);
+    if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0 + b + tk.npos, tab, lane);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1497,7 +1650,8 @@ Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma) {
     L.taskw = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchA * sizeof(PartialWord));
     L.recw = up(L.taskw + (size_t)B * kTaskWords * sizeof(Word));
     L.groupw = up(L.recw + (size_t)B * nS * kRecWords * sizeof(Word));
-    L.status = up(L.groupw + (size_t)B * nS * kGroups * kGroupWords * sizeof(Word));
+    L.remw = up(L.groupw + (size_t)B * nS * kGroups * kGroupWords * sizeof(Word));
+    L.status = up(L.remw + (size_t)B * kMaxRemoved * sizeof(Word));
     L.zero_begin = 0;
     L.zero_end = L.status;
     L.total = up(L.status + sizeof(uint32_t));

@@ -19,8 +19,8 @@ SV_MAX_GAMMA = 31
 
 # every exported symbol of the C ABI, in header order
 EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
-           "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_status_from_bits",
-           "spec_verify_status_string")
+           "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
+           "spec_verify_status_from_bits", "spec_verify_status_string")
 
 
 class SvDebug(ctypes.Structure):
@@ -50,6 +50,9 @@ def _load():
     L.spec_verify_fused.restype = ctypes.c_int
     L.spec_draft_ngram.argtypes = [vp, i32, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     L.spec_draft_ngram.restype = ctypes.c_int
+    L.spec_verify_tree.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp, vp, vp,
+                                   sz, vp]
+    L.spec_verify_tree.restype = ctypes.c_int
     L.spec_verify_status_from_bits.argtypes = [ctypes.c_uint32]
     L.spec_verify_status_from_bits.restype = ctypes.c_int
     L.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -114,6 +117,15 @@ def spec_draft_ngram(history, capacity, lengths, B, n_min, n_max, gamma_max, dra
     """N-gram drafts from the device-side histories. Pointer arguments are device addresses."""
     return lib.spec_draft_ngram(history, capacity, lengths, B, n_min, n_max, gamma_max, draft_tokens, gammas,
                                 seq_offsets, match_pos, device_status, cuda_stream)
+
+
+def spec_verify_tree(target_logits, dtype, draft_tokens, parents, seq_offsets, gammas, B, V, max_gamma, temperature,
+                     seed, step, out_tokens, out_num_accepted, out_path, device_status, workspace, workspace_bytes,
+                     cuda_stream) -> int:
+    """Token-tree verification with point-mass candidates. Pointer arguments are device addresses."""
+    return lib.spec_verify_tree(target_logits, dtype, draft_tokens, parents, seq_offsets, gammas, B, V, max_gamma,
+                                float(temperature), seed, step, out_tokens, out_num_accepted, out_path, device_status,
+                                workspace, workspace_bytes, cuda_stream)
 
 
 def spec_verify_status_from_bits(bits: int) -> int:

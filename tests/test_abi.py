@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
-                          "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram",
+                          "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
                           "spec_verify_status_from_bits", "spec_verify_status_string"}
 
 
@@ -155,3 +155,21 @@ def test_ngram_host_side_checks_without_gpu(libpath):
     assert call(gamma_max=32) == sv.SV_ERR_INVALID_ARG
     assert call(history=None) == sv.SV_ERR_INVALID_ARG
     assert call(seq_offsets=fake + 2) == sv.SV_ERR_INVALID_ARG
+
+
+def test_tree_host_side_checks_without_gpu(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    fake = 1 << 20  # never dereferenced: every call below fails its host checks first
+    args = dict(target_logits=fake, dtype=sv.SV_BF16, draft_tokens=fake, parents=fake, seq_offsets=fake, gammas=fake,
+                B=4, V=100, max_gamma=4, temperature=1.0, seed=1, step=0, out_tokens=fake, out_num_accepted=fake,
+                out_path=None, device_status=None, workspace=fake, workspace_bytes=1 << 30, cuda_stream=None)
+
+    def call(**kw):
+        a = dict(args); a.update(kw)
+        return sv.spec_verify_tree(**a)
+
+    assert call(parents=None) == sv.SV_ERR_INVALID_ARG
+    assert call(parents=fake + 2) == sv.SV_ERR_INVALID_ARG
+    assert call(out_path=fake + 1) == sv.SV_ERR_INVALID_ARG
+    assert call(max_gamma=32) == sv.SV_ERR_INVALID_ARG
+    assert call(workspace=None) == sv.SV_ERR_WORKSPACE
