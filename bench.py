@@ -369,6 +369,39 @@ def main():
     stream.synchronize()
     us_ngram = n0.elapsed_time(n1) / n_ng * 1e3
 
+    # token-tree verification (spec_verify_tree): 64 trees of up to 15 candidate nodes, V of the workload
+    tb = synth.make_tree_batch(64, b.V, 15, seed=1)
+    tmg = int(tb.gammas.max())
+    t_tg = torch.from_numpy(tb.target.view(np.int16)).view(torch.bfloat16).to(dev)
+    t_d = {k: torch.from_numpy(v).to(dev) for k, v in dict(t=tb.draft_tokens, p=tb.parents, o=tb.seq_offsets,
+                                                         g=tb.gammas).items()}
+    t_ws_bytes = sv.spec_verify_workspace_size(tb.B, tb.V, tmg)
+    t_ws = torch.empty(t_ws_bytes, dtype=torch.uint8, device=dev)
+    t_out = torch.empty(tb.R_t, dtype=torch.int32, device=dev)
+    t_n = torch.empty(tb.B, dtype=torch.int32, device=dev)
+    t_path = torch.empty(max(int(tb.seq_offsets[-1]), 1), dtype=torch.int32, device=dev)
+
+    def tree_call(i):
+        if sv.spec_verify_tree(t_tg.data_ptr(), sv.SV_BF16, t_d["t"].data_ptr(), t_d["p"].data_ptr(),
+                               t_d["o"].data_ptr(), t_d["g"].data_ptr(), tb.B, tb.V, tmg, 1.0, seed, i,
+                               t_out.data_ptr(), t_n.data_ptr(), t_path.data_ptr(), call.status.data_ptr(),
+                               t_ws.data_ptr(), t_ws_bytes, stream.cuda_stream) != sv.SV_OK:
+            raise RuntimeError("spec_verify_tree failed")
+
+    for i in range(3):
+        tree_call(i)
+    n_tree = 50
+    v0 = torch.cuda.Event(enable_timing=True)
+    v1 = torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for i in range(n_tree):
+        tree_call(i)
+    v1.record(stream)
+    stream.synchronize()
+    ms_tree = v0.elapsed_time(v1) / n_tree
+    if call.status_bits():
+        raise RuntimeError("device status bits set by the tree steps")
+
     rows = b.verified_rows()
     value = rows * world / (ms * 1e-3)
     e2e_value = rows * world / (ms_e2e * 1e-3)
@@ -407,6 +440,9 @@ def main():
                                    "fused_ms_per_step": ms_fused, "fused_steps": n_fused,
                                    "fused_extra_us_per_step": (ms_fused - ms) * 1e3,
                                    "fused_launch": f"spec_verify_fused from a CUDA graph of {G} steps"},
+            "tree_verify": {"ms_per_call": ms_tree, "calls": n_tree, "B": tb.B, "nodes": tb.R_t, "V": tb.V,
+                            "rows_per_s": tb.R_t / (ms_tree * 1e-3),
+                            "launch": "spec_verify_tree, stream-ordered, inputs resident (L2 may hold part)"},
             "ngram_drafter": {"us_per_call": us_ngram, "calls": n_ng, "B": b.B, "history_tokens": ng_len,
                               "n": "4..1", "gamma_max": ng_g,
                               "launch": "spec_draft_ngram: search (one CTA per sequence) + pack (one CTA)"},

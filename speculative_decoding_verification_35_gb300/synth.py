@@ -185,3 +185,53 @@ def make_batch(name_or_w, B: int | None = None, V: int | None = None, gammas=Non
                 gum = -np.log(-np.log(tok_rng.random(size=(g, V)) + 1e-300) + 1e-300)
                 tokens[d0:d0 + g] = np.argmax(dl / w.temperature + gum, axis=1)
     return Batch(w, target, draft if R_d and not w.point_mass else None, tokens, offs, gammas)
+
+
+@dataclass
+class TreeBatch:
+    """Token trees for spec_verify_tree: gamma_b non-root nodes per tree (CSR like Batch), node j >= 1 is
+    draft slot seq_offsets[b] + j - 1 with token draft_tokens[.] and parent parents[.] in [0, j); target row
+    seq_offsets[b] + b + j holds the logits after the path to node j."""
+    target: np.ndarray
+    draft_tokens: np.ndarray
+    parents: np.ndarray
+    seq_offsets: np.ndarray
+    gammas: np.ndarray
+    temperature: float
+
+    @property
+    def B(self):
+        return len(self.gammas)
+
+    @property
+    def V(self):
+        return int(self.target.shape[1])
+
+    @property
+    def R_t(self):
+        return int(self.seq_offsets[-1]) + self.B
+
+
+def make_tree_batch(B: int, V: int, gamma_max: int, seed: int, temperature: float = 1.0, f32: bool = False,
+                    chain: bool = False) -> TreeBatch:
+    """Random token trees (EAGLE-style top-K candidates stand-in): node j's parent uniform in [0, j) (or
+    j - 1 for a chain); a candidate is a planted token of its parent's row (raised by 6 nats) with
+    probability 0.6, else one of 6 common tokens (so siblings repeat tokens); logits N(0, 2^2) plus a
+    Zipf(1.1) prior, rounded once to bf16 (or kept fp32)."""
+    rng = np.random.Generator(np.random.PCG64(9000 + seed))
+    gam = rng.integers(0, gamma_max + 1, size=B).astype(np.int32)
+    offs = np.concatenate([[0], np.cumsum(gam)]).astype(np.int32)
+    R_d, R_t = int(offs[-1]), int(offs[-1]) + B
+    logits = rng.normal(0, 2.0, size=(R_t, V)) - 1.1 * np.log(np.arange(1, V + 1))
+    parents = np.zeros(R_d, np.int32)
+    tokens = np.zeros(R_d, np.int32)
+    for b in range(B):
+        d0, t0 = int(offs[b]), int(offs[b]) + b
+        planted = rng.integers(0, min(V, 64), size=gam[b] + 1)
+        logits[t0 + np.arange(gam[b] + 1), planted] += 6.0
+        for j in range(1, gam[b] + 1):
+            par = j - 1 if chain else int(rng.integers(0, j))
+            parents[d0 + j - 1] = par
+            tokens[d0 + j - 1] = planted[par] if rng.random() < 0.6 else int(rng.integers(0, 6))
+    target = logits.astype(np.float32) if f32 else to_bf16_bits(logits)
+    return TreeBatch(target, tokens, parents, offs, gam, temperature)

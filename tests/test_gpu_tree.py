@@ -22,26 +22,8 @@ def built():
 
 
 def _trees(B, V, gmax, seed, f32=False, chain=False):
-    """Random token trees: node j's parent uniform in [0, j); candidates are a planted token of the
-    parent's row (raised by 6 nats) with probability 0.6, else a token from a small set (so siblings
-    repeat tokens); logits N(0, 2^2) + Zipf(1.1) prior, rounded to bf16 (or kept fp32)."""
-    rng = np.random.default_rng(seed)
-    gam = rng.integers(0, gmax + 1, size=B).astype(np.int32)
-    offs = np.concatenate([[0], np.cumsum(gam)]).astype(np.int32)
-    R_d, R_t = int(offs[-1]), int(offs[-1]) + B
-    logits = rng.normal(0, 2.0, size=(R_t, V)) - 1.1 * np.log(np.arange(1, V + 1))
-    parents = np.zeros(R_d, np.int32)
-    tokens = np.zeros(R_d, np.int32)
-    for b in range(B):
-        d0, t0 = int(offs[b]), int(offs[b]) + b
-        planted = rng.integers(0, min(V, 64), size=gam[b] + 1)
-        logits[t0 + np.arange(gam[b] + 1), planted] += 6.0
-        for j in range(1, gam[b] + 1):
-            p = j - 1 if chain else int(rng.integers(0, j))
-            parents[d0 + j - 1] = p
-            tokens[d0 + j - 1] = planted[p] if rng.random() < 0.6 else int(rng.integers(0, 6))
-    target = logits.astype(np.float32) if f32 else synth.to_bf16_bits(logits)
-    return target, tokens, parents, offs, gam
+    t = synth.make_tree_batch(B, V, gmax, seed, f32=f32, chain=chain)
+    return t.target, t.draft_tokens, t.parents, t.seq_offsets, t.gammas
 
 
 def _gpu_tree(target, tokens, parents, offs, gam, V, T, seed, step):
