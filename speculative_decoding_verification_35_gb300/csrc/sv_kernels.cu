@@ -1211,29 +1211,24 @@ __device__ __forceinline__ float2 pair8(const Cols8& c, int e) {
 // bf16 task's loads are all issued before the first step), accumulating the p and q weights and their
 // selected parts. It stores the selected sums of each group of kGroupLanes lanes, then the warp's sums
 // as the task's record. TWOSUM: carry the rounding of l - m (see exp2_ff2).
-template <int DT, bool VEC, bool TWOSUM>
+template <int DT, bool VEC, bool TWOSUM, bool REMOVED>
 __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, const TaskInfo& tk, size_t prow,
-                                             size_t qrow, const float* tab, int lane) {
+                                             size_t qrow, const float* tab, int lane, uint32_t lane_rm) {
     const bool resid = tk.mode == kModeResidual;
     const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
     const int32_t cbase = i * kSTask;
     const ExpConst EC = exp_const(P);
-    // point-mass and tree residuals remove some columns: a task holding one selects all but them
-    // (bit j of lane_rm: the lane's column cbase + 32 lane + j is removed)
-    uint32_t lane_rm = 0;
-    if (tk.nrm) {  // warp-uniform
-        int32_t rtok = -1;
-        if (!removed_tokens(P, b, tk, lane, rtok)) return;
-        lane_rm = removed_bits(rtok, tk.nrm, cbase + 32 * lane, 32);
-    }
-    const bool excl = tk.nrm && __any_sync(0xFFFFFFFFu, lane_rm != 0u);
+    // REMOVED: a point-mass or tree residual whose removed columns include some of this task's (bit j of
+    // lane_rm: the lane's column cbase + 32 lane + j); its selected sums leave them out. A separate
+    // instantiation, so the ordinary tasks' code carries no trace of it.
+    constexpr bool excl = REMOVED;
     // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
     float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
     float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
     // one step: 8 consecutive columns k, k + 1, ... of the lane (4 pairs) of the p row, and of the q row
     // for a residual
     auto step = [&](const Cols8& cp, const Cols8& cq, int32_t k) {
-        if (resid) {
+        if (!REMOVED && resid) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
@@ -1250,7 +1245,7 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
                 Bh = fma2(mk, hq, Bh);
                 Bl = fma2(mk, lq, Bl);
             }
-        } else if (excl) {
+        } else if (REMOVED) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
@@ -1339,10 +1334,21 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
     if (!get_task(P, b, lane, tk) || tk.mode == kModeNone) return;
     const size_t prow = (size_t)(o0 + b + tk.n), qrow = (size_t)(o0 + tk.n);
     // rows whose maximum is near zero carry the rounding of l - m (see exp2_ff2)
-    if (fabsf(tk.m_p) < kNeedTwoSum || (tk.mode == kModeResidual && fabsf(tk.m_q) < kNeedTwoSum))
-        s_accumulate<DT, VEC, true>(P, b, i, tk, prow, qrow, tab, lane);
-    else
-        s_accumulate<DT, VEC, false>(P, b, i, tk, prow, qrow, tab, lane);
+    const bool twosum = fabsf(tk.m_p) < kNeedTwoSum || (tk.mode == kModeResidual && fabsf(tk.m_q) < kNeedTwoSum);
+    uint32_t lane_rm = 0;  // the draw's removed columns among this lane's (point-mass and tree residuals)
+    if (tk.nrm) {          // warp-uniform
+        int32_t rtok = -1;
+        if (!removed_tokens(P, b, tk, lane, rtok)) return;
+        lane_rm = removed_bits(rtok, tk.nrm, i * kSTask + 32 * lane, 32);
+    }
+    if (__any_sync(0xFFFFFFFFu, lane_rm != 0u)) {
+        if (twosum) s_accumulate<DT, VEC, true, true>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
+        else s_accumulate<DT, VEC, false, true>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
+    } else if (twosum) {
+        s_accumulate<DT, VEC, true, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
+    } else {
+        s_accumulate<DT, VEC, false, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
+    }
     if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0 + b + tk.npos, tab, lane);
 }
 
