@@ -1211,10 +1211,12 @@ __device__ __forceinline__ float2 pair8(const Cols8& c, int e) {
 // bf16 task's loads are all issued before the first step), accumulating the p and q weights and their
 // selected parts. It stores the selected sums of each group of kGroupLanes lanes, then the warp's sums
 // as the task's record. TWOSUM: carry the rounding of l - m (see exp2_ff2).
-template <int DT, bool VEC, bool TWOSUM, bool REMOVED>
+template <int DT, bool VEC, bool TWOSUM, bool REMOVED, bool RESID>
 __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, const TaskInfo& tk, size_t prow,
                                              size_t qrow, const float* tab, int lane, uint32_t lane_rm) {
-    const bool resid = tk.mode == kModeResidual;
+    // RESID: a residual draw (p and q rows); else p alone (bonus, point-mass and tree residuals). Each
+    // kind is its own instantiation, so each hot path's code is only its own.
+    constexpr bool resid = RESID;
     const float2 mp = f2(tk.m_p), mq = f2(tk.m_q);
     const int32_t cbase = i * kSTask;
     const ExpConst EC = exp_const(P);
@@ -1228,7 +1230,7 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
     // one step: 8 consecutive columns k, k + 1, ... of the lane (4 pairs) of the p row, and of the q row
     // for a residual
     auto step = [&](const Cols8& cp, const Cols8& cq, int32_t k) {
-        if (!REMOVED && resid) {
+        if (RESID) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
@@ -1342,12 +1344,15 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
         lane_rm = removed_bits(rtok, tk.nrm, i * kSTask + 32 * lane, 32);
     }
     if (__any_sync(0xFFFFFFFFu, lane_rm != 0u)) {
-        if (twosum) s_accumulate<DT, VEC, true, true>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
-        else s_accumulate<DT, VEC, false, true>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
+        if (twosum) s_accumulate<DT, VEC, true, true, false>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
+        else s_accumulate<DT, VEC, false, true, false>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
+    } else if (tk.mode == kModeResidual) {
+        if (twosum) s_accumulate<DT, VEC, true, false, true>(P, b, i, tk, prow, qrow, tab, lane, 0u);
+        else s_accumulate<DT, VEC, false, false, true>(P, b, i, tk, prow, qrow, tab, lane, 0u);
     } else if (twosum) {
-        s_accumulate<DT, VEC, true, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
+        s_accumulate<DT, VEC, true, false, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
     } else {
-        s_accumulate<DT, VEC, false, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
+        s_accumulate<DT, VEC, false, false, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
     }
     if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0 + b + tk.npos, tab, lane);
 }
