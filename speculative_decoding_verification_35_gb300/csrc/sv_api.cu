@@ -106,8 +106,8 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.out_n = out_num_accepted;
     P.status = device_status ? device_status : (uint32_t*)(ws + L.status);
     if (debug) P.dbg = *debug;
-    for (int j = 0; j < 64; ++j) {  // Tang's table: 2^(j/64) as a float pair (hi, lo)
-        const double v = std::exp2((double)j / 64.0);
+    for (int j = 0; j < 128; ++j) {  // Tang's table: 2^(j/128) as a float pair (hi, lo)
+        const double v = std::exp2((double)j / 128.0);
         const float hi = (float)v;
         P.exp2_tab[j] = make_float2(hi, (float)(v - (double)hi));
     }

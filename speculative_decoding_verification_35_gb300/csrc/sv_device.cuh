@@ -173,14 +173,15 @@ struct ffacc2 {
 // Constants of the precise exponential: K = log2(e) / T as float-float, and the clamp of l - m that
 // maps every argument at or below it (and -inf logits) to exactly 0.
 struct ExpConst {
-    float K_hi, K_lo, nK_hi;  // nK_hi = -K_hi
+    float K_hi, K_lo;         // log2(e) / T as float-float
     float d_min;              // about -126.5 / K: 2^(d_min K) would be subnormal
 };
 
 // 2^((l - m) K) for two columns, m the row maximum (so the argument is <= 0), as float-float with
-// relative error below about 1e-9. Tang's method: t = d K carried as t_hi + t_lo, j = rint(64 t),
-// 2^t = 2^(j >> 6) * 2^((j & 63) / 64) * e^y with |y| <= ln2/128 and e^y - 1 from its Taylor series.
-// tab holds 2^(i/64) split in floats: tab[i] (high part) and tab[64 + i] (low part), i = 0..63.
+// relative error below about 4e-10. Tang's method with a 128-entry table: t = d K, j = rint(128 t),
+// 2^t = 2^(j >> 7) * 2^((j & 127) / 128) * e^y, y = (t - j/128) ln 2, |y| <= ln2/256, and e^y - 1 from
+// its Taylor series to degree 3 (the next term is below 3e-12).
+// tab holds 2^(i/128) split in floats: tab[i] (high part) and tab[128 + i] (low part), i = 0..127.
 // TWOSUM: l - m is carried as float-float. For bf16 logits l - m rounds in float only when the two
 // exponents are more than 16 apart; with |m| >= 2^-4 that needs |l| >= 2^12 (a zero weight) or a
 // logit within 2^-16 |m| of zero (a single rare column, error below 1e-7 of its weight), so callers
@@ -188,6 +189,7 @@ struct ExpConst {
 // inputs) need it for every column.
 // Arguments at or below d_min K, including -inf logits, give exactly 0 (2^-126 and below only).
 constexpr float kNeedTwoSum = 0.0625f;
+constexpr int kExpTab = 128;
 template <bool TWOSUM = true>
 __device__ __forceinline__ ff2 exp2_ff2(float2 l, float2 m, const ExpConst& C, const float* tab) {
     float2 d = sub2(l, m);
@@ -199,29 +201,29 @@ __device__ __forceinline__ ff2 exp2_ff2(float2 l, float2 m, const ExpConst& C, c
         dl = make_float2(d.x > C.d_min ? dl.x : 0.f, d.y > C.d_min ? dl.y : 0.f);
     }
     d = make_float2(fmaxf(d.x, C.d_min), fmaxf(d.y, C.d_min));
-    const float2 nt = mul2(d, f2(C.nK_hi));          // -t_hi
-    float2 tl = fma2(d, f2(C.K_hi), nt);              // exact rounding error of d * K_hi
-    tl = fma2(d, f2(C.K_lo), tl);
-    if (TWOSUM) tl = fma2(dl, f2(C.K_hi), tl);
-    // j = rint(64 t_hi) lands in the low mantissa bits of jm (adding 1.5 * 2^23 rounds to an integer)
-    const float2 jm = fma2(nt, f2(-64.f), f2(12582912.f));
+    // adding 1.5 * 2^16 rounds d K_hi (exact inside the fused product-add) to a multiple of 1/128: the
+    // sum's unit in the last place; j lands in the low mantissa bits of jm
+    const float2 jm = fma2(d, f2(C.K_hi), f2(98304.f));
     const uint32_t b0 = __float_as_uint(jm.x), b1 = __float_as_uint(jm.y);
-    const float2 jf = add2(jm, f2(-12582912.f));
-    // r = t - j/64 = t_lo - (-t_hi + j/64), the bracket exact; y = r ln 2 with ln 2 in two parts
-    const float2 r = sub2(tl, fma2(jf, f2(0.015625f), nt));
-    const float2 y = fma2(r, f2(0.693145751953125f), mul2(r, f2(1.42860682030941723212e-6f)));
-    float2 c = fma2(y, f2(1.0f / 24.0f), f2(1.0f / 6.0f));
-    c = fma2(c, y, f2(0.5f));
-    const float2 em1 = fma2(mul2(c, y), y, y);  // e^y - 1
-    const uint32_t i0 = b0 & 63u, i1 = b1 & 63u;
-    const float2 Th = make_float2(tab[i0], tab[i1]), Tl = make_float2(tab[64 + i0], tab[64 + i1]);
+    const float2 njf = sub2(f2(98304.f), jm);  // -j/128, exact
+    // r = t - j/128 = (d K_hi - j/128) + d K_lo: |r| <= 1/256 + 2^-17, each step rounds once (<= 2^-33)
+    float2 r = fma2(d, f2(C.K_hi), njf);
+    r = fma2(d, f2(C.K_lo), r);
+    if (TWOSUM) r = fma2(dl, f2(C.K_hi), r);
+    // e^(r ln2) - 1 = r ln2 + r^2 (ln2)^2 / 2 + r^3 (ln2)^3 / 6, ln2 = L_hi + L_lo: the leading product
+    // r L_hi is exact inside the last fused product-add, so em1 rounds once
+    float2 c = fma2(r, f2(0.05550410866482158f), f2(0.2402265069591007f));
+    c = fma2(c, r, f2(-1.904654299957768e-09f));
+    const float2 em1 = fma2(r, f2(0.693147182464599609375f), mul2(c, r));
+    const uint32_t i0 = b0 & (kExpTab - 1), i1 = b1 & (kExpTab - 1);
+    const float2 Th = make_float2(tab[i0], tab[i1]), Tl = make_float2(tab[kExpTab + i0], tab[kExpTab + i1]);
     // Th (1 + em1) + Tl (1 + em1) as h + lo: Th - h is exact, and the fused product-add recovers
     // the rounding error of h
     const float2 h = fma2(Th, em1, Th);
     const float2 lo = add2(fma2(Th, em1, sub2(Th, h)), fma2(Tl, em1, Tl));
-    // 2^n, n = floor(j / 64), from j << 17 masked to the exponent field; n = -127 gives exactly 0
-    const float2 sc = make_float2(__uint_as_float(((b0 << 17) & 0xFF800000u) + 0x3F800000u),
-                                  __uint_as_float(((b1 << 17) & 0xFF800000u) + 0x3F800000u));
+    // 2^n, n = floor(j / 128): (j - (j & 127)) << 16 is n in the exponent field; n = -127 gives exactly 0
+    const float2 sc = make_float2(__uint_as_float(((b0 - i0) << 16) + 0x3F800000u),
+                                  __uint_as_float(((b1 - i1) << 16) + 0x3F800000u));
     return ff2{mul2(h, sc), mul2(lo, sc)};
 }
 

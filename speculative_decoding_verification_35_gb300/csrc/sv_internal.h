@@ -110,7 +110,7 @@ struct Params {
     int32_t cap;
     int32_t* lens;
     int32_t* next;
-    float2 exp2_tab[64];  // 2^(j/64), j = 0..63, as (hi, lo) floats, built on the host
+    float2 exp2_tab[128];  // 2^(j/128), j = 0..127, as (hi, lo) floats, built on the host
 };
 
 struct Layout {

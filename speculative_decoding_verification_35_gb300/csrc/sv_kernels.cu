@@ -147,15 +147,15 @@ __device__ __forceinline__ float logit_at(const void* base, size_t idx) {
     return __ldg((const float*)base + idx);
 }
 
-// Shared-memory copy of the table of 2^(j/64), j = 0..63 (built on the host): high parts in
-// tab[0..63], low parts in tab[64..127].
+// Shared-memory copy of the table of 2^(j/128), j = 0..127 (built on the host): high parts in
+// tab[0..127], low parts in tab[128..255].
 __device__ __forceinline__ void fill_exp2_table(const Params& P, float* tab) {
-    if (threadIdx.x < 64) {
+    if (threadIdx.x < kExpTab) {
         tab[threadIdx.x] = P.exp2_tab[threadIdx.x].x;
-        tab[64 + threadIdx.x] = P.exp2_tab[threadIdx.x].y;
+        tab[kExpTab + threadIdx.x] = P.exp2_tab[threadIdx.x].y;
     }
 }
-__device__ __forceinline__ ExpConst exp_const(const Params& P) { return ExpConst{P.K_hi, P.K_lo, -P.K_hi, P.d_min}; }
+__device__ __forceinline__ ExpConst exp_const(const Params& P) { return ExpConst{P.K_hi, P.K_lo, P.d_min}; }
 
 // ------------------------------------------------------------------------------------------------
 // Statistics of one row segment [0, len) of up to 4096 columns, one warp. Result on every lane:
@@ -1520,7 +1520,7 @@ template <int DT, bool VEC, bool GREEDY>
 __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ Params P) {
     constexpr bool kBulk = DT == SV_BF16 && VEC && !GREEDY;
     extern __shared__ __align__(128) unsigned char dsmem[];
-    __shared__ float tab[128];
+    __shared__ float tab[2 * kExpTab];
     __shared__ int s_bad;
     __shared__ int32_t s_base[kBaseCache];
     __shared__ int32_t s_row[GREEDY ? 1 : kRowCache];
