@@ -111,6 +111,36 @@ __device__ __forceinline__ ff warp_sum_ff(ff a) {
         a = ff_add(a, ff{__shfl_xor_sync(0xFFFFFFFFu, a.hi, o), __shfl_xor_sync(0xFFFFFFFFu, a.lo, o)});
     return a;
 }
+// The butterfly's remaining levels o0, 2 o0, ..., 16 (a sum already complete over groups of o0 lanes).
+__device__ __forceinline__ ff warp_sum_ff_from(ff a, int o0) {
+#pragma unroll
+    for (int o = o0; o < 32; o <<= 1)
+        a = ff_add(a, ff{__shfl_xor_sync(0xFFFFFFFFu, a.hi, o), __shfl_xor_sync(0xFFFFFFFFu, a.lo, o)});
+    return a;
+}
+// Two float-float values carried lane-wise in packed pairs (x: the first value, y: the second), so that
+// two sums share each f32x2 instruction; every component takes exactly the scalar ff_add's steps.
+struct ffp {
+    float2 hi, lo;
+};
+__device__ __forceinline__ ffp ffp_add(ffp a, ffp b) {
+    const float2 s = add2(a.hi, b.hi);  // TwoSum of the high parts
+    const float2 bb = sub2(s, a.hi);
+    const float2 e = add2(sub2(a.hi, sub2(s, bb)), sub2(b.hi, bb));
+    const float2 l = add2(e, add2(a.lo, b.lo));
+    const float2 h = add2(s, l);  // Fast2Sum normalisation
+    return ffp{h, sub2(l, sub2(h, s))};
+}
+__device__ __forceinline__ ffp shfl_xor_ffp(ffp v, int o) {
+    return ffp{make_float2(__shfl_xor_sync(0xFFFFFFFFu, v.hi.x, o), __shfl_xor_sync(0xFFFFFFFFu, v.hi.y, o)),
+               make_float2(__shfl_xor_sync(0xFFFFFFFFu, v.lo.x, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo.y, o))};
+}
+// lane_ff of two accumulator pairs at once: x from (ha, la), y from (hb, lb)
+__device__ __forceinline__ ffp lane_ffp(float2 ha, float2 la, float2 hb, float2 lb) {
+    return ffp_add(ffp{make_float2(ha.x, hb.x), make_float2(la.x, lb.x)},
+                   ffp{make_float2(ha.y, hb.y), make_float2(la.y, lb.y)});
+}
+
 // Inclusive float-float prefix over the warp.
 __device__ __forceinline__ ff warp_inscan_ff(ff v, int lane) {
 #pragma unroll
@@ -1295,30 +1325,38 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
         }
         step(cp, cq, cbase + 32 * lane + 8 * e);
     }
-    // the group words first (read by the find only, which polls them): sums over kGroupLanes lanes
-    const bool sel = resid || excl;  // the selected sums differ from the p sums
-    ff ga = sel ? lane_ff(Ah, Al) : lane_ff(Ph, Pl), gb = resid ? lane_ff(Bh, Bl) : ff{0.f, 0.f};
-#pragma unroll
-    for (int o = 1; o < kGroupLanes; o <<= 1) {
-        ga = ff_add(ga, ff{__shfl_xor_sync(0xFFFFFFFFu, ga.hi, o), __shfl_xor_sync(0xFFFFFFFFu, ga.lo, o)});
-        gb = ff_add(gb, ff{__shfl_xor_sync(0xFFFFFFFFu, gb.hi, o), __shfl_xor_sync(0xFFFFFFFFu, gb.lo, o)});
-    }
-    if (lane % kGroupLanes == 0) {
-        Word* gw = P.groupw + (((size_t)b * P.nS + i) * kGroups + lane / kGroupLanes) * kGroupWords;
-        st_word(gw, pack_ff(ga));
-        st_word(gw + 1, pack_ff(gb));
-    }
-    const ff sp = warp_sum_ff(lane_ff(Ph, Pl));
-    ff mine = sp;  // record word `lane` (lanes 0-3)
+    // the group words first (read by the find only, which polls them): sums over kGroupLanes lanes; the
+    // record's selected sums continue the same butterfly from the group sums
+    static_assert(kGroupLanes == 4, "two butterfly levels per group");
+    Word* gw = P.groupw + (((size_t)b * P.nS + i) * kGroups + lane / kGroupLanes) * kGroupWords;
+    ff mine;  // record word `lane` (lanes 0-3)
     if (resid) {
-        const ff sq = warp_sum_ff(lane_ff(Qh, Ql)), sa = warp_sum_ff(lane_ff(Ah, Al));
-        const ff sb = warp_sum_ff(lane_ff(Bh, Bl));
-        mine = lane == 1 ? sq : lane == 2 ? sa : lane == 3 ? sb : sp;
-    } else if (excl) {
-        const ff sa = warp_sum_ff(lane_ff(Ah, Al));
-        mine = lane == 2 ? sa : (lane == 1 || lane == 3) ? ff{0.f, 0.f} : sp;
-    } else if (lane == 1 || lane == 3) {
-        mine = ff{0.f, 0.f};
+        ffp g = lane_ffp(Ah, Al, Bh, Bl);  // (selected p, selected q)
+        g = ffp_add(g, shfl_xor_ffp(g, 1));
+        g = ffp_add(g, shfl_xor_ffp(g, 2));
+        if (lane % kGroupLanes == 0) {
+            st_word(gw, pack_ff(ff{g.hi.x, g.lo.x}));
+            st_word(gw + 1, pack_ff(ff{g.hi.y, g.lo.y}));
+        }
+        ffp t = lane_ffp(Ph, Pl, Qh, Ql);  // (all p, all q)
+#pragma unroll
+        for (int o = 16; o; o >>= 1) t = ffp_add(t, shfl_xor_ffp(t, o));
+#pragma unroll
+        for (int o = kGroupLanes; o < 32; o <<= 1) g = ffp_add(g, shfl_xor_ffp(g, o));
+        const ffp r = lane & 2 ? g : t;
+        mine = lane & 1 ? ff{r.hi.y, r.lo.y} : ff{r.hi.x, r.lo.x};
+    } else {
+        // excl: the group words hold the selected p sums; else the p sums (a bonus draw's selected sums)
+        ff ga = excl ? lane_ff(Ah, Al) : lane_ff(Ph, Pl);
+        ga = ff_add(ga, ff{__shfl_xor_sync(0xFFFFFFFFu, ga.hi, 1), __shfl_xor_sync(0xFFFFFFFFu, ga.lo, 1)});
+        ga = ff_add(ga, ff{__shfl_xor_sync(0xFFFFFFFFu, ga.hi, 2), __shfl_xor_sync(0xFFFFFFFFu, ga.lo, 2)});
+        if (lane % kGroupLanes == 0) {
+            st_word(gw, pack_ff(ga));
+            st_word(gw + 1, pack_ff(ff{0.f, 0.f}));
+        }
+        const ff sa = warp_sum_ff_from(ga, kGroupLanes);
+        const ff sp = excl ? warp_sum_ff(lane_ff(Ph, Pl)) : sa;
+        mine = (lane == 1 || lane == 3) ? ff{0.f, 0.f} : lane == 2 ? sa : sp;
     }
     if (lane < kRecWords) st_word(P.recw + ((size_t)b * P.nS + i) * kRecWords + lane, pack_ff(mine));
 }
