@@ -563,10 +563,25 @@ __device__ __noinline__ void tree_sampled(const Params& P, int32_t b, int32_t g,
 // both uniforms of every slot) is fetched before the partials are polled. Rows are reduced 8 at a
 // time without control flow between them, so their shuffle trees overlap.
 // ------------------------------------------------------------------------------------------------
+// Row statistics shared by the warps of a cooperative decision: (max, sum) per statistics row, and
+// the error bits of the rows; two sets, used by alternate decisions of the CTA.
+struct CoopRows {
+    float2 rs[2][2 * 32];
+    uint32_t err[2];
+};
+
+// nsub > 1: a cooperative decision. Warp wsub of the nsub deciding warps of the CTA reduces the rows
+// wsub, wsub + nsub, ...; the row statistics meet in shared memory (set `set` of `co`) behind a named
+// barrier over the deciding warps, and warp 0 goes on alone (the others return after the barrier).
+// nsub == 1: the warp reduces every row itself.
 template <int DT, bool GREEDY>
-__device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float* tab) {
+__device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float* tab,
+                                    int wsub, int nsub, CoopRows* co, int set) {
     const int32_t t0 = o0 + b;
-    const int nrows = stat_rows<GREEDY>(P, g);
+    const int nrows_all = stat_rows<GREEDY>(P, g);
+    // this warp's rows: jr = wsub + nsub * j, j = 0 .. nrows - 1
+    const int nrows = nrows_all > wsub ? (nrows_all - wsub + nsub - 1) / nsub : 0;
+    auto row_of = [&](int j) { return wsub + nsub * j; };
     const int32_t sbase = GREEDY || P.pm ? o0 + b : 2 * o0 + b;
     const int nch = P.nchA;
     const float K = P.K_hi;
@@ -577,7 +592,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             q[k] = j0 + k < nrows && c0 + lane < nch
-                       ? ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c0 + lane) : 1ull;
+                       ? ld_word(P.partials + (size_t)(sbase + row_of(j0 + k)) * nch + c0 + lane) : 1ull;
     };
     PartialWord qn[8];
     load_block(0, 0, qn);
@@ -586,7 +601,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     float lt = 0.f, ld = 0.f, u_acc = 0.f, u_draw = 0.f;
     // the node whose target row tests slot `lane`: its parent in a token tree, the slot itself otherwise
     int32_t par = lane;
-    if (lane < g) {
+    if (wsub == 0 && lane < g) {
         x = __ldg(P.tokens + o0 + lane);
         if (P.parents) {
             par = __ldg(P.parents + o0 + lane);
@@ -601,7 +616,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
             if (!P.pm) ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
         }
     }
-    if (!GREEDY) {
+    if (!GREEDY && wsub == 0) {
         if (lane < g) u_acc = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);
         if (lane <= g) u_draw = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 1);
     }
@@ -637,7 +652,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
                 ns = ns < 256 ? 2 * ns : 256;
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    if (q[k] == 0) q[k] = ld_word(P.partials + (size_t)(sbase + j0 + k) * nch + c);
+                    if (q[k] == 0) q[k] = ld_word(P.partials + (size_t)(sbase + row_of(j0 + k)) * nch + c);
             }
             {  // the next block's loads, in flight while this block is merged and reduced
                 const int nc0 = c0 + 32 < nch ? c0 + 32 : 0, nj0 = c0 + 32 < nch ? j0 : j0 + 8;
@@ -698,17 +713,39 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
             }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const int jr = j0 + k;
-            const bool in = jr < nrows;
+            const bool in = j0 + k < nrows;
+            const int jr = row_of(j0 + k);
             // a row with a NaN or +inf is reported as such, not as empty (both fail the sequence)
             const uint32_t rf = GREEDY ? (F[k] | (M[k] == INFINITY ? 1u << SV_ERR_NONFINITE : 0u))
                                        : (S[k] != S[k] ? 1u << SV_ERR_NONFINITE : 0u);
             if (in) err |= rf | (M[k] == -INFINITY && !rf ? 1u << SV_ERR_EMPTY_ROW : 0u);
-            if (in && lane == jr) { my_m0 = M[k]; my_s0 = GREEDY ? 0.f : S[k]; my_a0 = GREEDY ? A[k] : -1; }
-            if (in && lane == jr - 32) { my_m1 = M[k]; my_s1 = GREEDY ? 0.f : S[k]; }
+            if (nsub > 1) {
+                if (in && lane == 0) co->rs[set][jr] = make_float2(M[k], GREEDY ? 0.f : S[k]);
+            } else {
+                if (in && lane == jr) { my_m0 = M[k]; my_s0 = GREEDY ? 0.f : S[k]; my_a0 = GREEDY ? A[k] : -1; }
+                if (in && lane == jr - 32) { my_m1 = M[k]; my_s1 = GREEDY ? 0.f : S[k]; }
+            }
         }
     }
     err = warp_or(err);
+    if (nsub > 1) {  // meet the other deciding warps; warp 0 continues with every row's statistics
+        if (lane == 0 && err) atomicOr(&co->err[set], err);
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * nsub) : "memory");
+        if (wsub != 0) return;
+        err = co->err[set];
+        if (lane < nrows_all) {
+            const float2 r0 = co->rs[set][lane];
+            my_m0 = r0.x;
+            my_s0 = r0.y;
+        }
+        if (lane + 32 < nrows_all) {
+            const float2 r1 = co->rs[set][lane + 32];
+            my_m1 = r1.x;
+            my_s1 = r1.y;
+        }
+        __syncwarp();
+        if (lane == 0) co->err[set] = 0u;  // read by every lane above; cleared for the set's next use
+    }
     if (err) {
         if (lane == 0) {
             atomicOr(P.status, err);
@@ -759,7 +796,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int jr = lane + 32 * h;
-            if (jr < nrows) {
+            if (jr < nrows_all) {
                 const float m = h ? my_m1 : my_m0, sum = h ? my_s1 : my_s0;
                 const double lse = (double)m * P.invT64 + log((double)sum);
                 P.dbg.row_lse[jr <= g ? t0 + jr : R_t + o0 + (jr - g - 1)] = lse;
@@ -1456,9 +1493,11 @@ __device__ __forceinline__ void a_finish(const Params& P, const ATask& at, const
     }
 }
 
-// Decision of sequence b, run by its decider warp; it polls the partial words itself.
+// Decision of sequence b, run by its decider warp (or, cooperative, by the CTA's deciding warps); the
+// deciding warps poll the partial words themselves.
 template <int DT, bool GREEDY>
-__device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, const float* tab, int lane) {
+__device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, const float* tab, int lane, int wsub,
+                            int nsub, CoopRows* co, int set) {
     int32_t o0, g;
     if (bases) {  // from the validated offsets cached in shared memory: no dependent global load
         const int32_t s0 = bases[b], s1 = bases[b + 1];
@@ -1468,7 +1507,7 @@ __device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, co
         o0 = __ldg(P.offs + b);
         g = __ldg(P.gammas + b);
     }
-    decide<DT, GREEDY>(P, b, g, o0, lane, tab);
+    decide<DT, GREEDY>(P, b, g, o0, lane, tab, wsub, nsub, co, set);
 }
 
 // A streamer warp on the bulk-copy path: its statistics tasks (statically strided over all streamers)
@@ -1562,9 +1601,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     __shared__ int s_bad;
     __shared__ int32_t s_base[kBaseCache];
     __shared__ int32_t s_row[GREEDY ? 1 : kRowCache];
+    __shared__ CoopRows s_coop;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (!GREEDY) fill_exp2_table(P, tab);
-    if (tid == 0) s_bad = __ldg(P.offs) != 0;
+    if (tid == 0) {
+        s_bad = __ldg(P.offs) != 0;
+        s_coop.err[0] = s_coop.err[1] = 0u;
+    }
     __syncthreads();
     // every CTA checks the whole CSR structure before any row is read (and caches small batches' row
     // bases, b = 0..B, for the statistics tasks and the decisions)
@@ -1629,8 +1672,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     const bool streamer = kBulk && warp >= kWarps - kStreamWarps;
     const uint32_t ND = kBulk ? gridDim.x * (kWarps - kStreamWarps) : gridDim.x * kWarps;
     const uint32_t did = kBulk ? blockIdx.x * (kWarps - kStreamWarps) + warp : blockIdx.x * kWarps + warp;
-    if (!streamer)
-        for (uint32_t b = did; b < (uint32_t)P.B; b += ND) lead_decide<DT, GREEDY>(P, (int32_t)b, bases, tab, lane);
+    // Cooperative decisions when every CTA holds at most one: the non-streaming warps of CTA c share the
+    // rows of sequence c (the decision's latency, not its throughput, is what the step waits for)
+    const bool coop = kBulk && (uint32_t)P.B <= gridDim.x;
+    if (coop) {
+        if (!streamer && blockIdx.x < (uint32_t)P.B)
+            lead_decide<DT, GREEDY>(P, (int32_t)blockIdx.x, bases, tab, lane, warp, kWarps - kStreamWarps, &s_coop, 0);
+    } else if (!streamer) {
+        for (uint32_t b = did; b < (uint32_t)P.B; b += ND) lead_decide<DT, GREEDY>(P, (int32_t)b, bases, tab, lane, 0, 1, &s_coop, 0);
+    }
     if constexpr (!GREEDY) {
         while (true) {
             uint32_t t = 0;

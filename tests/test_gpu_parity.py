@@ -51,6 +51,15 @@ def test_ragged_tiles_and_unaligned_rows(name, B, V):
         parity.assert_parity(b, 99, step)
 
 
+def test_more_sequences_than_ctas():
+    # bf16 rows with V * 2 a multiple of 16 take the bulk-copy path; with more sequences than CTAs (304
+    # on a GB300) each decision is made by one warp instead of by a CTA's deciding warps together
+    b = synth.make_batch("b64_g5_v128256", B=400, V=2048)
+    parity.assert_parity(b, 77, 0)
+    bp = synth.make_batch("pointmass_b64_g5_v128256", B=350, V=1024)
+    parity.assert_parity(bp, 77, 1)
+
+
 def test_gamma_zero_and_max_gamma():
     b = synth.make_batch("ragged_b128_v129280", B=6, V=3000, gammas=[0, 31, 1, 0, 7, 31])
     for step in range(3):
