@@ -260,10 +260,15 @@ __device__ __forceinline__ SegStats stats_bf16(const uint4 (&v)[16], float K) {
 __device__ __forceinline__ SegStats stats_bf16_smem(const unsigned char* buf, int len, int lane, float K) {
     uint4 v[16];
     const uint4* b4 = reinterpret_cast<const uint4*>(buf);
+    if (len == kAChunk) {  // a full task (all but a row's last): no per-read guard
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const int e0 = (q * 32 + lane) * 8;
-        v[q] = e0 < len ? b4[q * 32 + lane] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        for (int q = 0; q < 16; ++q) v[q] = b4[q * 32 + lane];
+    } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int e0 = (q * 32 + lane) * 8;
+            v[q] = e0 < len ? b4[q * 32 + lane] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        }
     }
     return stats_bf16(v, K);
 }
