@@ -119,6 +119,42 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
                    const sv_debug* debug, void* cuda_stream);
 
 /*
+ * Device staging buffers of spec_verify_host, sized by the caller for the batch: target_logits
+ * R_t x V elements, draft_logits R_d x V (may be NULL when the host call passes no draft logits),
+ * draft_tokens R_d, seq_offsets B + 1, gammas B, out_tokens R_t, out_num_accepted B (R_d =
+ * seq_offsets[B], R_t = R_d + B). Alignment rules as for spec_verify_ex's device arguments.
+ */
+typedef struct {
+    void* target_logits;
+    void* draft_logits;
+    int32_t* draft_tokens;
+    int32_t* seq_offsets;
+    int32_t* gammas;
+    int32_t* out_tokens;
+    int32_t* out_num_accepted;
+} sv_device_buffers;
+
+/*
+ * Host-buffer form: the step on inputs and outputs in host memory ("Accelerating Sonar through
+ * speculation", §"Speculative decoding": the target model's logits for the gamma + 1 positions are
+ * verified and the accepted tokens returned to the caller). On `cuda_stream`, in this order: the inputs
+ * are copied from host memory into the staging buffers `dev`, the step runs as spec_verify_ex on them,
+ * and the tokens and accepted counts are copied back to out_tokens / out_num_accepted in host memory.
+ * With page-locked host memory every copy is asynchronous and the outputs are valid once the stream has
+ * synchronised; with pageable memory the CUDA runtime may synchronise inside the copies. seq_offsets[B]
+ * is read on the host to size the copies (SV_ERR_INVALID_ARG unless 0 <= seq_offsets[B] <=
+ * B * max_gamma); the device still checks the whole CSR structure. Every argument check of
+ * spec_verify_ex runs on the staging buffers before anything is enqueued. The host arrays, staging
+ * buffers and workspace must stay valid until the stream has passed the call's work. The library owns
+ * none of the buffers.
+ */
+int spec_verify_host(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                     const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas, int32_t B,
+                     int32_t V, int32_t max_gamma, float temperature, uint64_t seed, uint64_t step,
+                     int32_t* out_tokens, int32_t* out_num_accepted, const sv_device_buffers* dev,
+                     uint32_t* device_status, void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Allocation-free form, for callers that cannot call cudaMalloc (for example code running inside a
  * stream capture it does not own, or a runtime without a device allocator). The pages describe no
  * such entry point; it exists for those callers only. It behaves as spec_verify_ex on the same

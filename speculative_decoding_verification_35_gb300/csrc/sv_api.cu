@@ -56,7 +56,8 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
                 const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, int32_t max_gamma,
                 float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
                 uint32_t* device_status, void* workspace, size_t workspace_bytes, const sv_debug* debug,
-                const CommitBufs* commit, const int32_t* parents, int32_t* out_path, void* cuda_stream) {
+                const CommitBufs* commit, const int32_t* parents, int32_t* out_path, void* cuda_stream,
+                bool validate_only = false) {
     if (B < 0 || V < 1 || max_gamma < 0 || max_gamma > SV_MAX_GAMMA) return SV_ERR_INVALID_ARG;
     if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
     if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
@@ -78,6 +79,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
         return SV_ERR_INVALID_ARG;
     const Layout L = workspace_layout(B, V, max_gamma);
     if (!workspace || workspace_bytes < L.total || (uintptr_t)workspace % 256) return SV_ERR_WORKSPACE;
+    if (validate_only) return SV_OK;
 
     const bool uses_draft = !greedy && max_gamma > 0 && draft_logits;
     const bool vec = (uintptr_t)target_logits % 16 == 0 && (!uses_draft || (uintptr_t)draft_logits % 16 == 0) &&
@@ -173,6 +175,56 @@ int spec_verify_tree(const void* target_logits, sv_dtype dtype, const int32_t* d
     return verify_impl(target_logits, nullptr, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
                        temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
                        workspace_bytes, nullptr, nullptr, max_gamma > 0 ? parents : nullptr, out_path, cuda_stream);
+}
+
+int spec_verify_host(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                     const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas, int32_t B,
+                     int32_t V, int32_t max_gamma, float temperature, uint64_t seed, uint64_t step,
+                     int32_t* out_tokens, int32_t* out_num_accepted, const sv_device_buffers* dev,
+                     uint32_t* device_status, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    if (!dev || B < 0 || V < 1 || max_gamma < 0 || max_gamma > SV_MAX_GAMMA || (B > 0 && !seq_offsets))
+        return SV_ERR_INVALID_ARG;
+    if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    // the draft rows, from the host copy of the offsets (the device re-checks the whole structure)
+    const int64_t R_d = seq_offsets[B];
+    if (R_d < 0 || R_d > (int64_t)B * max_gamma) return SV_ERR_INVALID_ARG;
+    const int64_t R_t = R_d + B;
+    const bool with_draft = draft_logits != nullptr;
+    const bool with_tokens = draft_tokens != nullptr;
+    if (!target_logits || !gammas || !out_tokens || !out_num_accepted || (with_draft && !dev->draft_logits) ||
+        (with_tokens && !dev->draft_tokens))
+        return SV_ERR_INVALID_ARG;
+    // every argument check of the step, on the staging buffers, before anything is enqueued
+    const int rc = verify_impl(dev->target_logits, with_draft ? dev->draft_logits : nullptr, dtype,
+                               with_tokens ? dev->draft_tokens : nullptr, dev->seq_offsets, dev->gammas, B, V,
+                               max_gamma, temperature, seed, step, dev->out_tokens, dev->out_num_accepted,
+                               device_status, workspace, workspace_bytes, nullptr, nullptr, nullptr, nullptr,
+                               cuda_stream, true);
+    if (rc != SV_OK) return rc;
+    cudaStream_t st = (cudaStream_t)cuda_stream;
+    const size_t esz = dtype == SV_BF16 ? 2 : 4;
+    auto h2d = [&](void* d, const void* h, size_t bytes) {
+        return bytes == 0 || cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    if (!h2d(dev->target_logits, target_logits, (size_t)R_t * (size_t)V * esz) ||
+        (with_draft && !h2d(dev->draft_logits, draft_logits, (size_t)R_d * (size_t)V * esz)) ||
+        (with_tokens && !h2d(dev->draft_tokens, draft_tokens, (size_t)R_d * sizeof(int32_t))) ||
+        !h2d(dev->seq_offsets, seq_offsets, (size_t)(B + 1) * sizeof(int32_t)) ||
+        !h2d(dev->gammas, gammas, (size_t)B * sizeof(int32_t)))
+        return SV_ERR_CUDA;
+    const int r2 = verify_impl(dev->target_logits, with_draft ? dev->draft_logits : nullptr, dtype,
+                               with_tokens ? dev->draft_tokens : nullptr, dev->seq_offsets, dev->gammas, B, V,
+                               max_gamma, temperature, seed, step, dev->out_tokens, dev->out_num_accepted,
+                               device_status, workspace, workspace_bytes, nullptr, nullptr, nullptr, nullptr,
+                               cuda_stream);
+    if (r2 != SV_OK) return r2;
+    if (cudaMemcpyAsync(out_tokens, dev->out_tokens, (size_t)R_t * sizeof(int32_t), cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(out_num_accepted, dev->out_num_accepted, (size_t)B * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess)
+        return SV_ERR_CUDA;
+    return SV_OK;
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,

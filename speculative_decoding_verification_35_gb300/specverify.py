@@ -20,12 +20,19 @@ SV_MAX_GAMMA = 31
 # every exported symbol of the C ABI, in header order
 EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
            "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
-           "spec_verify_status_from_bits", "spec_verify_status_string")
+           "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host")
 
 
 class SvDebug(ctypes.Structure):
     _fields_ = [("row_lse", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p),
                 ("p_x", ctypes.c_void_p), ("q_x", ctypes.c_void_p), ("seq_mass", ctypes.c_void_p)]
+
+
+class SvDeviceBuffers(ctypes.Structure):
+    """Device staging buffers of spec_verify_host (device addresses)."""
+    _fields_ = [("target_logits", ctypes.c_void_p), ("draft_logits", ctypes.c_void_p),
+                ("draft_tokens", ctypes.c_void_p), ("seq_offsets", ctypes.c_void_p), ("gammas", ctypes.c_void_p),
+                ("out_tokens", ctypes.c_void_p), ("out_num_accepted", ctypes.c_void_p)]
 
 
 def _load():
@@ -53,6 +60,9 @@ def _load():
     L.spec_verify_tree.argtypes = [vp, ctypes.c_int, vp, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp, vp, vp, vp,
                                    sz, vp]
     L.spec_verify_tree.restype = ctypes.c_int
+    L.spec_verify_host.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
+                                   ctypes.POINTER(SvDeviceBuffers), vp, vp, sz, vp]
+    L.spec_verify_host.restype = ctypes.c_int
     L.spec_verify_status_from_bits.argtypes = [ctypes.c_uint32]
     L.spec_verify_status_from_bits.restype = ctypes.c_int
     L.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -128,6 +138,16 @@ def spec_verify_tree(target_logits, dtype, draft_tokens, parents, seq_offsets, g
                                 workspace, workspace_bytes, cuda_stream)
 
 
+def spec_verify_host(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                     temperature, seed, step, out_tokens, out_num_accepted, dev: SvDeviceBuffers | None,
+                     device_status, workspace, workspace_bytes, cuda_stream) -> int:
+    """Host-buffer form: host addresses for the inputs and outputs, device staging buffers in ``dev``."""
+    return lib.spec_verify_host(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V,
+                                max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
+                                ctypes.byref(dev) if dev is not None else None, device_status, workspace,
+                                workspace_bytes, cuda_stream)
+
+
 def spec_verify_status_from_bits(bits: int) -> int:
     return lib.spec_verify_status_from_bits(bits)
 
@@ -187,6 +207,22 @@ class Call:
                               _ptr(seq_offsets), _ptr(gammas), self.B, self.V, self.max_gamma, temperature,
                               seed, step, _ptr(self.out_tokens), _ptr(self.out_n), _ptr(self.status),
                               _ptr(self.workspace), self.ws_bytes, self.dbg_struct, st.cuda_stream)
+
+    def run_host(self, target, draft, draft_tokens, seq_offsets, gammas, temperature, seed, step, out_tokens,
+                 out_num_accepted, staging, stream=None, clear_status=True) -> int:
+        """Enqueue spec_verify_host: host tensors in (page-locked for asynchronous copies) and out, device
+        staging tensors in ``staging`` (keys target, draft, draft_tokens, seq_offsets, gammas)."""
+        import torch
+        if clear_status:
+            self.status.zero_()
+        st = stream if stream is not None else torch.cuda.current_stream()
+        dev = SvDeviceBuffers(_ptr(staging["target"]), _ptr(staging.get("draft")), _ptr(staging.get("draft_tokens")),
+                              _ptr(staging["seq_offsets"]), _ptr(staging["gammas"]), _ptr(self.out_tokens),
+                              _ptr(self.out_n))
+        return spec_verify_host(_ptr(target), _ptr(draft), dtype_code(target), _ptr(draft_tokens), _ptr(seq_offsets),
+                                _ptr(gammas), self.B, self.V, self.max_gamma, temperature, seed, step,
+                                _ptr(out_tokens), _ptr(out_num_accepted), dev, _ptr(self.status),
+                                _ptr(self.workspace), self.ws_bytes, st.cuda_stream)
 
     def commit(self, seq_offsets, history, capacity, lengths, next_tokens, stream=None) -> int:
         """Enqueue spec_verify_commit on this call's outputs (same stream, no host sync)."""

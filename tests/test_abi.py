@@ -30,7 +30,7 @@ def test_header_declares_the_api():
     names = declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
                           "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
-                          "spec_verify_status_from_bits", "spec_verify_status_string"}
+                          "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host"}
 
 
 def test_library_exports_every_declared_symbol(libpath):
@@ -173,3 +173,34 @@ def test_tree_host_side_checks_without_gpu(libpath):
     assert call(out_path=fake + 1) == sv.SV_ERR_INVALID_ARG
     assert call(max_gamma=32) == sv.SV_ERR_INVALID_ARG
     assert call(workspace=None) == sv.SV_ERR_WORKSPACE
+
+
+def test_host_buffer_form_checks_without_gpu(libpath):
+    import numpy as np
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    fake = 1 << 20  # device staging addresses, never dereferenced: every call below fails its host checks
+    offs = np.array([0, 4, 8, 12, 16], dtype=np.int32)  # read on the host by this entry point
+    gam = np.full(4, 4, dtype=np.int32)
+    dev = sv.SvDeviceBuffers(fake, fake, fake, fake, fake, fake, fake)
+    args = dict(target_logits=fake, draft_logits=fake, dtype=sv.SV_BF16, draft_tokens=fake,
+                seq_offsets=offs.ctypes.data, gammas=gam.ctypes.data, B=4, V=100, max_gamma=4, temperature=1.0,
+                seed=1, step=0, out_tokens=fake, out_num_accepted=fake, dev=dev, device_status=None, workspace=fake,
+                workspace_bytes=1 << 30, cuda_stream=None)
+
+    def call(**kw):
+        a = dict(args); a.update(kw)
+        return sv.spec_verify_host(**a)
+
+    assert call(dev=None) == sv.SV_ERR_INVALID_ARG
+    assert call(max_gamma=32) == sv.SV_ERR_INVALID_ARG
+    assert call(dtype=7) == sv.SV_ERR_INVALID_ARG
+    assert call(seq_offsets=None) == sv.SV_ERR_INVALID_ARG
+    bad = offs.copy(); bad[4] = -1
+    assert call(seq_offsets=bad.ctypes.data) == sv.SV_ERR_INVALID_ARG
+    bad[4] = 17  # more draft rows than B * max_gamma
+    assert call(seq_offsets=bad.ctypes.data) == sv.SV_ERR_INVALID_ARG
+    assert call(target_logits=None) == sv.SV_ERR_INVALID_ARG
+    assert call(dev=sv.SvDeviceBuffers(fake, None, fake, fake, fake, fake, fake)) == sv.SV_ERR_INVALID_ARG
+    assert call(temperature=float("nan")) == sv.SV_ERR_INVALID_ARG
+    assert call(workspace=None) == sv.SV_ERR_WORKSPACE
+    assert call(B=0) == sv.SV_OK

@@ -60,6 +60,30 @@ def test_more_sequences_than_ctas():
     parity.assert_parity(bp, 77, 1)
 
 
+@pytest.mark.parametrize("name,B,V", [("b64_g5_v128256", 64, 128256), ("pointmass_b64_g5_v128256", 9, 5000),
+                                      ("b1_g4_v1024_f32", 3, 777)])
+def test_host_buffer_form_matches_device_form(name, B, V):
+    # spec_verify_host copies page-locked host inputs into staging buffers, runs the step and copies the
+    # outputs back: the same tokens and counts as spec_verify_ex on device inputs, and oracle parity
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    b = synth.make_batch(name, B=B, V=V)
+    d = parity.to_device(b)
+    host = {k: (None if v is None else v.cpu().pin_memory()) for k, v in d.items()}
+    staging = {k: (None if v is None else torch.empty_like(v)) for k, v in d.items()}
+    mg = int(b.gammas.max())
+    call = sv.Call(b.B, b.V, mg, b.R_t, b.R_d)
+    out_t = torch.full((b.R_t,), -9, dtype=torch.int32).pin_memory()
+    out_n = torch.full((b.B,), -9, dtype=torch.int32).pin_memory()
+    rc = call.run_host(host["target"], host["draft"], host["draft_tokens"], host["seq_offsets"], host["gammas"],
+                       b.temperature, 31, 2, out_t, out_n, staging)
+    assert rc == sv.SV_OK, sv.spec_verify_status_string(rc)
+    torch.cuda.synchronize()
+    assert call.status_bits() == 0
+    g = parity.run_gpu(b, 31, 2, dev_in=d, debug=False)
+    assert np.array_equal(out_t.numpy(), g["tokens"]) and np.array_equal(out_n.numpy(), g["n"])
+    parity.assert_parity(b, 31, 2, g=g, check_debug=False)
+
+
 def test_gamma_zero_and_max_gamma():
     b = synth.make_batch("ragged_b128_v129280", B=6, V=3000, gammas=[0, 31, 1, 0, 7, 31])
     for step in range(3):
