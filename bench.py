@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -44,12 +45,23 @@ def peaks():
     return 6800.0, "fallback"
 
 
+_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def code_only(src: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed (string literals kept)."""
+    src = _TOKENS.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources' code (comments and layout excluded), keying profiled figures to the
+    code they were measured on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_35_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(f.encode() + b"\0" + code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -4,7 +4,7 @@
 // Sources: Philox4x32-10 follows Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
 // 1, 2, 3" (SC'11). The float-float operations are the classic error-free transformations (Knuth's
 // TwoSum, Dekker's product via fused multiply-add). The exponential is Tang's table method:
-// 2^t = 2^n * 2^(j/64) * e^y with |y| <= ln(2)/128, the table built on the host from exp2() in
+// 2^t = 2^n * 2^(j/128) * e^y with |y| <= ln(2)/256, the table built on the host from exp2() in
 // double and the remainder by its Taylor series (written from the series, no library constants).
 #pragma once
 #include <cstdint>

@@ -13,11 +13,12 @@
 //     by a 1-D bulk copy into a shared-memory ring (two stages per streamer, evict-first in L2), and
 //     the warp reduces it to the raw max and the fp32 sum of 2^((l - max) K) (greedy: first argmax).
 //     One 64-bit partial word per task. This pass moves all the algorithmic HBM traffic.
-//   decision (one warp per sequence, the lower warps of the CTAs by static slot): polls the sequence's
-//     partial words, merges each row (fp32 online rescaling), evaluates u q(x) < p(x) for every slot with
-//     a float-float exponential of the exact logit gap, takes the first rejection with a ballot, writes
-//     the accepted tokens and publishes the draw (mode, slot, row maxima, approximate normaliser ratio,
-//     uniform) as self-validating task words.
+//   decision (bulk-copy path with no more sequences than CTAs: CTA b's four non-streaming warps share
+//     sequence b's rows, warp 0 finishing; otherwise one warp per sequence, the lower warps of the CTAs
+//     by static slot): polls the sequence's partial words, merges each row (fp32 online rescaling),
+//     evaluates u q(x) < p(x) for every slot with a float-float exponential of the exact logit gap,
+//     takes the first rejection with a ballot, writes the accepted tokens and publishes the draw (mode,
+//     slot, row maxima, approximate normaliser ratio, uniform) as self-validating task words.
 //   sampler task (sequence b, 1024 columns), claimed from a counter in sequence-major order by any free
 //     warp: the draw's weights max(0, p - q) (or p for a bonus) in float-float precision, stored as four
 //     per-task sums and per-128-column group sums.
