@@ -160,7 +160,9 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload},
+            "data": "synthetic",
+            "config": {"workload": args.workload, "B": w.B, "gamma": int(w.gamma) if w.gamma else "U{1..8}",
+                       "V": w.V, "temperature": w.temperature, "sample_B": sample_b},
             "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
