@@ -37,7 +37,11 @@
  * any logit row is read: every out_num_accepted is -1 and out_tokens is not written. A draft token
  * outside [0, V), a NaN or +inf logit, or a row whose logits are all -inf (-inf entries are
  * otherwise allowed and mean p = 0) fail only their sequence: its out_num_accepted is -1 and its
- * out_tokens slots are -1. No device check traps.
+ * out_tokens slots are -1. No device check traps. Every wait of one warp on another within the launch
+ * is bounded: a wait that gives up sets SV_ERR_TIMEOUT and fails the sequence it waited for in the
+ * same way (n = -1, tokens -1; with the fused update its history and length are left unchanged and
+ * its next token is -1). A sampled sequence's outputs have one writer, chosen by an atomic claim, so
+ * a failed sequence's outputs are never overwritten by a late writer.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
@@ -75,6 +79,13 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  *   p_x, q_x   double[R_d]: p_i(x_i) and q_i(x_i) of every draft slot (sampling mode only).
  *   seq_mass   double[B]: total weight S of the sequence's draw relative to p (1 - beta at a
  *              rejected slot; about 1 for a bonus draw) (sampling mode only).
+ *   beta       double[R_d]: beta_i = sum_x min(p_i(x), q_i(x)) of every draft slot, the acceptance
+ *              probability of slot i when x_i is drawn from q_i (velog "6-1편. Speculative Decoding",
+ *              §2-3); p_i(x_i) for a point-mass draft (sampling mode only). Computed by a second kernel
+ *              enqueued after the step, from the logits.
+ *   spin_limit polls after which a wait of one warp on another warp's word gives up (SV_ERR_TIMEOUT);
+ *              0 keeps the library's bound (about a second). A small value exists to exercise the
+ *              time-out path in tests: a sequence whose wait gave up reports n = -1 and tokens -1.
  */
 typedef struct {
     double* row_lse;
@@ -82,6 +93,8 @@ typedef struct {
     double* p_x;
     double* q_x;
     double* seq_mass;
+    double* beta;
+    uint32_t spin_limit;
 } sv_debug;
 
 /*
@@ -186,7 +199,8 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_
  *   (the n accepted drafts and the drawn token are appended; the drawn token is the next step's input
  *   token, at position lengths[b] - 1).
  *   A sequence with n < 0 (it failed verification) is left unchanged and gets next_tokens[b] = -1.
- *   A sequence with n > seq_offsets[b+1] - seq_offsets[b] (inconsistent outputs) or with L < 0 or
+ *   A sequence with n > seq_offsets[b+1] - seq_offsets[b] or n > SV_MAX_GAMMA (outputs no verify call
+ *   writes) or with L < 0 or
  *   L + n + 1 > capacity is left unchanged, gets next_tokens[b] = -1, and sets bit
  *   (1u << SV_ERR_BAD_OFFSETS) or (1u << SV_ERR_CAPACITY) of *device_status (if not NULL).
  *

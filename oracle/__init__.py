@@ -44,7 +44,7 @@ def build(force: bool = False) -> str:
 class _Debug(ctypes.Structure):
     _fields_ = [("row_lse", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p),
                 ("p_x", ctypes.c_void_p), ("q_x", ctypes.c_void_p),
-                ("seq_mass", ctypes.c_void_p), ("seq_fallback", ctypes.c_void_p)]
+                ("seq_mass", ctypes.c_void_p), ("seq_fallback", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
 
 
 def lib():
@@ -66,6 +66,12 @@ def lib():
                                         ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.POINTER(_Debug), ctypes.c_int]
             L.oracle_verify.restype = ctypes.c_uint32
+            L.oracle_verify_steps.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                              ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            L.oracle_verify_steps.restype = ctypes.c_uint32
             L.oracle_draw_bracket.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                               ctypes.c_int32, ctypes.c_double, ctypes.c_double,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
@@ -129,6 +135,7 @@ class Result:
         self.q_x = np.full(R_d, np.nan)
         self.seq_mass = np.full(B, np.nan)
         self.seq_fallback = np.zeros(B, dtype=np.int32)
+        self.beta = np.full(R_d, np.nan)
         self.status = 0
 
 
@@ -155,7 +162,7 @@ def verify(target, draft, draft_tokens, seq_offsets, gammas, V, temperature, see
     R_t = R_d + B
     res = Result(B, R_t, R_d)
     dbg = _Debug(_ptr(res.row_lse), _ptr(res.row_argmax), _ptr(res.p_x), _ptr(res.q_x),
-                 _ptr(res.seq_mass), _ptr(res.seq_fallback))
+                 _ptr(res.seq_mass), _ptr(res.seq_fallback), _ptr(res.beta))
     if nthreads is None:
         nthreads = len(os.sched_getaffinity(0))
     res.status = lib().oracle_verify(_ptr(target), _ptr(draft), dtype, _ptr(tok), _ptr(offs),
@@ -163,6 +170,32 @@ def verify(target, draft, draft_tokens, seq_offsets, gammas, V, temperature, see
                                      _ptr(res.tokens), _ptr(res.num_accepted), ctypes.byref(dbg),
                                      int(nthreads))
     return res
+
+
+def verify_steps(target, draft, draft_tokens, seq_offsets, gammas, V, temperature, seed, step0, nsteps,
+                 nthreads: int | None = None):
+    """``verify`` for steps step0 .. step0 + nsteps - 1 of one batch (temperature > 0), each sequence's
+    probabilities computed once (see ``oracle_verify_steps``). Returns (tokens [nsteps, R_t],
+    num_accepted [nsteps, B], status)."""
+    target = np.ascontiguousarray(target)
+    dtype = BF16 if target.dtype == np.uint16 else F32
+    if dtype == F32:
+        target = target.astype(np.float32, copy=False)
+    if draft is not None:
+        draft = np.ascontiguousarray(draft).astype(np.uint16 if dtype == BF16 else np.float32, copy=False)
+    offs = np.ascontiguousarray(seq_offsets, dtype=np.int32)
+    gam = np.ascontiguousarray(gammas, dtype=np.int32)
+    tok = None if draft_tokens is None else np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    B = len(gam)
+    R_t = (int(offs[-1]) if B else 0) + B
+    out_t = np.full((nsteps, R_t), -7, dtype=np.int32)
+    out_n = np.full((nsteps, B), -7, dtype=np.int32)
+    if nthreads is None:
+        nthreads = len(os.sched_getaffinity(0))
+    st = lib().oracle_verify_steps(_ptr(target), _ptr(draft), dtype, _ptr(tok), _ptr(offs), _ptr(gam), B, V,
+                                   float(temperature), seed, step0, int(nsteps), _ptr(out_t), _ptr(out_n),
+                                   int(nthreads))
+    return out_t, out_n, int(st)
 
 
 def draw_bracket(trow, drow, V, temperature, u, k_query, x_excl=-1):

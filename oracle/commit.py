@@ -6,7 +6,8 @@ length. Plainest reading, written out: for each sequence with n >= 0 accepted dr
 emitted tokens (the accepted drafts and the drawn token, slots 0..n of the verify output) are appended
 to its token history at its current length, the length grows by n + 1, and the drawn token becomes the
 next input token. Failed sequences (n < 0) are left as they are, with next token -1; so is a sequence
-whose outputs are inconsistent (n above its gamma) or whose history would overflow, which is flagged.
+whose outputs are inconsistent (n above its gamma, or above 31, the largest gamma a verify call takes)
+or whose history would overflow, which is flagged.
 Plain Python loops: the function is the definition, nothing more.
 """
 from __future__ import annotations
@@ -14,6 +15,7 @@ from __future__ import annotations
 import numpy as np
 
 SV_ERR_BAD_OFFSETS, SV_ERR_CAPACITY = 4, 9
+MAX_GAMMA = 31  # a verify call takes gamma_b <= 31, so it never reports n above 31
 
 
 def commit(out_tokens, out_num_accepted, seq_offsets, history, capacity, lengths):
@@ -32,7 +34,7 @@ def commit(out_tokens, out_num_accepted, seq_offsets, history, capacity, lengths
         if n < 0:
             continue
         gamma = offs[b + 1] - offs[b]
-        if n > gamma or offs[b] < 0:
+        if n > gamma or n > MAX_GAMMA or offs[b] < 0:
             status |= 1 << SV_ERR_BAD_OFFSETS
             continue
         L = lens[b]

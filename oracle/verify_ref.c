@@ -223,6 +223,7 @@ typedef struct {
     double* q_x;          /* [R_d] q_i(x_i) of every draft slot */
     double* seq_mass;     /* [B] normaliser S of the sequence's draw */
     int32_t* seq_fallback;/* [B] 1 where the S == 0 fallback was taken */
+    double* beta;         /* [R_d] beta_i = sum_x min(p_i(x), q_i(x)) of every draft slot ([velog] §2-3) */
 } oracle_debug;
 
 typedef struct {
@@ -239,13 +240,18 @@ typedef struct {
     int32_t* out_n;
     oracle_debug* dbg;
     int32_t b0, b1;
+    int32_t nsteps;   /* sampling mode: draws for steps step .. step + nsteps - 1 (outputs step-major) */
     uint32_t status;
 } job_t;
 
 static void fail_seq(job_t* J, int32_t b, int code) {
     const int32_t d0 = J->off[b], g = J->gam[b];
-    for (int32_t j = 0; j <= g; ++j) J->out_tok[d0 + b + j] = -1;
-    J->out_n[b] = -1;
+    const size_t R_t = (size_t)J->off[J->B] + (size_t)J->B;
+    const int32_t ns = J->T == 0.0 ? 1 : J->nsteps;
+    for (int32_t s = 0; s < ns; ++s) {
+        for (int32_t j = 0; j <= g; ++j) J->out_tok[(size_t)s * R_t + (size_t)(d0 + b + j)] = -1;
+        J->out_n[(size_t)s * (size_t)J->B + b] = -1;
+    }
     J->status |= 1u << code;
 }
 
@@ -290,22 +296,38 @@ static void verify_one(job_t* J, int32_t b, double* prow, double* qrow, double* 
             qi[x[i]] = 1.0;
             if (J->dbg && J->dbg->p_x) J->dbg->p_x[d0 + i] = prow[(size_t)i * V + x[i]];
             if (J->dbg && J->dbg->q_x) J->dbg->q_x[d0 + i] = 1.0;
+            if (J->dbg && J->dbg->beta) J->dbg->beta[d0 + i] = prow[(size_t)i * V + x[i]]; /* min(p, 1{x}) */
         } else if (i < g) {
             e = row_softmax(J->draft, J->dtype, (size_t)(d0 + i), V, J->T, qrow + (size_t)i * V, &lse);
             if (e) { fail_seq(J, b, e); return; }
             if (J->dbg && J->dbg->row_lse) J->dbg->row_lse[R_t + d0 + i] = lse;
             if (J->dbg && J->dbg->p_x) J->dbg->p_x[d0 + i] = prow[(size_t)i * V + x[i]];
             if (J->dbg && J->dbg->q_x) J->dbg->q_x[d0 + i] = qrow[(size_t)i * V + x[i]];
+            if (J->dbg && J->dbg->beta) { /* [velog] §2-3: beta = sum_x min(p(x), q(x)) */
+                const double* pi = prow + (size_t)i * V;
+                const double* qi = qrow + (size_t)i * V;
+                double bsum = 0.0;
+                for (int32_t k = 0; k < V; ++k) bsum += pi[k] < qi[k] ? pi[k] : qi[k];
+                J->dbg->beta[d0 + i] = bsum;
+            }
         }
-        u_acc[i] = oracle_uniform(J->seed, J->step, (uint32_t)b, (uint32_t)i, 0);
-        u_smp[i] = oracle_uniform(J->seed, J->step, (uint32_t)b, (uint32_t)i, 1);
     }
-    double S = 0.0;
-    int32_t fb = 0;
-    const int32_t n = oracle_verify_probs(prow, qrow, x, g, V, u_acc, u_smp, J->out_tok + t0, &S, &fb);
-    J->out_n[b] = n;
-    if (J->dbg && J->dbg->seq_mass) J->dbg->seq_mass[b] = S;
-    if (J->dbg && J->dbg->seq_fallback) J->dbg->seq_fallback[b] = fb;
+    /* the draws of this step and of every further step the job asks for: the same rule on the same
+       probabilities, with the uniforms of step + s (multi-step verification of one batch) */
+    for (int32_t s = 0; s < J->nsteps; ++s) {
+        const uint64_t step = J->step + (uint64_t)s;
+        for (int32_t i = 0; i <= g; ++i) {
+            u_acc[i] = oracle_uniform(J->seed, step, (uint32_t)b, (uint32_t)i, 0);
+            u_smp[i] = oracle_uniform(J->seed, step, (uint32_t)b, (uint32_t)i, 1);
+        }
+        double S = 0.0;
+        int32_t fb = 0;
+        int32_t* out_tok = J->out_tok + (size_t)s * (size_t)R_t;
+        const int32_t n = oracle_verify_probs(prow, qrow, x, g, V, u_acc, u_smp, out_tok + t0, &S, &fb);
+        J->out_n[(size_t)s * (size_t)J->B + b] = n;
+        if (s == 0 && J->dbg && J->dbg->seq_mass) J->dbg->seq_mass[b] = S;
+        if (s == 0 && J->dbg && J->dbg->seq_fallback) J->dbg->seq_fallback[b] = fb;
+    }
 }
 
 static void* run_job(void* arg) {
@@ -329,12 +351,12 @@ static void* run_job(void* arg) {
  * a failed sequence gets n = -1 and tokens -1. Batch-level argument errors return
  * 1 << OR_ERR_INVALID_ARG or 1 << OR_ERR_BAD_OFFSETS without touching the outputs.
  */
-uint32_t oracle_verify(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
-                       const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V,
-                       double temperature, uint64_t seed, uint64_t step, int32_t* out_tokens,
-                       int32_t* out_num_accepted, oracle_debug* dbg, int nthreads) {
+static uint32_t verify_batch(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                             const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V,
+                             double temperature, uint64_t seed, uint64_t step, int32_t nsteps,
+                             int32_t* out_tokens, int32_t* out_num_accepted, oracle_debug* dbg, int nthreads) {
     if (B < 0 || V <= 0 || !(temperature >= 0.0) || isinf(temperature) || !target || !seq_offsets ||
-        !gammas || !out_tokens || !out_num_accepted)
+        !gammas || !out_tokens || !out_num_accepted || nsteps < 1)
         return 1u << OR_ERR_INVALID_ARG;
     if (seq_offsets[0] != 0) return 1u << OR_ERR_BAD_OFFSETS;
     for (int32_t b = 0; b < B; ++b)
@@ -352,6 +374,7 @@ uint32_t oracle_verify(const void* target, const void* draft, int dtype, const i
         J->off = seq_offsets; J->gam = gammas; J->B = B; J->V = V; J->T = temperature;
         J->seed = seed; J->step = step; J->out_tok = out_tokens; J->out_n = out_num_accepted;
         J->dbg = dbg;
+        J->nsteps = nsteps;
         J->b0 = (int32_t)((int64_t)B * t / nthreads);
         J->b1 = (int32_t)((int64_t)B * (t + 1) / nthreads);
     }
@@ -364,6 +387,29 @@ uint32_t oracle_verify(const void* target, const void* draft, int dtype, const i
     }
     free(jobs); free(th);
     return st;
+}
+
+uint32_t oracle_verify(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                       const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V,
+                       double temperature, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                       int32_t* out_num_accepted, oracle_debug* dbg, int nthreads) {
+    return verify_batch(target, draft, dtype, draft_tokens, seq_offsets, gammas, B, V, temperature, seed, step,
+                        1, out_tokens, out_num_accepted, dbg, nthreads);
+}
+
+/*
+ * oracle_verify for steps step .. step + nsteps - 1 of one batch (sampling mode, temperature > 0): the
+ * same rule on the same probabilities, each sequence's softmaxes computed once and its draws made with
+ * every step's uniforms. out_tokens [nsteps][R_t] and out_num_accepted [nsteps][B], step-major; debug
+ * values of the first step only. Identical to nsteps calls of oracle_verify.
+ */
+uint32_t oracle_verify_steps(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                             const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V,
+                             double temperature, uint64_t seed, uint64_t step, int32_t nsteps,
+                             int32_t* out_tokens, int32_t* out_num_accepted, int nthreads) {
+    if (!(temperature > 0.0)) return 1u << OR_ERR_INVALID_ARG;
+    return verify_batch(target, draft, dtype, draft_tokens, seq_offsets, gammas, B, V, temperature, seed, step,
+                        nsteps, out_tokens, out_num_accepted, NULL, nthreads);
 }
 
 /*

@@ -108,6 +108,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.out_n = out_num_accepted;
     P.status = device_status ? device_status : (uint32_t*)(ws + L.status);
     if (debug) P.dbg = *debug;
+    P.spin = debug && debug->spin_limit ? debug->spin_limit : kSpinLimit;
     for (int j = 0; j < 128; ++j) {  // Tang's table: 2^(j/128) as a float pair (hi, lo)
         const double v = std::exp2((double)j / 128.0);
         const float hi = (float)v;
@@ -118,6 +119,8 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.recw = (Word*)(ws + L.recw);
     P.groupw = (Word*)(ws + L.groupw);
     P.remw = (Word*)(ws + L.remw);
+    P.pathw = (Word*)(ws + L.pathw);
+    P.seqstate = (uint32_t*)(ws + L.seqstate);
     P.ctr = (Counters*)(ws + L.counters);
     P.parents = parents;
     P.out_path = out_path;

@@ -23,7 +23,9 @@ __global__ void __launch_bounds__(256) k_commit(const int32_t* __restrict__ out_
         const int32_t o0 = offs[b], g = offs[b + 1] - o0;
         const int32_t L = lengths[b];
         uint32_t err = 0;
-        if (n >= 0 && (n > g || o0 < 0)) err = 1u << SV_ERR_BAD_OFFSETS;
+        // n above the sequence's gap, or above the largest gamma a verify call writes (lanes 0..31 copy
+        // the slots), means the outputs are not a verify call's: nothing is appended
+        if (n >= 0 && (n > g || n > SV_MAX_GAMMA || o0 < 0)) err = 1u << SV_ERR_BAD_OFFSETS;
         else if (n >= 0 && (L < 0 || (int64_t)L + n + 1 > capacity)) err = 1u << SV_ERR_CAPACITY;
         if (n < 0 || err) {
             if (lane == 0) {

@@ -30,6 +30,7 @@ constexpr int kRowCache = 2048;             // sampling batches with up to this 
 // kModeResidualSet: a token-tree node whose candidates were all rejected: p with their tokens removed.
 enum : int32_t { kModeNone = 0, kModeResidual = 1, kModeBonus = 2, kModeResidualPM = 3, kModeResidualSet = 4 };
 constexpr int kMaxRemoved = 32;  // removed-token words per sequence (a node has at most 31 children)
+constexpr uint32_t kSpinLimit = 1u << 21;  // polls before a wait gives up (about 1 s with back-off)
 
 // Data handed between warps of one launch is written as 64-bit words, each exactly once per call with
 // one relaxed store, into a region zeroed before the call, and each non-zero once written. A reader
@@ -90,6 +91,8 @@ struct Params {
     unsigned long long nS_recip;  // floor(2^64 / nS) + 1 (nS >= 2): c / nS = high 64 bits of c * nS_recip
     float K_hi, K_lo;  // log2(e) / T as float-float
     float d_min;       // clamp of l - m in the precise exponential (about -126.5 / K)
+    uint32_t spin;     // polls before a wait on another warp's word gives up (kSpinLimit unless a caller
+                       // testing the time-out path asks for fewer)
     double invT64;     // 1 / T (debug output of the row log-normalisers only)
     uint64_t seed, step;
     int32_t* out_tokens;
@@ -102,6 +105,9 @@ struct Params {
     Word* recw;             // [B * nS * kRecWords]
     Word* groupw;           // [B * nS * kGroups * kGroupWords]
     Word* remw;             // [B * kMaxRemoved] removed tokens of a tree draw: 0x80000000 << 32 | token
+    Word* pathw;            // [B * kMaxRemoved] accepted path of a sampled tree: (0x80000000 | node) << 32 | token
+    uint32_t* seqstate;     // [B] who writes a sampled sequence's outputs: 0 open, 1 its find, 2 failed (a wait
+                            // on the sequence gave up); claimed by compare-and-swap
     const int32_t* parents; // token trees: parent node of each non-root node (nullptr: linear drafts)
     int32_t* out_path;      // token trees: the accepted nodes (nullable)
     Counters* ctr;
@@ -114,7 +120,7 @@ struct Params {
 };
 
 struct Layout {
-    size_t counters, partials, taskw, recw, groupw, remw, status;
+    size_t counters, partials, taskw, recw, groupw, remw, pathw, seqstate, status;
     size_t zero_begin, zero_end;  // byte range the launch sequence clears
     size_t total;
 };

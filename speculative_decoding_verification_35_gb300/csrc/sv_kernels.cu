@@ -45,8 +45,6 @@
 
 namespace sv {
 
-constexpr uint32_t kSpinLimit = 1u << 21;  // polls before a wait gives up (about 1 s with back-off)
-
 // ------------------------------------------------------------------------------------------------
 // Words handed between warps during the launch (never read through L1's non-coherent path)
 // ------------------------------------------------------------------------------------------------
@@ -375,11 +373,12 @@ __device__ __forceinline__ SegStats seg_stats(const char* rowp, int len, int lan
 // ------------------------------------------------------------------------------------------------
 // Fused post-verify update (spec_verify_fused; "Accelerating Sonar through speculation",
 // §"MTP scheduling"): run by the one warp that writes a sequence's final token, after writing it. It
-// appends the n accepted drafts and the drawn token to the sequence's history at its length, advances
-// the length and writes the next input token; a failed sequence (n < 0) gets next token -1, and one
-// whose history would overflow is left as it is with next token -1 and SV_ERR_CAPACITY.
+// appends the n accepted drafts (acc, lane j < n holding slot j's) and the drawn token to the sequence's
+// history at its length, advances the length and writes the next input token; a failed sequence (n < 0)
+// gets next token -1, and one whose history would overflow is left as it is with next token -1 and
+// SV_ERR_CAPACITY.
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ void commit_seq(const Params& P, int32_t b, int32_t n, int32_t o0, int32_t drawn, int lane) {
+__device__ __forceinline__ void commit_seq(const Params& P, int32_t b, int32_t n, int32_t acc, int32_t drawn, int lane) {
     if (!P.hist) return;
     const int32_t L = n >= 0 ? P.lens[b] : 0;
     if (n < 0 || L < 0 || (int64_t)L + n + 1 > P.cap) {
@@ -390,12 +389,40 @@ __device__ __forceinline__ void commit_seq(const Params& P, int32_t b, int32_t n
         return;
     }
     int32_t* h = P.hist + (size_t)b * (size_t)P.cap + (size_t)L;
-    if (lane < n) h[lane] = __ldg(P.tokens + o0 + lane);  // the accepted drafts
+    if (lane < n) h[lane] = acc;  // the accepted drafts
     if (lane == n) h[n] = drawn;
     if (lane == 0) {
         P.lens[b] = L + n + 1;
         P.next[b] = drawn;
     }
+}
+
+// Outputs of a failed sequence: n = -1, every slot -1, no accepted path; with the fused update, next
+// token -1 and the history and length untouched.
+__device__ __noinline__ void fail_outputs(const Params& P, int32_t b, int lane) {
+    const int32_t o0 = __ldg(P.offs + b), g = __ldg(P.offs + b + 1) - o0;  // validated by every CTA
+    for (int32_t j = lane; j <= g; j += 32) P.out_tokens[o0 + b + j] = -1;
+    if (P.out_path)
+        for (int32_t j = lane; j < g; j += 32) P.out_path[o0 + j] = -1;
+    if (lane == 0) {
+        P.out_n[b] = -1;
+        if (P.hist) P.next[b] = -1;
+    }
+}
+
+// A sampled sequence's outputs have one writer: its find, or a warp whose wait on the sequence gave up.
+// Each claims the sequence's state word (0 -> 1 for the find, 0 -> 2 for a failure); the loser writes
+// nothing. Returns the word's previous value, on every lane.
+__device__ __forceinline__ uint32_t claim_seq(const Params& P, int32_t b, uint32_t who, int lane) {
+    uint32_t old = 0;
+    if (lane == 0) old = atomicCAS(P.seqstate + b, 0u, who);
+    return __shfl_sync(0xFFFFFFFFu, old, 0);
+}
+
+// A wait on sequence b's words gave up (SV_ERR_TIMEOUT already set): fail the sequence unless its find
+// holds it (the find then fails it itself, when its own wait on the missing words gives up).
+__device__ __noinline__ void give_up_seq(const Params& P, int32_t b, int lane) {
+    if (claim_seq(P, b, 2u, lane) == 0u) fail_outputs(P, b, lane);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -425,7 +452,7 @@ __device__ __forceinline__ bool get_task(const Params& P, int32_t b, int lane, T
     Word v = lane < 3 ? ld_word(w + lane) : 1ull;
     uint32_t spins = 0, ns = 32;
     while (__any_sync(0xFFFFFFFFu, v == 0)) {
-        if (++spins > kSpinLimit) {
+        if (++spins > P.spin) {
             if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
             return false;
         }
@@ -467,7 +494,7 @@ __device__ __forceinline__ bool removed_tokens(const Params& P, int32_t b, const
     Word v = lane < tk.nrm ? ld_word(w + lane) : (Word)kWordMark << 32;
     uint32_t spins = 0, ns = 32;
     while (__any_sync(0xFFFFFFFFu, v == 0)) {
-        if (++spins > kSpinLimit) {
+        if (++spins > P.spin) {
             if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
             return false;
         }
@@ -523,7 +550,6 @@ __device__ __noinline__ void tree_greedy(const Params& P, int32_t b, int32_t g, 
 // px: p_par(x) of slot `lane`; m_row: the raw maximum of row `lane`.
 __device__ __noinline__ void tree_sampled(const Params& P, int32_t b, int32_t g, int32_t o0, int32_t x, int32_t par,
                                           float px, float u_acc, float u_draw, float m_row, int lane) {
-    const int32_t t0 = o0 + b;
     int cur = 0, n = 0, mytok = -1, mynode = -1;
     uint32_t removed = 0;  // slots holding the tokens the final draw removes
     while (true) {
@@ -551,8 +577,8 @@ __device__ __noinline__ void tree_sampled(const Params& P, int32_t b, int32_t g,
         ++n;
         cur = c + 1;
     }
-    if (lane <= g && lane != n) P.out_tokens[t0 + lane] = lane < n ? mytok : -1;
-    if (P.out_path && lane < g) P.out_path[o0 + lane] = lane < n ? mynode : -1;
+    // the accepted path, for the find (the sequence's one output writer)
+    if (lane < n) st_word(P.pathw + (size_t)b * kMaxRemoved + lane, pack_words(kWordMark | (uint32_t)mynode, (uint32_t)mytok));
     const int nrm = __popc(removed);
     if ((removed >> lane) & 1u)
         st_word(P.remw + (size_t)b * kMaxRemoved + __popc(removed & ((1u << lane) - 1u)),
@@ -560,7 +586,6 @@ __device__ __noinline__ void tree_sampled(const Params& P, int32_t b, int32_t g,
     const float pm = __shfl_sync(0xFFFFFFFFu, m_row, cur);
     const float un = __shfl_sync(0xFFFFFFFFu, u_draw, cur);
     put_task(P, b, lane, nrm ? kModeResidualSet : kModeBonus, cur, pm, 0.f, nrm ? __int_as_float(nrm) : 1.f, un, n);
-    if (lane == 0) P.out_n[b] = n;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -649,7 +674,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
             uint32_t spins = 0, ns = 64;
             while (__any_sync(0xFFFFFFFFu, q[0] == 0 || q[1] == 0 || q[2] == 0 || q[3] == 0 || q[4] == 0 ||
                                                q[5] == 0 || q[6] == 0 || q[7] == 0)) {
-                if (++spins > kSpinLimit) {
+                if (++spins > P.spin) {
                     if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
                     err |= 1u << SV_ERR_TIMEOUT;
                     break;
@@ -760,7 +785,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         if (!GREEDY) put_task(P, b, lane, kModeNone, 0, 0.f, 0.f, 1.f, 0.f, 0);
         for (int32_t j = lane; j <= g; j += 32) P.out_tokens[t0 + j] = -1;
         if (P.out_path && lane < g) P.out_path[o0 + lane] = -1;
-        commit_seq(P, b, -1, o0, -1, lane);
+        commit_seq(P, b, -1, -1, -1, lane);
         return;
     }
     if (GREEDY) {
@@ -774,7 +799,7 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         const int n = mism ? __ffs(mism) - 1 : g;
         if (lane <= g) P.out_tokens[t0 + lane] = lane < n ? x : (lane == n ? a : -1);
         if (lane == 0) P.out_n[b] = n;
-        commit_seq(P, b, n, o0, __shfl_sync(0xFFFFFFFFu, a, n), lane);
+        commit_seq(P, b, n, x, __shfl_sync(0xFFFFFFFFu, a, n), lane);
         return;
     }
     // the draft row of slot `lane` is statistics row g + 1 + lane: lane (g+1+lane) & 31, register >> 5
@@ -813,9 +838,9 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         tree_sampled(P, b, g, o0, x, par, px, u_acc, u_draw, my_m0, lane);
         return;
     }
+    // the sequence's outputs are written by its find, once the draw is known (one writer per sequence)
     const uint32_t rej = __ballot_sync(0xFFFFFFFFu, lane < g && !acc);
     const int n = rej ? __ffs(rej) - 1 : g;
-    if (lane <= g && lane != n) P.out_tokens[t0 + lane] = lane < n ? x : -1;
     // statistics of the emitting slot's rows
     const float pm = __shfl_sync(0xFFFFFFFFu, my_m0, n), ps = __shfl_sync(0xFFFFFFFFu, my_s0, n);
     const float qm = __shfl_sync(0xFFFFFFFFu, dm, n), qs = __shfl_sync(0xFFFFFFFFu, ds, n);
@@ -827,7 +852,6 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     else
         put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, pm, n < g ? qm : 0.f,
                  n < g ? div_fma(ps, qs) : 1.f, un, n);
-    if (lane == 0) P.out_n[b] = n;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1008,7 +1032,7 @@ __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int uni
     Word wa = lane < kGroups ? ld_word(gw) : (Word)kWordMark, wb = lane < kGroups ? ld_word(gw + 1) : (Word)kWordMark;
     uint32_t spins = 0, ns = 32;
     while (__any_sync(0xFFFFFFFFu, wa == 0 || wb == 0)) {
-        if (++spins > kSpinLimit) {
+        if (++spins > P.spin) {
             if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
             return -2;
         }
@@ -1073,7 +1097,31 @@ __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int uni
 // the records' weights, then the crossing column inside that task.
 template <int DT, bool VEC>
 __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk, size_t prow, size_t qrow,
-                                  int32_t out_pos, const float* tab, int lane) {
+                                  int32_t o0, const float* tab, int lane) {
+    // the sequence's outputs are this warp's to write, unless a wait on the sequence gave up first
+    if (claim_seq(P, b, 1u, lane) != 0u) return;
+    // the accepted tokens (slot j on lane j < npos): the draft tokens, or a tree's accepted path (written
+    // by the decision before the draw)
+    int32_t acc_tok = -1, acc_node = -1;
+    if (!P.parents) {
+        if (lane < tk.npos) acc_tok = __ldg(P.tokens + o0 + lane);
+    } else {
+        const Word* pw = P.pathw + (size_t)b * kMaxRemoved + lane;
+        Word v = lane < tk.npos ? ld_word(pw) : (Word)kWordMark << 32;
+        uint32_t spins = 0, ns = 32;
+        while (__any_sync(0xFFFFFFFFu, v == 0)) {
+            if (++spins > P.spin) {
+                if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+                fail_outputs(P, b, lane);
+                return;
+            }
+            __nanosleep(ns);
+            ns = ns < 256 ? 2 * ns : 256;
+            if (v == 0) v = ld_word(pw);
+        }
+        acc_node = (int32_t)((uint32_t)(v >> 32) & 0x7FFFFFFFu);
+        acc_tok = (int32_t)(uint32_t)v;
+    }
     const int nS = P.nS;
     const Word* rec = P.recw + (size_t)b * nS * kRecWords;
     // lane owns the run of tasks [s0, s1), read four tasks (16 words) at a time
@@ -1097,7 +1145,7 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
 #pragma unroll
                 for (int j = 0; j < kRecWords; ++j) missing |= w[k][j] == 0;
             if (!__any_sync(0xFFFFFFFFu, missing)) break;
-            if (++spins > kSpinLimit) {
+            if (++spins > P.spin) {
                 if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
                 return false;
             }
@@ -1131,13 +1179,13 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
     ff ka[4], kb[4];  // the lane's first four tasks, kept for the crossing search
     const int nchunk = (per + 3) / 4;  // the same on every lane
     if (!__all_sync(0xFFFFFFFFu, poll4(s0, lp, lq, la, lb, ka, kb))) {
-        commit_seq(P, b, -1, 0, -1, lane);  // timed out (reported in the status word)
+        fail_outputs(P, b, lane);  // timed out (reported in the status word)
         return;
     }
     for (int q = 1; q < nchunk; ++q) {
         ff va[4], vb[4];
         if (!__all_sync(0xFFFFFFFFu, poll4(s0 + 4 * q, lp, lq, la, lb, va, vb))) {
-            commit_seq(P, b, -1, 0, -1, lane);
+            fail_outputs(P, b, lane);
             return;
         }
     }
@@ -1229,13 +1277,20 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
             token = scan_elements<DT, VEC>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule, rtok,
                                            by_p ? 0 : tk.nrm, tab, lane);
         }
-        if (token == -2) token = -1;  // time-out (reported in the status word)
     }
+    if (token < 0) {  // a time-out (reported in the status word)
+        fail_outputs(P, b, lane);
+        return;
+    }
+    // every output of the sequence: the accepted tokens, the drawn one, -1 after it
+    const int32_t g = __ldg(P.offs + b + 1) - o0, npos = tk.npos;
+    if (lane <= g) P.out_tokens[o0 + b + lane] = lane < npos ? acc_tok : (lane == npos ? token : -1);
+    if (P.out_path && lane < g) P.out_path[o0 + lane] = lane < npos ? acc_node : -1;
     if (lane == 0) {
-        P.out_tokens[out_pos] = token;
+        P.out_n[b] = npos;
         if (P.dbg.seq_mass) P.dbg.seq_mass[b] = ((double)S.hi + (double)S.lo) / ((double)sp.hi + (double)sp.lo);
     }
-    commit_seq(P, b, token >= 0 ? tk.npos : -1, out_pos - b - tk.npos, token, lane);
+    commit_seq(P, b, npos, acc_tok, token, lane);
 }
 
 // 8 consecutive columns k0 .. k0 + 7 of `row`, packed (bf16: 4 words; fp32: 8 words); -inf past V.
@@ -1414,14 +1469,21 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
     const int i = (int)(c - (uint32_t)b * (uint32_t)P.nS);
     const int32_t o0 = __ldg(P.offs + b);
     TaskInfo tk;
-    if (!get_task(P, b, lane, tk) || tk.mode == kModeNone) return;
+    if (!get_task(P, b, lane, tk)) {
+        give_up_seq(P, b, lane);
+        return;
+    }
+    if (tk.mode == kModeNone) return;
     const size_t prow = (size_t)(o0 + b + tk.n), qrow = (size_t)(o0 + tk.n);
     // rows whose maximum is near zero carry the rounding of l - m (see exp2_ff2)
     const bool twosum = fabsf(tk.m_p) < kNeedTwoSum || (tk.mode == kModeResidual && fabsf(tk.m_q) < kNeedTwoSum);
     uint32_t lane_rm = 0;  // the draw's removed columns among this lane's (point-mass and tree residuals)
     if (tk.nrm) {          // warp-uniform
         int32_t rtok = -1;
-        if (!removed_tokens(P, b, tk, lane, rtok)) return;
+        if (!removed_tokens(P, b, tk, lane, rtok)) {
+            give_up_seq(P, b, lane);
+            return;
+        }
         lane_rm = removed_bits(rtok, tk.nrm, i * kSTask + 32 * lane, 32);
     }
     if (__any_sync(0xFFFFFFFFu, lane_rm != 0u)) {
@@ -1435,7 +1497,7 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
     } else {
         s_accumulate<DT, VEC, false, false, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
     }
-    if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0 + b + tk.npos, tab, lane);
+    if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0, tab, lane);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1569,18 +1631,20 @@ __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, 
             nbytes = (uint32_t)len_of(ci) * 2u;
         }
         advance(ri, ci);
-        // one verdict for the whole warp: a time-out seen by some lanes only must not split it
+        // one verdict for the whole warp: a time-out seen by some lanes only must not split it (a copy
+        // always lands: this bound is the library's, never a caller's)
         const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[s], (parity >> s) & 1u, kSpinLimit));
-        parity ^= 1u << s;
         if (!ok) {
-            // a copy that never lands: report, let the copies still in flight land, stop streaming
+            // a copy that does not land: report, give every copy in flight (this stage's included) its
+            // own bound to land before the shared memory is left, stop streaming
             if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
-            for (int q = 1; q < kStages; ++q) {
+            for (int q = 0; q < kStages; ++q) {
                 const int s2 = (k + q) % kStages;
                 if (t + q * SW < nA) mbar_wait(&bars[s2], (parity >> s2) & 1u, kSpinLimit);
             }
             return;
         }
+        parity ^= 1u << s;
         ATask at;
         at.r = (int32_t)rp;
         at.ch = (int32_t)cp;
@@ -1699,6 +1763,75 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------------------------------------
+// Debug output beta_i = sum_x min(p_i(x), q_i(x)) (velog "6-1편. Speculative Decoding", §2-3: the
+// probability that slot i's draft is accepted), recomputed from the logits after the step, one CTA per
+// draft row: fp32 exponentials, fp64 sums. Point-mass drafts: beta_i = p_i(x_i). Not on the step's path.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ double block_sum(double v, double* red) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    double t = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+    return t;
+}
+__device__ __forceinline__ float block_max(float v, double* red) {
+    v = warp_max(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = (double)v;
+    __syncthreads();
+    float t = -INFINITY;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t = fmaxf(t, (float)red[w]);
+    return t;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) k_debug_beta(const __grid_constant__ Params P) {
+    __shared__ double red[8];
+    const int32_t r = (int32_t)blockIdx.x;  // draft slot
+    if (*(volatile uint32_t*)P.status & (1u << SV_ERR_BAD_OFFSETS)) return;  // rows not owned reliably
+    const int32_t R_d = __ldg(P.offs + P.B);
+    if (r >= R_d) return;
+    int32_t lo = 0, hi = P.B - 1;  // sequence b with offs[b] <= r < offs[b + 1]
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(P.offs + mid) <= r) lo = mid; else hi = mid - 1;
+    }
+    const int32_t b = lo, x = __ldg(P.tokens + r);
+    if (x < 0 || x >= P.V) return;
+    const size_t trow = (size_t)(r + b) * (size_t)P.V, drow = (size_t)r * (size_t)P.V;
+    const float K = P.K_hi;
+    float mt = -INFINITY, md = -INFINITY;
+    for (int32_t k = threadIdx.x; k < P.V; k += blockDim.x) {
+        mt = fmaxf(mt, logit_at<DT>(P.target, trow + k));
+        if (!P.pm) md = fmaxf(md, logit_at<DT>(P.draft, drow + k));
+    }
+    mt = block_max(mt, red);
+    if (!P.pm) md = block_max(md, red);
+    double st = 0.0, sd = 0.0;
+    for (int32_t k = threadIdx.x; k < P.V; k += blockDim.x) {
+        st += (double)exp2f((logit_at<DT>(P.target, trow + k) - mt) * K);
+        if (!P.pm) sd += (double)exp2f((logit_at<DT>(P.draft, drow + k) - md) * K);
+    }
+    st = block_sum(st, red);
+    if (P.pm) {
+        if (threadIdx.x == 0) P.dbg.beta[r] = (double)exp2f((logit_at<DT>(P.target, trow + x) - mt) * K) / st;
+        return;
+    }
+    sd = block_sum(sd, red);
+    double m = 0.0;
+    for (int32_t k = threadIdx.x; k < P.V; k += blockDim.x) {
+        const double pk = (double)exp2f((logit_at<DT>(P.target, trow + k) - mt) * K) / st;
+        const double qk = (double)exp2f((logit_at<DT>(P.draft, drow + k) - md) * K) / sd;
+        m += pk < qk ? pk : qk;
+    }
+    m = block_sum(m, red);
+    if (threadIdx.x == 0) P.dbg.beta[r] = m;
+}
+
+// ------------------------------------------------------------------------------------------------
 // Launch
 // ------------------------------------------------------------------------------------------------
 template <int DT, bool VEC, bool GREEDY>
@@ -1734,14 +1867,21 @@ static cudaError_t launch_typed(const Params& P, cudaStream_t st) {
 cudaError_t launch_verify(const Params& P, const Layout& L, void* ws, int dtype, bool vec, bool greedy,
                           cudaStream_t st) {
     if (P.B == 0) return cudaSuccess;
-    const cudaError_t e = cudaMemsetAsync((char*)ws + L.zero_begin, 0, L.zero_end - L.zero_begin, st);
+    cudaError_t e = cudaMemsetAsync((char*)ws + L.zero_begin, 0, L.zero_end - L.zero_begin, st);
     if (e != cudaSuccess) return e;
     if (dtype == SV_BF16) {
-        if (vec) return greedy ? launch_typed<SV_BF16, true, true>(P, st) : launch_typed<SV_BF16, true, false>(P, st);
-        return greedy ? launch_typed<SV_BF16, false, true>(P, st) : launch_typed<SV_BF16, false, false>(P, st);
+        if (vec) e = greedy ? launch_typed<SV_BF16, true, true>(P, st) : launch_typed<SV_BF16, true, false>(P, st);
+        else e = greedy ? launch_typed<SV_BF16, false, true>(P, st) : launch_typed<SV_BF16, false, false>(P, st);
+    } else {
+        if (vec) e = greedy ? launch_typed<SV_F32, true, true>(P, st) : launch_typed<SV_F32, true, false>(P, st);
+        else e = greedy ? launch_typed<SV_F32, false, true>(P, st) : launch_typed<SV_F32, false, false>(P, st);
     }
-    if (vec) return greedy ? launch_typed<SV_F32, true, true>(P, st) : launch_typed<SV_F32, true, false>(P, st);
-    return greedy ? launch_typed<SV_F32, false, true>(P, st) : launch_typed<SV_F32, false, false>(P, st);
+    if (e != cudaSuccess || greedy || !P.dbg.beta || P.max_gamma == 0) return e;
+    // debug output only: beta of every draft slot, after the step on the same stream
+    const unsigned grid = (unsigned)((int64_t)P.B * P.max_gamma);
+    if (dtype == SV_BF16) k_debug_beta<SV_BF16><<<grid, 256, 0, st>>>(P);
+    else k_debug_beta<SV_F32><<<grid, 256, 0, st>>>(P);
+    return cudaGetLastError();
 }
 
 Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma) {
@@ -1749,14 +1889,16 @@ Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma) {
     const size_t nchA = ((size_t)V + kAChunk - 1) / kAChunk;
     const size_t nS = ((size_t)V + kSTask - 1) / kSTask;
     Layout L;
-    // the first four regions are cleared before every call, with one memset
+    // every region before the status word is cleared before every call, with one memset
     L.counters = 0;
     L.partials = up(L.counters + sizeof(Counters));
     L.taskw = up(L.partials + (size_t)B * (2 * (size_t)max_gamma + 1) * nchA * sizeof(PartialWord));
     L.recw = up(L.taskw + (size_t)B * kTaskWords * sizeof(Word));
     L.groupw = up(L.recw + (size_t)B * nS * kRecWords * sizeof(Word));
     L.remw = up(L.groupw + (size_t)B * nS * kGroups * kGroupWords * sizeof(Word));
-    L.status = up(L.remw + (size_t)B * kMaxRemoved * sizeof(Word));
+    L.pathw = up(L.remw + (size_t)B * kMaxRemoved * sizeof(Word));
+    L.seqstate = up(L.pathw + (size_t)B * kMaxRemoved * sizeof(Word));
+    L.status = up(L.seqstate + (size_t)B * sizeof(uint32_t));
     L.zero_begin = 0;
     L.zero_end = L.status;
     L.total = up(L.status + sizeof(uint32_t));

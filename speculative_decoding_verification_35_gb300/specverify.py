@@ -25,7 +25,8 @@ EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_
 
 class SvDebug(ctypes.Structure):
     _fields_ = [("row_lse", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p),
-                ("p_x", ctypes.c_void_p), ("q_x", ctypes.c_void_p), ("seq_mass", ctypes.c_void_p)]
+                ("p_x", ctypes.c_void_p), ("q_x", ctypes.c_void_p), ("seq_mass", ctypes.c_void_p),
+                ("beta", ctypes.c_void_p), ("spin_limit", ctypes.c_uint32)]
 
 
 class SvDeviceBuffers(ctypes.Structure):
@@ -193,9 +194,10 @@ class Call:
                             row_argmax=torch.full((R_t,), -7, dtype=torch.int32, device=device),
                             p_x=torch.full((R_d,), float("nan"), dtype=torch.float64, device=device),
                             q_x=torch.full((R_d,), float("nan"), dtype=torch.float64, device=device),
-                            seq_mass=torch.full((B,), float("nan"), dtype=torch.float64, device=device))
+                            seq_mass=torch.full((B,), float("nan"), dtype=torch.float64, device=device),
+                            beta=torch.full((R_d,), float("nan"), dtype=torch.float64, device=device))
             self.dbg_struct = SvDebug(*(self.dbg[k].data_ptr() for k in
-                                        ("row_lse", "row_argmax", "p_x", "q_x", "seq_mass")))
+                                        ("row_lse", "row_argmax", "p_x", "q_x", "seq_mass", "beta")), 0)
 
     def run(self, target, draft, draft_tokens, seq_offsets, gammas, temperature, seed, step, stream=None,
             clear_status=True) -> int:

@@ -105,6 +105,57 @@ def assert_parity(b, seed, step, g=None, r=None, check_debug=True):
         m = r.q_x >= 1e-30
         np.testing.assert_allclose(g["q_x"][m], r.q_x[m], rtol=REL)
         np.testing.assert_allclose(g["seq_mass"], r.seq_mass, rtol=REL)
+        m = r.beta >= 1e-30
+        np.testing.assert_allclose(g["beta"][m], r.beta[m], rtol=REL)
+        np.testing.assert_allclose(g["beta"][~m], r.beta[~m], rtol=0, atol=1e-30)
     if check_debug and b.temperature == 0 and r.status == 0:
         np.testing.assert_array_equal(g["row_argmax"], r.row_argmax)
     return rep
+
+
+def compare_steps(b, g_tokens, g_n, r_tokens, r_n, r0, seed, step0):
+    """``compare`` over many steps of one batch at once: g_* / r_* are [steps, R_t] tokens and [steps, B]
+    counts from the GPU and from ``oracle.verify_steps``; r0 is the oracle's debug ``Result`` of the batch
+    (p(x_i), q(x_i) do not depend on the step). Exact matches are found with array operations; only the
+    disagreeing sequences are classified (band or mismatch) one by one. Returns counts: uniform draws
+    (accept tests and draws), token draws, band and mismatch lists."""
+    T = t32(b.temperature)
+    S, B = r_n.shape
+    gam = b.gammas.astype(np.int64)
+    t0 = (b.seq_offsets[:-1] + np.arange(B)).astype(np.int64)
+    # per sequence and step: do all gamma + 1 slots and the count agree
+    same = g_n == r_n
+    slot_ok = g_tokens == r_tokens  # [S, R_t]
+    seq_of_slot = np.repeat(np.arange(B), gam + 1)
+    bad_slot = np.zeros((S, B), dtype=bool)
+    for s in range(S):
+        bad_slot[s] = np.bincount(seq_of_slot, weights=~slot_ok[s], minlength=B) > 0
+    agree = same & ~bad_slot
+    ok = r_n >= 0
+    uni = np.where(r_n < gam, r_n + 1, gam) + 1
+    draws = int(uni[ok].sum())
+    token_draws = int(ok.sum())
+    band, bad = [], []
+    for s, q in zip(*np.nonzero(~agree)):
+        nr, ng = int(r_n[s, q]), int(g_n[s, q])
+        if T == 0 or nr < 0 or ng < 0:
+            bad.append((int(s), int(q), "greedy/err", nr, ng))
+            continue
+        d0 = int(b.seq_offsets[q])
+        if nr != ng:
+            i = min(nr, ng)
+            u = oracle.uniform(seed, step0 + int(s), int(q), i, 0)
+            px, qx = r0.p_x[d0 + i], r0.q_x[d0 + i]
+            ratio = px / qx if qx > 0 else np.inf
+            (band if abs(u - ratio) < BAND else bad).append((int(s), int(q), "accept", i, u, ratio))
+            continue
+        n = nr
+        kg = int(g_tokens[s, t0[q] + n])
+        u = oracle.uniform(seed, step0 + int(s), int(q), n, 1)
+        gm = int(gam[q])
+        drow = b.draft[d0 + n] if n < gm and b.draft is not None else None
+        x_excl = int(b.draft_tokens[d0 + n]) if n < gm and b.draft is None else -1
+        tok, lo, hi, Sm = oracle.draw_bracket(b.target[t0[q] + n], drow, b.V, T, u, kg, x_excl)
+        dist = 0.0 if lo <= u < hi else min(abs(u - lo), abs(u - hi))
+        (band if dist < BAND else bad).append((int(s), int(q), "draw", n, u, kg, tok, lo, hi))
+    return dict(draws=draws, token_draws=token_draws, band=band, bad=bad)

@@ -55,6 +55,20 @@ def test_commit_matches_oracle_on_synthetic_outputs(B, cap):
     assert gs == rs
 
 
+def test_commit_rejects_counts_above_the_largest_gamma():
+    # gaps above 31 with n above 31: lanes 0..31 could not copy the slots, so nothing is appended
+    out = np.arange(200, dtype=np.int32)
+    offs = np.array([0, 40, 80, 120], np.int32)
+    n = np.array([35, 31, 40], np.int32)
+    hist = np.full((3, 100), 5, np.int32)
+    lens = np.array([0, 1, 2], np.int32)
+    gh, gl, gn, gs = _gpu_commit(out, n, offs, hist, 100, lens)
+    rh, rl, rn, rs = commit(out, n, offs, hist, 100, lens)
+    assert rs == 1 << 4 and gs == rs
+    assert np.array_equal(gh, rh) and np.array_equal(gl, rl) and np.array_equal(gn, rn)
+    assert gn.tolist() == [-1, int(out[40 + 1 + 31]), -1]
+
+
 @pytest.mark.parametrize("name", ["b64_g5_v128256", "ragged_b128_v129280"])
 def test_verify_then_commit_over_steps_without_host_sync(name):
     from speculative_decoding_verification_35_gb300 import specverify as sv

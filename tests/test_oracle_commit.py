@@ -35,6 +35,16 @@ def test_inconsistent_count_is_flagged():
     assert st == 1 << SV_ERR_BAD_OFFSETS and lens.tolist() == [0] and nxt.tolist() == [-1]
 
 
+def test_count_above_the_largest_gamma_is_flagged():
+    # a gap of 40 slots with n = 35: no verify call reports n above 31, so the outputs are not a verify
+    # call's and nothing is appended
+    out = list(range(41))
+    h, lens, nxt, st = commit(out, [35], [0, 40], np.zeros((1, 64), np.int32), 64, [0])
+    assert st == 1 << SV_ERR_BAD_OFFSETS and lens.tolist() == [0] and nxt.tolist() == [-1]
+    h, lens, nxt, st = commit(out, [31], [0, 40], np.zeros((1, 64), np.int32), 64, [0])
+    assert st == 0 and lens.tolist() == [32] and h[0, :32].tolist() == list(range(32))
+
+
 def test_appended_tokens_are_the_accepted_drafts():
     # a verify step of the oracle, then the update: the first n appended tokens equal the draft tokens,
     # the last one is the drawn token, and nothing outside the appended range changes
