@@ -175,8 +175,10 @@ int spec_verify_host(const void* target_logits, const void* draft_logits, sv_dty
  * loads the library until the process exits) instead of a caller workspace. It allocates and frees
  * nothing. Batches whose spec_verify_workspace_size(B, V, max_gamma) exceeds 8 MiB are rejected with
  * SV_ERR_WORKSPACE before anything is launched. The first call on a device looks up the array's
- * device address (cudaGetSymbolAddress with that device current); make that first call before any
- * stream capture. All calls share the one array and each call clears what it needs at its start, so
+ * device address (cudaGetSymbolAddress with that device current) and keeps it for that device; make
+ * that first call before any stream capture. The kept address belongs to the device's primary
+ * context as it was at that first call: after cudaDeviceReset, or from a different (non-primary)
+ * context on the same device, it is no longer valid, and this entry point must not be used there. All calls share the one array and each call clears what it needs at its start, so
  * calls that may overlap on the GPU (other streams, other threads) race and must be serialised by the
  * caller.
  */
