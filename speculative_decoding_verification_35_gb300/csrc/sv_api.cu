@@ -101,6 +101,12 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.K_hi = K_hi;
     P.K_lo = (float)(K64 - (double)K_hi);
     P.d_min = greedy ? 0.f : (float)(-126.5 / (double)K_hi);
+    // The sampler's value table serves a draw whose rows' maxima m make its two stand-ins negligible and
+    // keep its sums finite: m <= 63.75 (no logit above the table), m >= -63.75 + 60 / K (every logit at
+    // or below -63.75, taken as weight 0, lies 2^60 below the row's largest weight) and m K <= 96 (sums of
+    // up to 2^31 weights of at most 2^96 stay finite).
+    P.tab_mlo = greedy ? 1.f : (float)(-63.75 + 60.0 / (double)K_hi);
+    P.tab_mhi = greedy ? 0.f : (float)std::min(63.75, 96.0 / (double)K_hi);
     P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;
     P.seed = seed;
     P.step = step;

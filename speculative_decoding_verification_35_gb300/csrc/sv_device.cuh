@@ -8,7 +8,10 @@
 // double and the remainder by its Taylor series (written from the series, no library constants).
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include "sv_internal.h"
 
 namespace sv {
 
@@ -234,9 +237,37 @@ __device__ __forceinline__ float gt_mask(float a, float b) {
     return r;
 }
 
-// Split of a weight w in [0, 1] into a part on the 2^-20 grid (hi) and the rest (lo, |lo| <= 2^-21):
-// sums of up to 16 grid parts are exact in float, so an accumulator only needs plain adds.
-__device__ __forceinline__ float2 grid_hi(float2 w) { return add2(add2(w, f2(12.f)), f2(-12.f)); }
+// Split of a weight w in [0, 2^E] into a part on the 2^(E-20) grid (hi) and the rest (lo, |lo| <= 2^(E-21)),
+// G = 1.5 * 2^(E+3) (G = 12 for weights in [0, 1]): w + G rounds w to the grid (the unit in the last place
+// of G), and sums of up to 16 grid parts (at most 2^(E+4), on a grid of 2^(E-20)) are exact in float, so
+// an accumulator only needs plain adds.
+__device__ __forceinline__ float2 grid_hi(float2 w, float G) { return add2(add2(w, f2(G)), f2(-G)); }
+__device__ __forceinline__ float2 grid_hi(float2 w) { return grid_hi(w, 12.f); }
+
+// The grid constant for weights below 2^(floor(e) + 1), e = the log2 of the largest weight (|e| <= 100).
+__device__ __forceinline__ float grid_const(float e) {
+    const int E = (int)floorf(e) + 1;
+    return 3.f * __int_as_float((E + 2 + 127) << 23);  // 1.5 * 2^(E + 3)
+}
+
+// Weights of the two columns of a bf16 pair word from the value table in shared memory (see kTabCodeLo):
+// both magnitudes clamped to the table's range by one bf16x2 max and one min (exact), their offsets from
+// the range's start scaled by the entry size in one shift, the sign bit of each column selecting the
+// table's half. x: the low column, y: the high column.
+__device__ __forceinline__ ff2 tab_pair(uint32_t w, const char* vt) {
+    const uint32_t a = w & 0x7FFF7FFFu;
+    __nv_bfloat162 v = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                               __halves2bfloat162(__ushort_as_bfloat16((unsigned short)kTabCodeLo),
+                                                  __ushort_as_bfloat16((unsigned short)kTabCodeLo)));
+    v = __hmin2(v, __halves2bfloat162(__ushort_as_bfloat16((unsigned short)kTabCodeHi),
+                                      __ushort_as_bfloat16((unsigned short)kTabCodeHi)));
+    const uint32_t d3 = (*reinterpret_cast<const uint32_t*>(&v) - (kTabCodeLo | kTabCodeLo << 16)) << 3;
+    const uint32_t o0 = (d3 & 0x7FF8u) | (w & 0x8000u);  // 8 (i + 4096 s) of the low column
+    const uint32_t o1 = (d3 | (w & 0x80000000u)) >> 16;  // and of the high column
+    const float2 t0 = *reinterpret_cast<const float2*>(vt + o0);
+    const float2 t1 = *reinterpret_cast<const float2*>(vt + o1);
+    return ff2{make_float2(t0.x, t1.x), make_float2(t0.y, t1.y)};
+}
 
 // ------------------------------------------------------------------------------------------------
 // Fast (MUFU) 2^x for the statistics pass: relative error about 2^-22, ex2(-inf) = 0.

@@ -9,19 +9,33 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;               // threads per CTA
+constexpr int kThreads = 512;               // threads per CTA (one CTA per SM: its shared memory holds the
+                                            // bulk-copy stages and the sampler's value table)
 constexpr int kWarps = kThreads / 32;       // independent warp workers per CTA
 constexpr int kAChunk = 4096;               // vocabulary columns of one statistics task (one warp, one row)
 constexpr int kSTask = 1024;                // vocabulary columns of one sampler task (one warp): the unit
                                             // of the inverse-CDF search's first level
 constexpr int kScanBlock = 512;             // columns the find's element scan covers per pass
 constexpr int kScanPerLane = kScanBlock / 32;  // 16 consecutive columns per lane
-constexpr int kStreamWarps = 4;             // statistics streamers per CTA on the bulk-copy path
-constexpr int kStages = 2;                  // bulk-copy stages per streamer (64 KB in flight per CTA:
+constexpr int kStreamWarps = 8;             // statistics streamers per CTA on the bulk-copy path
+constexpr int kStages = 2;                  // bulk-copy stages per streamer (128 KB in flight per SM:
                                             // enough for the HBM rate, short enough that other requests
                                             // and instruction fetches are not queued far behind)
 constexpr int kStageBytes = kAChunk * 2;    // one bf16 statistics task
 constexpr int kTmaSmemBytes = kStreamWarps * kStages * (kStageBytes + 8);
+
+// The sampler's value table (bf16 logits): 2^(l K) as float-float for every bf16 magnitude in
+// [2^-26, 64) of either sign, indexed by the bf16 code itself: entry (s << 12) | i holds sign s and
+// magnitude code 0x3280 + i (0x3280 = 2^-26, 0x427F = 63.75). Entry i = 0 stands for every magnitude
+// below 2^-26 and holds 2^0 (l = 0); the last negative entry (l = -63.75) holds 0 and stands for every
+// logit at or below it, -inf included. A draw uses the table only when its rows' maxima make those two
+// stand-ins negligible (tab_ok); its weights are then 2^(l K) instead of 2^((l - m) K), a per-row scale
+// that cancels in every ratio the inverse CDF uses.
+constexpr uint32_t kTabCodeLo = 0x3280u;    // bf16 code of 2^-26
+constexpr uint32_t kTabCodeHi = 0x427Fu;    // bf16 code of 63.75
+constexpr int kTabHalf = 4096;              // entries per sign
+constexpr int kTabBytes = 2 * kTabHalf * 8; // 64 KB
+constexpr int kTabSmemOffset = (kTmaSmemBytes + 15) & ~15;  // after the stages and their barriers
 constexpr int kBaseCache = 1024;            // batches up to this size keep their row bases in shared memory
 constexpr int kRowCache = 2048;             // sampling batches with up to this many statistics rows keep a
                                             // row map (target or draft, row index) in shared memory
@@ -91,6 +105,7 @@ struct Params {
     unsigned long long nS_recip;  // floor(2^64 / nS) + 1 (nS >= 2): c / nS = high 64 bits of c * nS_recip
     float K_hi, K_lo;  // log2(e) / T as float-float
     float d_min;       // clamp of l - m in the precise exponential (about -126.5 / K)
+    float tab_mlo, tab_mhi;  // a draw uses the value table when its rows' raw maxima lie in [tab_mlo, tab_mhi]
     uint32_t spin;     // polls before a wait on another warp's word gives up (kSpinLimit unless a caller
                        // testing the time-out path asks for fewer)
     double invT64;     // 1 / T (debug output of the row log-normalisers only)

@@ -209,9 +209,9 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
 }
 
 // Sampling-mode statistics of 16 x 8 bf16 values per lane (4096 columns per warp): bf16x2 max, then the
-// fp32 sum of 2^((l - m) K) with packed FMA/ADD and one MUFU ex2 per value.
-__device__ __forceinline__ SegStats stats_bf16(const uint4 (&v)[16], float K) {
-    SegStats r{-INFINITY, 0.f, 0x7FFFFFFF, 0u};
+// fp32 sum of 2^((l - m) K) with packed FMA/ADD and one MUFU ex2 per value. In two parts: the lane's
+// maximum (which reads every value, so the values are in registers once it is done), then the rest.
+__device__ __forceinline__ float lane_max_bf16(const uint4 (&v)[16]) {
     __nv_bfloat162 mx = __halves2bfloat162(__ushort_as_bfloat16(0xFF80), __ushort_as_bfloat16(0xFF80));
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
@@ -220,7 +220,11 @@ __device__ __forceinline__ SegStats stats_bf16(const uint4 (&v)[16], float K) {
         mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].z));
         mx = __hmax2(mx, *reinterpret_cast<const __nv_bfloat162*>(&v[q].w));
     }
-    const float m = warp_max(fmaxf(__low2float(mx), __high2float(mx)));
+    return fmaxf(__low2float(mx), __high2float(mx));
+}
+__device__ __forceinline__ SegStats stats_bf16_finish(const uint4 (&v)[16], float mlane, float K) {
+    SegStats r{-INFINITY, 0.f, 0x7FFFFFFF, 0u};
+    const float m = warp_max(mlane);
     float s = 0.f;
     if (m != -INFINITY) {
         const float2 K2 = make_float2(K, K);
@@ -254,10 +258,12 @@ __device__ __forceinline__ SegStats stats_bf16(const uint4 (&v)[16], float K) {
     r.s = warp_sumf(s);  // a NaN or +inf logit makes this NaN (flagged by the caller)
     return r;
 }
+__device__ __forceinline__ SegStats stats_bf16(const uint4 (&v)[16], float K) {
+    return stats_bf16_finish(v, lane_max_bf16(v), K);
+}
 
-// The same statistics from a bulk-copied shared-memory stage of `len` columns.
-__device__ __forceinline__ SegStats stats_bf16_smem(const unsigned char* buf, int len, int lane, float K) {
-    uint4 v[16];
+// A bulk-copied shared-memory stage of `len` columns into registers (-inf past len).
+__device__ __forceinline__ void load_stage(const unsigned char* buf, int len, int lane, uint4 (&v)[16]) {
     const uint4* b4 = reinterpret_cast<const uint4*>(buf);
     if (len == kAChunk) {  // a full task (all but a row's last): no per-read guard
 #pragma unroll
@@ -269,7 +275,6 @@ __device__ __forceinline__ SegStats stats_bf16_smem(const unsigned char* buf, in
             v[q] = e0 < len ? b4[q * 32 + lane] : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
         }
     }
-    return stats_bf16(v, K);
 }
 
 template <int DT, bool VEC, bool GREEDY>
@@ -428,10 +433,40 @@ __device__ __noinline__ void give_up_seq(const Params& P, int32_t b, int lane) {
 // ------------------------------------------------------------------------------------------------
 // Sampler work of a sequence (see kTaskWords)
 // ------------------------------------------------------------------------------------------------
+// Whether a draw's weights come from the value table (bf16 rows with 16-byte alignment, both maxima in the
+// table's range; see kTabCodeLo): decided from the draw's words alone, so its decision, every sampler task
+// and its find agree.
+template <int DT, bool VEC>
+__device__ __forceinline__ bool draw_uses_table(const Params& P, int32_t mode, float m_p, float m_q) {
+    if (!(DT == SV_BF16 && VEC)) return false;
+    auto ok = [&](float m) { return m >= P.tab_mlo && m <= P.tab_mhi; };
+    return ok(m_p) && (mode != kModeResidual || ok(m_q));
+}
+
+// The value table in shared memory: entry (s << 12) | i = 2^(l K) as (hi, lo) for the bf16 value l of sign
+// s and magnitude code kTabCodeLo + i; entry i = 0 holds l = 0 and the last negative entry 0 (see
+// kTabCodeLo). Built by threads t = 0 .. nt - 1 of the CTA, two entries per exponential, with the precise
+// exponential of the sampler's fallback path (l - m with m = 0 is exact). Entries whose 2^(l K) would
+// leave the float range hold 2^126 and are never read by a draw that uses the table.
+__device__ __noinline__ void build_value_table(const Params& P, float2* vt, const float* tab, int t, int nt) {
+    const ExpConst EC{P.K_hi, P.K_lo, P.d_min};
+    const float lmax = 126.f / P.K_hi;
+    for (int j = 2 * t; j < 2 * kTabHalf; j += 2 * nt) {  // j, j + 1: one sign, consecutive codes
+        const uint32_t sgn = (uint32_t)j >> 12, i = (uint32_t)j & (kTabHalf - 1);
+        auto val = [&](uint32_t ii) {
+            return ii ? fminf(__uint_as_float(((sgn << 15) | (kTabCodeLo + ii)) << 16), lmax) : 0.f;
+        };
+        const ff2 e = exp2_ff2<false>(make_float2(val(i), val(i + 1)), f2(0.f), EC, tab);
+        vt[j] = make_float2(e.hi.x, e.lo.x);
+        vt[j + 1] = sgn && i + 1 == kTabHalf - 1 ? make_float2(0.f, 0.f) : make_float2(e.hi.y, e.lo.y);
+    }
+}
+
 struct TaskInfo {
     int32_t mode, n;  // n: the node (slot) whose target row the draw takes
     int32_t npos;     // the output slot of the drawn token (n itself, except in a token tree)
-    float m_p, m_q, rho, u;
+    float m_p, m_q, rho, u;  // rho: the selection ratio (s_p / s_q approximately; for a draw that uses the
+                             // value table, in table units: times 2^((m_p - m_q) K))
     int32_t xcl;  // kModeResidualPM: the column the draw removes (the draft token); else -1
     int32_t nrm;  // tokens the draw removes: 1 (kModeResidualPM), k (kModeResidualSet), else 0
 };
@@ -605,7 +640,7 @@ struct CoopRows {
 // wsub, wsub + nsub, ...; the row statistics meet in shared memory (set `set` of `co`) behind a named
 // barrier over the deciding warps, and warp 0 goes on alone (the others return after the barrier).
 // nsub == 1: the warp reduces every row itself.
-template <int DT, bool GREEDY>
+template <int DT, bool VEC, bool GREEDY>
 __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float* tab,
                                     int wsub, int nsub, CoopRows* co, int set) {
     const int32_t t0 = o0 + b;
@@ -849,9 +884,15 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     if (P.pm)  // the residual of a point-mass draft removes column x_n; rho's word carries x_n + 1
         put_task(P, b, lane, n < g ? kModeResidualPM : kModeBonus, n, pm, 0.f,
                  n < g ? __int_as_float(xn + 1) : 1.f, un, n);
-    else
-        put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, pm, n < g ? qm : 0.f,
-                 n < g ? div_fma(ps, qs) : 1.f, un, n);
+    else {
+        // the selection ratio s_p / s_q, in table units (times 2^((m_p - m_q) K)) for a draw the table serves
+        float rho = 1.f;
+        if (n < g) {
+            rho = div_fma(ps, qs);
+            if (draw_uses_table<DT, VEC>(P, kModeResidual, pm, qm)) rho *= exp2_fma((pm - qm) * K);
+        }
+        put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, pm, n < g ? qm : 0.f, rho, un, n);
+    }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -934,16 +975,40 @@ __device__ __forceinline__ ff column_weight(float lp, float lq, const TaskInfo& 
     const bool sel = e.hi.x > tk.rho * e.hi.y;  // the selection rule of sel_mask
     return resid_weight(e.hi.x, e.lo.x, e.hi.y, e.lo.y, sel ? 1.f : 0.f, rho);
 }
+// The same in the value table's units, from the columns' raw bf16 codes (p in the low half of pq, q in
+// the high half): the weights the sampler tasks summed for a draw that uses the table.
+__device__ __forceinline__ ff column_weight_tab(uint32_t pq, const TaskInfo& tk, bool resid, ff rho, const char* vt,
+                                                bool removed) {
+    const ff2 e = tab_pair(pq, vt);
+    if (!resid) return removed ? ff{0.f, 0.f} : ff_norm(e.hi.x, e.lo.x);
+    const bool sel = e.hi.x > tk.rho * e.hi.y;  // the selection rule of sel_mask
+    return resid_weight(e.hi.x, e.lo.x, e.hi.y, e.lo.y, sel ? 1.f : 0.f, rho);
+}
+// Column k's weight in the find, either way (TAB: the value table's, from the raw codes).
+template <int DT, bool TAB>
+__device__ __forceinline__ ff weight_at(const Params& P, size_t prow, size_t qrow, int32_t k, const TaskInfo& tk,
+                                        const ExpConst& EC, bool resid, ff rho, const float* tab, const char* vt,
+                                        bool removed) {
+    if constexpr (TAB) {
+        const uint32_t cp = __ldg((const unsigned short*)P.target + prow * (size_t)P.V + k);
+        const uint32_t cq = resid ? __ldg((const unsigned short*)P.draft + qrow * (size_t)P.V + k) : 0u;
+        return column_weight_tab(cp | cq << 16, tk, resid, rho, vt, removed);
+    } else {
+        const float lpk = logit_at<DT>(P.target, prow * (size_t)P.V + k);
+        const float lqk = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + k) : 0.f;
+        return column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab, removed);
+    }
+}
 
 // Inverse-CDF search over the columns [k_lo, k_hi) for the remaining target `rem`, kScanBlock columns
 // per pass (16 consecutive columns per lane, float-float). Each lane keeps only its total; once the
 // crossing lane is known, 16 lanes recompute its columns in parallel (their data are L1-resident) and
 // a 16-lane prefix picks the column. Returns the first column whose running sum exceeds `rem`, or the
 // last column of positive weight when the crossing is lost to rounding (or `tail_rule` asks for it).
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool TAB>
 __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& tk, size_t prow, size_t qrow, bool resid, ff rho,
                                  int32_t k_lo, int32_t k_hi, ff rem, bool tail_rule, int32_t rtok, int32_t nrm,
-                                 const float* tab, int lane) {
+                                 const float* tab, const char* vt, int lane) {
     const ExpConst EC = exp_const(P);
     // a unit spans at most kSTask columns: NB passes; bf16 issues every pass's loads first
     constexpr int NB = kSTask / kScanBlock;
@@ -976,9 +1041,16 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
         const uint32_t rb = removed_bits(rtok, nrm, k0, kScanPerLane);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float2 lpv = col2<DT>(cp, e), lqv = resid ? col2<DT>(cq, e) : f2(0.f);
-            const ff w0 = column_weight<DT>(lpv.x, lqv.x, tk, EC, resid, rho, tab, (rb >> (2 * e)) & 1u);
-            const ff w1 = column_weight<DT>(lpv.y, lqv.y, tk, EC, resid, rho, tab, (rb >> (2 * e + 1)) & 1u);
+            ff w0, w1;
+            if constexpr (TAB) {  // the pair word of the p row, and of the q row, by halves
+                const uint32_t pw = cp.w[e], qw = resid ? cq.w[e] : 0u;
+                w0 = column_weight_tab((pw & 0xFFFFu) | (qw << 16), tk, resid, rho, vt, (rb >> (2 * e)) & 1u);
+                w1 = column_weight_tab((pw >> 16) | (qw & 0xFFFF0000u), tk, resid, rho, vt, (rb >> (2 * e + 1)) & 1u);
+            } else {
+                const float2 lpv = col2<DT>(cp, e), lqv = resid ? col2<DT>(cq, e) : f2(0.f);
+                w0 = column_weight<DT>(lpv.x, lqv.x, tk, EC, resid, rho, tab, (rb >> (2 * e)) & 1u);
+                w1 = column_weight<DT>(lpv.y, lqv.y, tk, EC, resid, rho, tab, (rb >> (2 * e + 1)) & 1u);
+            }
             if (k0 + 2 * e < k_hi && w0.hi > 0.f) {
                 tot = ff_add(tot, w0);
                 lastp = k0 + 2 * e;
@@ -1002,9 +1074,7 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
             const uint32_t rj = removed_bits(rtok, nrm, kj, 1);
             ff w{0.f, 0.f};
             if (lane < kScanPerLane && kj < k_hi) {
-                const float lpj = logit_at<DT>(P.target, prow * (size_t)P.V + kj);
-                const float lqj = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + kj) : 0.f;
-                w = column_weight<DT>(lpj, lqj, tk, EC, resid, rho, tab, rj != 0u);
+                w = weight_at<DT, TAB>(P, prow, qrow, kj, tk, EC, resid, rho, tab, vt, rj != 0u);
                 if (!(w.hi > 0.f)) w = ff{0.f, 0.f};
             }
             const ff c = ff_add(pre, warp_inscan_ff(w, lane));  // lanes >= 16 add zeros
@@ -1024,9 +1094,10 @@ __device__ __noinline__ int32_t scan_elements(const Params& P, const TaskInfo& t
 // that group's kGroupCols columns, 4 consecutive ones recomputed per lane. `rem` is the target left
 // after the tasks before. Rounding that loses the crossing (or tail_rule) picks the last group, then
 // column, of positive weight. Returns -1 when nothing in the task has positive weight, -2 on a time-out.
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool TAB>
 __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int unit, const TaskInfo& tk, size_t prow, size_t qrow,
-                                bool resid, ff rho, ff rem, bool tail_rule, int32_t rtok, const float* tab, int lane) {
+                                bool resid, ff rho, ff rem, bool tail_rule, int32_t rtok, const float* tab,
+                                const char* vt, int lane) {
     static_assert(kGroupCols == 4 * 32, "four columns per lane");
     const Word* gw = P.groupw + (((size_t)b * P.nS + unit) * kGroups + (lane % kGroups)) * kGroupWords;
     Word wa = lane < kGroups ? ld_word(gw) : (Word)kWordMark, wb = lane < kGroups ? ld_word(gw + 1) : (Word)kWordMark;
@@ -1056,17 +1127,37 @@ __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int uni
     const uint32_t r4 = removed_bits(rtok, tk.nrm, k0, 4);
     ff cw[4];
     ff tot{0.f, 0.f};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int32_t k = k0 + e;
-        cw[e] = ff{0.f, 0.f};
-        if (k < P.V) {
-            const float lpk = logit_at<DT>(P.target, prow * (size_t)P.V + k);
-            const float lqk = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + k) : 0.f;
-            cw[e] = column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab, (r4 >> e) & 1u);
-            if (!(cw[e].hi > 0.f)) cw[e] = ff{0.f, 0.f};
+    if constexpr (TAB) {  // rows 16-byte aligned, V a multiple of 8: the 4 columns are one 8-byte load per row
+        uint2 pw = make_uint2(0u, 0u), qw = make_uint2(0u, 0u);
+        if (k0 < P.V) {
+            pw = __ldg((const uint2*)((const unsigned short*)P.target + prow * (size_t)P.V + k0));
+            if (resid) qw = __ldg((const uint2*)((const unsigned short*)P.draft + qrow * (size_t)P.V + k0));
         }
-        tot = ff_add(tot, cw[e]);
+        const uint32_t pws[2] = {pw.x, pw.y}, qws[2] = {qw.x, qw.y};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t p16 = e & 1 ? pws[e >> 1] >> 16 : pws[e >> 1] & 0xFFFFu;
+            const uint32_t q16 = e & 1 ? qws[e >> 1] >> 16 : qws[e >> 1] & 0xFFFFu;
+            cw[e] = ff{0.f, 0.f};
+            if (k0 + e < P.V) {
+                cw[e] = column_weight_tab(p16 | q16 << 16, tk, resid, rho, vt, (r4 >> e) & 1u);
+                if (!(cw[e].hi > 0.f)) cw[e] = ff{0.f, 0.f};
+            }
+            tot = ff_add(tot, cw[e]);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int32_t k = k0 + e;
+            cw[e] = ff{0.f, 0.f};
+            if (k < P.V) {
+                const float lpk = logit_at<DT>(P.target, prow * (size_t)P.V + k);
+                const float lqk = resid ? logit_at<DT>(P.draft, qrow * (size_t)P.V + k) : 0.f;
+                cw[e] = column_weight<DT>(lpk, lqk, tk, EC, resid, rho, tab, (r4 >> e) & 1u);
+                if (!(cw[e].hi > 0.f)) cw[e] = ff{0.f, 0.f};
+            }
+            tot = ff_add(tot, cw[e]);
+        }
     }
     const ff tin = warp_inscan_ff(tot, lane);
     const ff cincl = ff_add(pre, tin), cexcl = ff_add(pre, exclusive_of(tin, lane));
@@ -1095,9 +1186,9 @@ __device__ __noinline__ int32_t group_search(const Params& P, int32_t b, int uni
 // Find for sequence b (one warp): run by the warp that holds the sequence's last sampler task, after
 // its own task. Exact normalisers from all task records (polled until written), the crossing task over
 // the records' weights, then the crossing column inside that task.
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool TAB>
 __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk, size_t prow, size_t qrow,
-                                  int32_t o0, const float* tab, int lane) {
+                                  int32_t o0, const float* tab, const char* vt, int lane) {
     // the sequence's outputs are this warp's to write, unless a wait on the sequence gave up first
     if (claim_seq(P, b, 1u, lane) != 0u) return;
     // the accepted tokens (slot j on lane j < npos): the draft tokens, or a tree's accepted path (written
@@ -1271,11 +1362,12 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
         int32_t rtok = -1;
         if (!by_p && !removed_tokens(P, b, tk, lane, rtok)) token = -2;
         if (!by_p && token != -2)
-            token = group_search<DT, VEC>(P, b, unit, tk, prow, qrow, resid, rho, rem, tail_rule, rtok, tab, lane);
+            token = group_search<DT, VEC, TAB>(P, b, unit, tk, prow, qrow, resid, rho, rem, tail_rule, rtok, tab, vt,
+                                               lane);
         if (by_p || token == -1) {
             const int32_t k_lo = unit * kSTask, k_hi = min(P.V, k_lo + kSTask);
-            token = scan_elements<DT, VEC>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule, rtok,
-                                           by_p ? 0 : tk.nrm, tab, lane);
+            token = scan_elements<DT, VEC, TAB>(P, tk, prow, qrow, resid, rho, k_lo, k_hi, rem, tail_rule, rtok,
+                                                by_p ? 0 : tk.nrm, tab, vt, lane);
         }
     }
     if (token < 0) {  // a time-out (reported in the status word)
@@ -1338,10 +1430,14 @@ __device__ __forceinline__ float2 pair8(const Cols8& c, int e) {
 // walks its 32 consecutive columns [32 L, 32 L + 32) in 4 steps of 8 (one 16-byte load per row; a
 // bf16 task's loads are all issued before the first step), accumulating the p and q weights and their
 // selected parts. It stores the selected sums of each group of kGroupLanes lanes, then the warp's sums
-// as the task's record. TWOSUM: carry the rounding of l - m (see exp2_ff2).
-template <int DT, bool VEC, bool TWOSUM, bool REMOVED, bool RESID>
+// as the task's record. TWOSUM: carry the rounding of l - m (see exp2_ff2). TAB: the weights are the
+// value table's 2^(l K) (table units, bf16 only), Gp / Gq the grid constants of their rows' largest
+// weights; otherwise the precise exponential's 2^((l - m) K) <= 1 (Gp = Gq = 12). rho_sel: the selection
+// ratio in the weights' units.
+template <int DT, bool VEC, bool TWOSUM, bool REMOVED, bool RESID, bool TAB>
 __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, const TaskInfo& tk, size_t prow,
-                                             size_t qrow, const float* tab, int lane, uint32_t lane_rm) {
+                                          size_t qrow, const float* tab, const char* vt, int lane, uint32_t lane_rm,
+                                          float Gp, float Gq, float rho_sel) {
     // RESID: a residual draw (p and q rows); else p alone (bonus, point-mass and tree residuals). Each
     // kind is its own instantiation, so each hot path's code is only its own.
     constexpr bool resid = RESID;
@@ -1355,16 +1451,24 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
     // grid-split accumulators (see grid_hi): all p and q weights, and those of the selected columns
     float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f);
     float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
+    auto wp = [&](const Cols8& c, int h) {
+        if constexpr (TAB) return tab_pair(c.w[h], vt);
+        else return exp2_ff2<TWOSUM>(pair8<DT>(c, h), mp, EC, tab);
+    };
+    auto wq = [&](const Cols8& c, int h) {
+        if constexpr (TAB) return tab_pair(c.w[h], vt);
+        else return exp2_ff2<TWOSUM>(pair8<DT>(c, h), mq, EC, tab);
+    };
     // one step: 8 consecutive columns k, k + 1, ... of the lane (4 pairs) of the p row, and of the q row
     // for a residual
     auto step = [&](const Cols8& cp, const Cols8& cq, int32_t k) {
         if (RESID) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
-                const ff2 eq = exp2_ff2<TWOSUM>(pair8<DT>(cq, h), mq, EC, tab);
-                const float2 mk = sel_mask(ep, eq, tk.rho);
-                const float2 hp = grid_hi(ep.hi), hq = grid_hi(eq.hi);
+                const ff2 ep = wp(cp, h);
+                const ff2 eq = wq(cq, h);
+                const float2 mk = sel_mask(ep, eq, rho_sel);
+                const float2 hp = grid_hi(ep.hi, Gp), hq = grid_hi(eq.hi, Gq);
                 const float2 lp = add2(sub2(ep.hi, hp), ep.lo), lq = add2(sub2(eq.hi, hq), eq.lo);
                 Ph = add2(Ph, hp);
                 Pl = add2(Pl, lp);
@@ -1378,10 +1482,10 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
         } else if (REMOVED) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
+                const ff2 ep = wp(cp, h);
                 const int bit = k - (cbase + 32 * lane) + 2 * h;
                 const float2 mk = make_float2((lane_rm >> bit) & 1u ? 0.f : 1.f, (lane_rm >> (bit + 1)) & 1u ? 0.f : 1.f);
-                const float2 hp = grid_hi(ep.hi), lp = add2(sub2(ep.hi, hp), ep.lo);
+                const float2 hp = grid_hi(ep.hi, Gp), lp = add2(sub2(ep.hi, hp), ep.lo);
                 Ph = add2(Ph, hp);
                 Pl = add2(Pl, lp);
                 Ah = fma2(mk, hp, Ah);
@@ -1390,8 +1494,8 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
         } else {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                const ff2 ep = exp2_ff2<TWOSUM>(pair8<DT>(cp, h), mp, EC, tab);
-                const float2 hp = grid_hi(ep.hi);
+                const ff2 ep = wp(cp, h);
+                const float2 hp = grid_hi(ep.hi, Gp);
                 Ph = add2(Ph, hp);
                 Pl = add2(Pl, add2(sub2(ep.hi, hp), ep.lo));
             }
@@ -1461,9 +1565,9 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
 
 // Sampler task c: sequence b = c / nS, task i = c % nS. The warp reads the sequence's sampler work
 // (polled), accumulates and stores the task; the warp holding the last task of a sequence then runs
-// its find.
+// its find. vt: the value table (nullptr where the kernel has none).
 template <int DT, bool VEC>
-__device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) {
+__device__ void s_task(const Params& P, uint32_t c, const float* tab, const char* vt, int lane) {
     // c / nS by a multiply-high with floor(2^64 / nS) + 1: exact for c, nS < 2^32 (no MUFU reciprocal)
     const int32_t b = P.nS == 1 ? (int32_t)c : (int32_t)__umul64hi((unsigned long long)c, P.nS_recip);
     const int i = (int)(c - (uint32_t)b * (uint32_t)P.nS);
@@ -1475,8 +1579,6 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
     }
     if (tk.mode == kModeNone) return;
     const size_t prow = (size_t)(o0 + b + tk.n), qrow = (size_t)(o0 + tk.n);
-    // rows whose maximum is near zero carry the rounding of l - m (see exp2_ff2)
-    const bool twosum = fabsf(tk.m_p) < kNeedTwoSum || (tk.mode == kModeResidual && fabsf(tk.m_q) < kNeedTwoSum);
     uint32_t lane_rm = 0;  // the draw's removed columns among this lane's (point-mass and tree residuals)
     if (tk.nrm) {          // warp-uniform
         int32_t rtok = -1;
@@ -1486,18 +1588,34 @@ __device__ void s_task(const Params& P, uint32_t c, const float* tab, int lane) 
         }
         lane_rm = removed_bits(rtok, tk.nrm, i * kSTask + 32 * lane, 32);
     }
-    if (__any_sync(0xFFFFFFFFu, lane_rm != 0u)) {
-        if (twosum) s_accumulate<DT, VEC, true, true, false>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
-        else s_accumulate<DT, VEC, false, true, false>(P, b, i, tk, prow, qrow, tab, lane, lane_rm);
-    } else if (tk.mode == kModeResidual) {
-        if (twosum) s_accumulate<DT, VEC, true, false, true>(P, b, i, tk, prow, qrow, tab, lane, 0u);
-        else s_accumulate<DT, VEC, false, false, true>(P, b, i, tk, prow, qrow, tab, lane, 0u);
-    } else if (twosum) {
-        s_accumulate<DT, VEC, true, false, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
-    } else {
-        s_accumulate<DT, VEC, false, false, false>(P, b, i, tk, prow, qrow, tab, lane, 0u);
+    const bool rm = __any_sync(0xFFFFFFFFu, lane_rm != 0u);
+    const bool res = tk.mode == kModeResidual;
+    if constexpr (DT == SV_BF16 && VEC) {
+        if (vt && draw_uses_table<DT, VEC>(P, tk.mode, tk.m_p, tk.m_q)) {
+            // value-table weights 2^(l K): below 2^(m K) in each row, which sets the grid constant
+            const float Gp = grid_const(tk.m_p * P.K_hi), Gq = res ? grid_const(tk.m_q * P.K_hi) : 12.f;
+            if (rm) s_accumulate<DT, VEC, false, true, false, true>(P, b, i, tk, prow, qrow, tab, vt, lane, lane_rm, Gp, Gq, tk.rho);
+            else if (res) s_accumulate<DT, VEC, false, false, true, true>(P, b, i, tk, prow, qrow, tab, vt, lane, 0u, Gp, Gq, tk.rho);
+            else s_accumulate<DT, VEC, false, false, false, true>(P, b, i, tk, prow, qrow, tab, vt, lane, 0u, Gp, Gq, tk.rho);
+            if (i == P.nS - 1) find<DT, VEC, true>(P, b, tk, prow, qrow, o0, tab, vt, lane);
+            return;
+        }
     }
-    if (i == P.nS - 1) find<DT, VEC>(P, b, tk, prow, qrow, o0, tab, lane);
+    // precise-exponential weights 2^((l - m) K) <= 1; rows whose maximum is near zero carry the rounding of
+    // l - m (see exp2_ff2)
+    const bool twosum = fabsf(tk.m_p) < kNeedTwoSum || (res && fabsf(tk.m_q) < kNeedTwoSum);
+    if (rm) {
+        if (twosum) s_accumulate<DT, VEC, true, true, false, false>(P, b, i, tk, prow, qrow, tab, vt, lane, lane_rm, 12.f, 12.f, tk.rho);
+        else s_accumulate<DT, VEC, false, true, false, false>(P, b, i, tk, prow, qrow, tab, vt, lane, lane_rm, 12.f, 12.f, tk.rho);
+    } else if (res) {
+        if (twosum) s_accumulate<DT, VEC, true, false, true, false>(P, b, i, tk, prow, qrow, tab, vt, lane, 0u, 12.f, 12.f, tk.rho);
+        else s_accumulate<DT, VEC, false, false, true, false>(P, b, i, tk, prow, qrow, tab, vt, lane, 0u, 12.f, 12.f, tk.rho);
+    } else if (twosum) {
+        s_accumulate<DT, VEC, true, false, false, false>(P, b, i, tk, prow, qrow, tab, vt, lane, 0u, 12.f, 12.f, tk.rho);
+    } else {
+        s_accumulate<DT, VEC, false, false, false, false>(P, b, i, tk, prow, qrow, tab, vt, lane, 0u, 12.f, 12.f, tk.rho);
+    }
+    if (i == P.nS - 1) find<DT, VEC, false>(P, b, tk, prow, qrow, o0, tab, vt, lane);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1563,7 +1681,7 @@ __device__ __forceinline__ void a_finish(const Params& P, const ATask& at, const
 
 // Decision of sequence b, run by its decider warp (or, cooperative, by the CTA's deciding warps); the
 // deciding warps poll the partial words themselves.
-template <int DT, bool GREEDY>
+template <int DT, bool VEC, bool GREEDY>
 __device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, const float* tab, int lane, int wsub,
                             int nsub, CoopRows* co, int set) {
     int32_t o0, g;
@@ -1575,7 +1693,7 @@ __device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, co
         o0 = __ldg(P.offs + b);
         g = __ldg(P.gammas + b);
     }
-    decide<DT, GREEDY>(P, b, g, o0, lane, tab, wsub, nsub, co, set);
+    decide<DT, VEC, GREEDY>(P, b, g, o0, lane, tab, wsub, nsub, co, set);
 }
 
 // A streamer warp on the bulk-copy path: its statistics tasks (statically strided over all streamers)
@@ -1649,7 +1767,12 @@ __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, 
         at.r = (int32_t)rp;
         at.ch = (int32_t)cp;
         at.len = len_of(cp);
-        const SegStats st = stats_bf16_smem(bufs + (size_t)s * kStageBytes, at.len, lane, P.K_hi);
+        // the stage is refilled only once its task is reduced: with one copy per streamer in flight during
+        // the reduction the stream keeps HBM busy without queueing the handoff loads of the decisions and
+        // finds behind it (refilling right after the stage is read into registers measured slower)
+        uint4 v[16];
+        load_stage(bufs + (size_t)s * kStageBytes, at.len, lane, v);
+        const SegStats st = stats_bf16(v, P.K_hi);
         __syncwarp();
         if (lane == 0 && tn < nA) {
             fence_proxy_async_smem();  // this stage's reads come before the copy that overwrites it
@@ -1664,7 +1787,7 @@ __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, 
 // The kernel
 // ------------------------------------------------------------------------------------------------
 template <int DT, bool VEC, bool GREEDY>
-__global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kThreads, 1) k_verify(const __grid_constant__ Params P) {
     constexpr bool kBulk = DT == SV_BF16 && VEC && !GREEDY;
     extern __shared__ __align__(128) unsigned char dsmem[];
     __shared__ float tab[2 * kExpTab];
@@ -1715,10 +1838,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     const int32_t* rows = !GREEDY && !P.pm && 2 * oB + P.B <= kRowCache ? s_row : nullptr;
 
     // Statistics. Bulk-copy path: the upper kStreamWarps warps of the CTA stream while the lower ones
-    // decide and take sampler tasks at once. Other paths: every warp streams its strided tasks from
-    // registers first.
+    // build the sampler's value table, then decide and take sampler tasks. Other paths: every warp streams
+    // its strided tasks from registers first.
+    // The value table is built by the non-streaming warps, which wait for one another (named barrier 2)
+    // and then only signal barrier 3; a streamer waits on barrier 3 once its stream is done, before its
+    // first sampler task (by then the table is long finished).
+    const char* vt = kBulk ? reinterpret_cast<const char*>(dsmem + kTabSmemOffset) : nullptr;
+    constexpr int kBuilders = (kWarps - kStreamWarps) * 32;
     if (kBulk) {
-        if (warp >= kWarps - kStreamWarps) stream_bulk(P, nA, dsmem, bases, rows, warp - (kWarps - kStreamWarps), lane);
+        if (warp >= kWarps - kStreamWarps) {
+            stream_bulk(P, nA, dsmem, bases, rows, warp - (kWarps - kStreamWarps), lane);
+            asm volatile("bar.sync 3, %0;" ::"r"(kThreads) : "memory");
+        } else {
+            build_value_table(P, reinterpret_cast<float2*>(dsmem + kTabSmemOffset), tab, tid, kBuilders);
+            asm volatile("bar.sync 2, %0;" ::"r"(kBuilders) : "memory");
+            asm volatile("bar.arrive 3, %0;" ::"r"(kThreads) : "memory");
+        }
     } else {
         const uint32_t W = gridDim.x * kWarps;
         int32_t cur = 0;
@@ -1747,9 +1882,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
     const bool coop = kBulk && (uint32_t)P.B <= gridDim.x;
     if (coop) {
         if (!streamer && blockIdx.x < (uint32_t)P.B)
-            lead_decide<DT, GREEDY>(P, (int32_t)blockIdx.x, bases, tab, lane, warp, kWarps - kStreamWarps, &s_coop, 0);
+            lead_decide<DT, VEC, GREEDY>(P, (int32_t)blockIdx.x, bases, tab, lane, warp, kWarps - kStreamWarps, &s_coop, 0);
     } else if (!streamer) {
-        for (uint32_t b = did; b < (uint32_t)P.B; b += ND) lead_decide<DT, GREEDY>(P, (int32_t)b, bases, tab, lane, 0, 1, &s_coop, 0);
+        for (uint32_t b = did; b < (uint32_t)P.B; b += ND) lead_decide<DT, VEC, GREEDY>(P, (int32_t)b, bases, tab, lane, 0, 1, &s_coop, 0);
     }
     if constexpr (!GREEDY) {
         while (true) {
@@ -1757,7 +1892,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_verify(const __grid_constant__ 
             if (lane == 0) t = atomicAdd(&P.ctr->claim, 1u);
             t = __shfl_sync(0xFFFFFFFFu, t, 0);
             if (t >= nStot) break;
-            s_task<DT, VEC>(P, t, tab, lane);
+            s_task<DT, VEC>(P, t, tab, vt, lane);
         }
     }
 }
@@ -1837,7 +1972,7 @@ __global__ void __launch_bounds__(256) k_debug_beta(const __grid_constant__ Para
 template <int DT, bool VEC, bool GREEDY>
 static cudaError_t launch_typed(const Params& P, cudaStream_t st) {
     constexpr bool kBulk = DT == SV_BF16 && VEC && !GREEDY;
-    constexpr int smem = kBulk ? kTmaSmemBytes : 0;
+    constexpr int smem = kBulk ? kTabSmemOffset + kTabBytes : 0;  // stages, their barriers, the value table
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
