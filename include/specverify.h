@@ -282,6 +282,64 @@ int spec_verify_tree(const void* target_logits, sv_dtype dtype, const int32_t* d
                      int32_t* out_path, uint32_t* device_status, void* workspace, size_t workspace_bytes,
                      void* cuda_stream);
 
+/*
+ * Vocabulary-sharded verify ("All About Transformer Inference", the model-parallel sections: the logits
+ * come out of an unembedding sharded over the vocabulary across tensor-parallel ranks; "Accelerating Sonar
+ * through speculation", the tensor-parallel scheduling section). Shard j of S holds columns
+ * [bounds[j], bounds[j+1]) of every target and draft row as its own row-major arrays of
+ * Vs = bounds[j+1] - bounds[j] columns (bounds[0] = 0, bounds[S] = V, S <= 8). The step is the
+ * unsharded one (same rule, same uniforms, same outputs up to the rounding order of the sums), run as
+ * four calls per shard with three exchanges between the shards (all-gathers over the tensor-parallel
+ * group; a caller running the shards in one process concatenates the records instead):
+ *   1. spec_shard_stats   per row, the statistics of the shard's slice      -> sv_shard_partial[rows]
+ *      exchange 1: all-gather the partials into [S][rows] (rows = R_t + R_d, targets first; R_t alone
+ *      in greedy mode or with point-mass drafts)
+ *   2. spec_shard_decide  the merged statistics, the accept tests and the first rejection (every shard
+ *      computes the same): writes out_num_accepted, the accepted tokens and -1 past the emitting slot
+ *      (greedy: the whole output), and each sequence's draw           -> sv_shard_draw[B]
+ *   3. spec_shard_sums    per sequence, the draw's exact sums over the slice -> 4 float pairs [B][4]
+ *      exchange 2: all-gather the sums into [S][B][4]
+ *   4. spec_shard_finish  the shard holding the draw's target u S scans its slice and writes the drawn
+ *      token (a global column) at the emitting slot; every other shard writes -1 there
+ *      exchange 3: element-wise max of out_tokens over the shards (the drawn slot); every other entry is
+ *      the same on all shards.
+ * All arrays are DEVICE pointers owned by the caller: partial and draw arrays 16-byte aligned, the rest
+ * 4-byte aligned. draft_tokens, seq_offsets and gammas are the unsharded batch's, identical on every
+ * shard; shard_draft is NULL in greedy mode or for point-mass drafts (then point_mass = 1 at T > 0).
+ * Data errors go to *device_status as in spec_verify_ex (pass the same word to stats and decide; a bad
+ * CSR structure fails every sequence). Each call is asynchronous on cuda_stream; returns
+ * SV_ERR_INVALID_ARG for bad scalars or pointers, SV_ERR_CUDA if a launch fails, else SV_OK.
+ */
+typedef struct {
+    float m;     /* raw maximum of the slice's logits (NaN: a NaN or +inf logit in the slice) */
+    float s;     /* sum over the slice of 2^((l - m) log2(e) / T) (sampling) */
+    int32_t arg; /* first argmax of the slice as a global column, -1 if none */
+    float g;     /* the logit at the row's draft token if this shard holds that column, else 0 */
+} sv_shard_partial;
+
+typedef struct {
+    int32_t words[8]; /* one sequence's draw (mode, emitting slot, row maxima, ratio, uniform), opaque */
+} sv_shard_draw;
+
+int spec_shard_stats(const void* shard_target, const void* shard_draft, sv_dtype dtype, const int32_t* draft_tokens,
+                     const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, int32_t v0, int32_t Vs,
+                     int32_t max_gamma, float temperature, void* partials, uint32_t* device_status, void* cuda_stream);
+
+/* shard_bounds_host: a HOST array of S + 1 columns (see above). */
+int spec_shard_decide(const void* all_partials, int32_t S, const int32_t* shard_bounds_host, const int32_t* draft_tokens,
+                      const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V, int32_t max_gamma,
+                      float temperature, int32_t point_mass, uint64_t seed, uint64_t step, int32_t* out_tokens,
+                      int32_t* out_num_accepted, void* draws, uint32_t* device_status, void* cuda_stream);
+
+int spec_shard_sums(const void* shard_target, const void* shard_draft, sv_dtype dtype, int32_t v0, int32_t Vs,
+                    const void* draws, const int32_t* seq_offsets, int32_t B, int32_t V, float temperature, void* sums,
+                    void* cuda_stream);
+
+int spec_shard_finish(int32_t shard, int32_t S, const int32_t* shard_bounds_host, const void* shard_target,
+                      const void* shard_draft, sv_dtype dtype, const void* draws, const void* all_sums,
+                      const int32_t* seq_offsets, int32_t B, int32_t V, float temperature, int32_t* out_tokens,
+                      void* cuda_stream);
+
 /* Map a device status word (OR of 1u << code) to one status code, by the priority above. */
 int spec_verify_status_from_bits(uint32_t bits);
 

@@ -134,6 +134,46 @@ struct Params {
     float2 exp2_tab[128];  // 2^(j/128), j = 0..127, as (hi, lo) floats, built on the host
 };
 
+// Vocabulary-sharded verify (sv_shard.cu): one shard's view of the step.
+struct ShardPartial {  // per row and shard, 16 bytes (sv_shard_partial in the C ABI)
+    float m;           // raw max of the slice (NaN: a NaN or +inf logit in the slice)
+    float s;           // sum over the slice of 2^((l - m) K) (sampling)
+    int32_t arg;       // first argmax of the slice as a global column (-1: none)
+    float g;           // the logit at the row's draft token when this shard holds that column, else 0
+};
+struct ShardDraw {     // per sequence, 32 bytes (sv_shard_draw in the C ABI)
+    int32_t mode, n;   // kMode*, the emitting slot
+    float m_p, m_q;    // merged raw maxima of the draw's target and draft rows
+    float rho;         // selection ratio s_p / s_q (approximate)
+    float u;           // the draw's uniform
+    int32_t xcl;       // point-mass residual: the removed column (global), else -1
+    int32_t pad;
+};
+constexpr int kMaxShards = 8;
+struct ShardArgs {
+    const void* target;   // this shard's slice of the target rows, [R_t, Vs]
+    const void* draft;    // this shard's slice of the draft rows, [R_d, Vs] (nullptr: greedy or point-mass)
+    int32_t dtype;
+    const int32_t* tokens;
+    const int32_t* offs;
+    const int32_t* gammas;
+    int32_t B, V, Vs, v0, max_gamma;
+    int32_t S, shard;               // shard count and this shard's index
+    int32_t bounds[kMaxShards + 1]; // first column of each shard, V last
+    int32_t greedy, pm;
+    float K_hi, K_lo, d_min;
+    uint64_t seed, step;
+    int32_t* out_tokens;
+    int32_t* out_n;
+    uint32_t* status;
+    int32_t nrows;                  // grid of the statistics kernel (an upper bound of the rows)
+    cudaStream_t stream;
+    float2 exp2_tab[128];
+};
+// stage 0: statistics (a = partials of this shard); 1: decisions (a = all partials, b = draws);
+// 2: sums (a = draws, b = this shard's sums); 3: finish (a = draws, b = all sums)
+cudaError_t launch_shard(int stage, const ShardArgs& A, void* a, void* b, void* c);
+
 struct Layout {
     size_t counters, partials, taskw, recw, groupw, remw, pathw, seqstate, status;
     size_t zero_begin, zero_end;  // byte range the launch sequence clears

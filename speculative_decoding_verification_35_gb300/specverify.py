@@ -20,6 +20,7 @@ SV_MAX_GAMMA = 31
 # every exported symbol of the C ABI, in header order
 EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
            "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
+           "spec_shard_stats", "spec_shard_decide", "spec_shard_sums", "spec_shard_finish",
            "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host")
 
 
@@ -64,6 +65,14 @@ def _load():
     L.spec_verify_host.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
                                    ctypes.POINTER(SvDeviceBuffers), vp, vp, sz, vp]
     L.spec_verify_host.restype = ctypes.c_int
+    L.spec_shard_stats.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp]
+    L.spec_shard_stats.restype = ctypes.c_int
+    L.spec_shard_decide.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, i32, u64, u64, vp, vp, vp, vp, vp]
+    L.spec_shard_decide.restype = ctypes.c_int
+    L.spec_shard_sums.argtypes = [vp, vp, ctypes.c_int, i32, i32, vp, vp, i32, i32, f32, vp, vp]
+    L.spec_shard_sums.restype = ctypes.c_int
+    L.spec_shard_finish.argtypes = [i32, i32, vp, vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, f32, vp, vp]
+    L.spec_shard_finish.restype = ctypes.c_int
     L.spec_verify_status_from_bits.argtypes = [ctypes.c_uint32]
     L.spec_verify_status_from_bits.restype = ctypes.c_int
     L.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -147,6 +156,37 @@ def spec_verify_host(target_logits, draft_logits, dtype, draft_tokens, seq_offse
                                 max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
                                 ctypes.byref(dev) if dev is not None else None, device_status, workspace,
                                 workspace_bytes, cuda_stream)
+
+
+def spec_shard_stats(shard_target, shard_draft, dtype, draft_tokens, seq_offsets, gammas, B, V, v0, Vs, max_gamma,
+                     temperature, partials, device_status, cuda_stream) -> int:
+    """Per-row statistics of one vocabulary shard's slice. Pointer arguments are device addresses."""
+    return lib.spec_shard_stats(shard_target, shard_draft, dtype, draft_tokens, seq_offsets, gammas, B, V, v0, Vs,
+                                max_gamma, float(temperature), partials, device_status, cuda_stream)
+
+
+def spec_shard_decide(all_partials, S, bounds, draft_tokens, seq_offsets, gammas, B, V, max_gamma, temperature,
+                      point_mass, seed, step, out_tokens, out_num_accepted, draws, device_status, cuda_stream) -> int:
+    """Decisions from the gathered partials; `bounds` is a host sequence of S + 1 columns."""
+    hb = (ctypes.c_int32 * (S + 1))(*[int(v) for v in bounds])
+    return lib.spec_shard_decide(all_partials, S, hb, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                                 float(temperature), int(point_mass), seed, step, out_tokens, out_num_accepted, draws,
+                                 device_status, cuda_stream)
+
+
+def spec_shard_sums(shard_target, shard_draft, dtype, v0, Vs, draws, seq_offsets, B, V, temperature, sums,
+                    cuda_stream) -> int:
+    """The draws' exact sums over one shard's slice."""
+    return lib.spec_shard_sums(shard_target, shard_draft, dtype, v0, Vs, draws, seq_offsets, B, V, float(temperature),
+                               sums, cuda_stream)
+
+
+def spec_shard_finish(shard, S, bounds, shard_target, shard_draft, dtype, draws, all_sums, seq_offsets, B, V,
+                      temperature, out_tokens, cuda_stream) -> int:
+    """The drawn tokens from the gathered sums (written by the owning shard, -1 elsewhere)."""
+    hb = (ctypes.c_int32 * (S + 1))(*[int(v) for v in bounds])
+    return lib.spec_shard_finish(shard, S, hb, shard_target, shard_draft, dtype, draws, all_sums, seq_offsets, B, V,
+                                 float(temperature), out_tokens, cuda_stream)
 
 
 def spec_verify_status_from_bits(bits: int) -> int:

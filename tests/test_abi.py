@@ -30,7 +30,8 @@ def test_header_declares_the_api():
     names = declared_functions()
     assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
                           "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
-                          "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host"}
+                          "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host",
+                          "spec_shard_stats", "spec_shard_decide", "spec_shard_sums", "spec_shard_finish"}
 
 
 def test_library_exports_every_declared_symbol(libpath):
@@ -173,6 +174,44 @@ def test_tree_host_side_checks_without_gpu(libpath):
     assert call(out_path=fake + 1) == sv.SV_ERR_INVALID_ARG
     assert call(max_gamma=32) == sv.SV_ERR_INVALID_ARG
     assert call(workspace=None) == sv.SV_ERR_WORKSPACE
+
+
+def test_shard_host_side_checks_without_gpu(libpath):
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    fake = 1 << 20  # never dereferenced: every call below fails its host checks first
+    st = dict(shard_target=fake, shard_draft=fake, dtype=sv.SV_BF16, draft_tokens=fake, seq_offsets=fake, gammas=fake,
+              B=4, V=100, v0=50, Vs=50, max_gamma=4, temperature=1.0, partials=fake, device_status=fake,
+              cuda_stream=None)
+
+    def stats(**kw):
+        a = dict(st); a.update(kw)
+        return sv.spec_shard_stats(**a)
+
+    assert stats(v0=60) == sv.SV_ERR_INVALID_ARG          # slice past V
+    assert stats(Vs=0) == sv.SV_ERR_INVALID_ARG
+    assert stats(partials=fake + 8) == sv.SV_ERR_INVALID_ARG  # records 16-byte aligned
+    assert stats(temperature=-1.0) == sv.SV_ERR_INVALID_ARG
+    assert stats(max_gamma=32) == sv.SV_ERR_INVALID_ARG
+    assert stats(B=0) == sv.SV_OK
+    dc = dict(all_partials=fake, S=2, bounds=[0, 50, 100], draft_tokens=fake, seq_offsets=fake, gammas=fake, B=4,
+              V=100, max_gamma=4, temperature=1.0, point_mass=0, seed=1, step=0, out_tokens=fake,
+              out_num_accepted=fake, draws=fake, device_status=fake, cuda_stream=None)
+
+    def decide(**kw):
+        a = dict(dc); a.update(kw)
+        return sv.spec_shard_decide(**a)
+
+    assert decide(bounds=[0, 50, 99]) == sv.SV_ERR_INVALID_ARG   # last bound must be V
+    assert decide(bounds=[0, 60, 50]) == sv.SV_ERR_INVALID_ARG   # bounds increase
+    assert decide(S=9, bounds=list(range(0, 99, 11)) + [100]) == sv.SV_ERR_INVALID_ARG  # at most 8 shards
+    assert decide(draws=fake + 4) == sv.SV_ERR_INVALID_ARG
+    assert decide(B=0) == sv.SV_OK
+    assert sv.spec_shard_sums(fake, fake, sv.SV_BF16, 90, 20, fake, fake, 4, 100, 1.0, fake, None) == \
+        sv.SV_ERR_INVALID_ARG
+    assert sv.spec_shard_finish(2, 2, [0, 50, 100], fake, fake, sv.SV_BF16, fake, fake, fake, 4, 100, 1.0, fake,
+                                None) == sv.SV_ERR_INVALID_ARG  # shard index past S
+    assert sv.spec_shard_finish(0, 2, [0, 50, 100], fake, fake, sv.SV_BF16, fake, fake, fake, 4, 100, 0.0, fake,
+                                None) == sv.SV_OK  # greedy: nothing to finish
 
 
 def test_host_buffer_form_checks_without_gpu(libpath):
