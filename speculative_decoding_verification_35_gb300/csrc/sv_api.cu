@@ -105,6 +105,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     // keep its sums finite: m <= 63.75 (no logit above the table), m >= -63.75 + 60 / K (every logit at
     // or below -63.75, taken as weight 0, lies 2^60 below the row's largest weight) and m K <= 96 (sums of
     // up to 2^31 weights of at most 2^96 stay finite).
+    P.use_tab = !greedy && (int64_t)B * P.nS >= kTabMinTasks;
     P.tab_mlo = greedy ? 1.f : (float)(-63.75 + 60.0 / (double)K_hi);
     P.tab_mhi = greedy ? 0.f : (float)std::min(63.75, 96.0 / (double)K_hi);
     P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;

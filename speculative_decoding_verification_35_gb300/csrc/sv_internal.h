@@ -36,6 +36,9 @@ constexpr uint32_t kTabCodeHi = 0x427Fu;    // bf16 code of 63.75
 constexpr int kTabHalf = 4096;              // entries per sign
 constexpr int kTabBytes = 2 * kTabHalf * 8; // 64 KB
 constexpr int kTabSmemOffset = (kTmaSmemBytes + 15) & ~15;  // after the stages and their barriers
+constexpr int kTabMinTasks = 2048;  // sampler tasks (sequences x 1024-column tasks) from which a call builds
+                                    // the table: below, its build (~4 us at the launch's start) would sit on
+                                    // the step's critical path instead of under the stream
 constexpr int kBaseCache = 1024;            // batches up to this size keep their row bases in shared memory
 constexpr int kRowCache = 2048;             // sampling batches with up to this many statistics rows keep a
                                             // row map (target or draft, row index) in shared memory
@@ -105,6 +108,7 @@ struct Params {
     unsigned long long nS_recip;  // floor(2^64 / nS) + 1 (nS >= 2): c / nS = high 64 bits of c * nS_recip
     float K_hi, K_lo;  // log2(e) / T as float-float
     float d_min;       // clamp of l - m in the precise exponential (about -126.5 / K)
+    int32_t use_tab;         // the CTAs build the value table (batches with enough sampler work, bf16 rows)
     float tab_mlo, tab_mhi;  // a draw uses the value table when its rows' raw maxima lie in [tab_mlo, tab_mhi]
     uint32_t spin;     // polls before a wait on another warp's word gives up (kSpinLimit unless a caller
                        // testing the time-out path asks for fewer)

@@ -438,7 +438,7 @@ __device__ __noinline__ void give_up_seq(const Params& P, int32_t b, int lane) {
 // and its find agree.
 template <int DT, bool VEC>
 __device__ __forceinline__ bool draw_uses_table(const Params& P, int32_t mode, float m_p, float m_q) {
-    if (!(DT == SV_BF16 && VEC)) return false;
+    if (!(DT == SV_BF16 && VEC) || !P.use_tab) return false;
     auto ok = [&](float m) { return m >= P.tab_mlo && m <= P.tab_mhi; };
     return ok(m_p) && (mode != kModeResidual || ok(m_q));
 }
@@ -1843,13 +1843,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_verify(const __grid_constant__ 
     // The value table is built by the non-streaming warps, which wait for one another (named barrier 2)
     // and then only signal barrier 3; a streamer waits on barrier 3 once its stream is done, before its
     // first sampler task (by then the table is long finished).
-    const char* vt = kBulk ? reinterpret_cast<const char*>(dsmem + kTabSmemOffset) : nullptr;
+    const bool use_tab = kBulk && P.use_tab;
+    const char* vt = use_tab ? reinterpret_cast<const char*>(dsmem + kTabSmemOffset) : nullptr;
     constexpr int kBuilders = (kWarps - kStreamWarps) * 32;
     if (kBulk) {
         if (warp >= kWarps - kStreamWarps) {
             stream_bulk(P, nA, dsmem, bases, rows, warp - (kWarps - kStreamWarps), lane);
-            asm volatile("bar.sync 3, %0;" ::"r"(kThreads) : "memory");
-        } else {
+            if (use_tab) asm volatile("bar.sync 3, %0;" ::"r"(kThreads) : "memory");
+        } else if (use_tab) {
             build_value_table(P, reinterpret_cast<float2*>(dsmem + kTabSmemOffset), tab, tid, kBuilders);
             asm volatile("bar.sync 2, %0;" ::"r"(kBuilders) : "memory");
             asm volatile("bar.arrive 3, %0;" ::"r"(kThreads) : "memory");
