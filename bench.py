@@ -503,7 +503,7 @@ def main():
     out_n_host = torch.empty(b.B, dtype=torch.int32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = out_t_host.numel() * 4 + out_n_host.numel() * 4
-    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    n_e2e = max(1, args.e2e_steps)  # its own step count: a few ms of copies, independent of --steps
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
