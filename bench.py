@@ -654,6 +654,45 @@ def main():
     rig.check_status("the tree steps")
     del t_tg
 
+    # vocabulary-sharded verify (spec_shard_*): the headline batch split over S shards held by this process
+    # on this one GPU, each shard's four calls in turn and the exchanges as stacks of the shards' records
+    # (the protocol a tensor-parallel group runs over NCCL); a single-GPU figure, not a multi-GPU one
+    sharded = None
+    if world == 1:
+        from speculative_decoding_verification_35_gb300.shard import CudaShard, local_steps
+        sharded = {}
+        c0d = rig.copies[0]
+        for S in (2, 4):
+            bounds = [b.V * j // S for j in range(S + 1)]
+            shards = [CudaShard(j, bounds, c0d["target"][:, bounds[j]:bounds[j + 1]].contiguous(),
+                                c0d["draft"][:, bounds[j]:bounds[j + 1]].contiguous() if c0d["draft"] is not None else None,
+                                c0d["draft_tokens"], c0d["seq_offsets"], c0d["gammas"], b.B, b.V, rig.mg, b.R_t, b.R_d,
+                                w.temperature) for j in range(S)]
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    local_steps(shards, rig.seed, i)
+            stream.synchronize()
+            n_sh = 20  # steps per graph (the calls and the exchanges' stacks, captured once)
+            sgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(sgraph, stream=stream):
+                for i in range(n_sh):
+                    local_steps(shards, rig.seed, 3 + i)
+            rig.replay(sgraph)
+            stream.synchronize()
+            s0, s1 = rig.event(), rig.event()
+            s0.record(stream)
+            rig.replay(sgraph, 5)
+            s1.record(stream)
+            stream.synchronize()
+            n_sh *= 5
+            if any(int(sh.status.item()) for sh in shards):
+                raise RuntimeError("device status bits set by the sharded steps")
+            sharded[f"S{S}"] = {"ms_per_step": s0.elapsed_time(s1) / n_sh, "steps": n_sh, "shards": S}
+            del shards
+        sharded["launch"] = ("per step and shard: statistics, decisions, sums, finish (4 launches), the records "
+                             "stacked between them; shards run in turn on one GPU, inputs resident (one copy); "
+                             "replayed from a CUDA graph of 20 steps")
+
     rows = b.verified_rows()
     value = rows * world / (ms * 1e-3)
     e2e_value = rows * world / (ms_e2e * 1e-3)
@@ -706,6 +745,7 @@ def main():
             "tree_verify": {"ms_per_call": ms_tree, "calls": n_tree, "B": tb.B, "nodes": tb.R_t, "V": tb.V,
                             "rows_per_s": tb.R_t / (ms_tree * 1e-3),
                             "launch": f"spec_verify_tree, stream-ordered, {t_ncopy} rotating input copies"},
+            "vocab_sharded_verify": sharded,
             "ngram_drafter": {"us_per_call": us_ngram, "calls": n_ng, "B": b.B, "history_tokens": ng_len,
                               "n": "4..1", "gamma_max": ng_g,
                               "launch": "spec_draft_ngram: search (one CTA per sequence) + pack (one CTA)"},

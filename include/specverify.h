@@ -297,19 +297,24 @@ int spec_verify_tree(const void* target_logits, sv_dtype dtype, const int32_t* d
  *   2. spec_shard_decide  the merged statistics, the accept tests and the first rejection (every shard
  *      computes the same): writes out_num_accepted, the accepted tokens and -1 past the emitting slot
  *      (greedy: the whole output), and each sequence's draw           -> sv_shard_draw[B]
- *   3. spec_shard_sums    per sequence, the draw's exact sums over the slice -> 4 float pairs [B][4]
- *      exchange 2: all-gather the sums into [S][B][4]
- *   4. spec_shard_finish  the shard holding the draw's target u S scans its slice and writes the drawn
- *      token (a global column) at the emitting slot; every other shard writes -1 there
+ *   3. spec_shard_sums    per sequence and SV_SHARD_CHUNK-column chunk of the slice, the draw's exact
+ *      sums (4 float pairs)                                           -> float[B][NC][4][2]
+ *      exchange 2: all-gather the sums into [S][B][NC][4][2]; NC = spec_shard_chunks(S, bounds), the
+ *      chunk count of the widest shard (a narrower shard's records past its slice are zero)
+ *   4. spec_shard_finish  the (shard, chunk) holding the draw's target u S, found from the gathered sums;
+ *      that shard scans the chunk and writes the drawn token (a global column) at the emitting slot,
+ *      every other shard writes -1 there
  *      exchange 3: element-wise max of out_tokens over the shards (the drawn slot); every other entry is
  *      the same on all shards.
- * All arrays are DEVICE pointers owned by the caller: partial and draw arrays 16-byte aligned, the rest
+ * All arrays are DEVICE pointers owned by the caller: partial, draw and sums arrays 16-byte aligned, the rest
  * 4-byte aligned. draft_tokens, seq_offsets and gammas are the unsharded batch's, identical on every
  * shard; shard_draft is NULL in greedy mode or for point-mass drafts (then point_mass = 1 at T > 0).
  * Data errors go to *device_status as in spec_verify_ex (pass the same word to stats and decide; a bad
  * CSR structure fails every sequence). Each call is asynchronous on cuda_stream; returns
  * SV_ERR_INVALID_ARG for bad scalars or pointers, SV_ERR_CUDA if a launch fails, else SV_OK.
  */
+#define SV_SHARD_CHUNK 8192 /* columns per sums record */
+
 typedef struct {
     float m;     /* raw maximum of the slice's logits (NaN: a NaN or +inf logit in the slice) */
     float s;     /* sum over the slice of 2^((l - m) log2(e) / T) (sampling) */
@@ -331,9 +336,13 @@ int spec_shard_decide(const void* all_partials, int32_t S, const int32_t* shard_
                       float temperature, int32_t point_mass, uint64_t seed, uint64_t step, int32_t* out_tokens,
                       int32_t* out_num_accepted, void* draws, uint32_t* device_status, void* cuda_stream);
 
-int spec_shard_sums(const void* shard_target, const void* shard_draft, sv_dtype dtype, int32_t v0, int32_t Vs,
-                    const void* draws, const int32_t* seq_offsets, int32_t B, int32_t V, float temperature, void* sums,
-                    void* cuda_stream);
+/* Records per sequence and shard in the sums: ceil(max_j (bounds[j+1] - bounds[j]) / SV_SHARD_CHUNK), or 0
+ * for bounds that are not S + 1 increasing columns from 0 with S <= 8 (a host call). */
+int32_t spec_shard_chunks(int32_t S, const int32_t* shard_bounds_host);
+
+int spec_shard_sums(int32_t shard, int32_t S, const int32_t* shard_bounds_host, const void* shard_target,
+                    const void* shard_draft, sv_dtype dtype, const void* draws, const int32_t* seq_offsets, int32_t B,
+                    int32_t V, float temperature, void* sums, void* cuda_stream);
 
 int spec_shard_finish(int32_t shard, int32_t S, const int32_t* shard_bounds_host, const void* shard_target,
                       const void* shard_draft, sv_dtype dtype, const void* draws, const void* all_sums,

@@ -154,6 +154,7 @@ struct ShardDraw {     // per sequence, 32 bytes (sv_shard_draw in the C ABI)
     int32_t pad;
 };
 constexpr int kMaxShards = 8;
+constexpr int kShChunk = 8192;     // columns per sums record (SV_SHARD_CHUNK)
 struct ShardArgs {
     const void* target;   // this shard's slice of the target rows, [R_t, Vs]
     const void* draft;    // this shard's slice of the draft rows, [R_d, Vs] (nullptr: greedy or point-mass)
@@ -171,11 +172,12 @@ struct ShardArgs {
     int32_t* out_n;
     uint32_t* status;
     int32_t nrows;                  // grid of the statistics kernel (an upper bound of the rows)
+    int32_t nc;                     // sums records per sequence and shard: chunks of the widest shard
     cudaStream_t stream;
     float2 exp2_tab[128];
 };
 // stage 0: statistics (a = partials of this shard); 1: decisions (a = all partials, b = draws);
-// 2: sums (a = draws, b = this shard's sums); 3: finish (a = draws, b = all sums)
+// 2: sums (a = draws, b = this shard's per-chunk sums); 3: finish (a = draws, b = all shards' sums)
 cudaError_t launch_shard(int stage, const ShardArgs& A, void* a, void* b, void* c);
 
 struct Layout {

@@ -12,6 +12,7 @@
 //      slice for the drawn column and writes the token, the others -1 -- combined by an element-wise max.
 // The rule is the unsharded verify step's (velog "6-1편. Speculative Decoding", §2-1/§2-2), so the outputs
 // equal the unsharded step's up to the rounding order of the sums.
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 
@@ -31,7 +32,20 @@ __device__ __forceinline__ float lg(const void* base, size_t idx) {
     return __ldg((const float*)base + idx);
 }
 
-// CTA-wide max / sum helpers (kShThreads threads)
+// NaN-propagating maxima (a NaN operand gives NaN)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ __nv_bfloat162 bits_bf162(uint32_t w) {
+    __nv_bfloat162 r;
+    memcpy(&r, &w, sizeof r);
+    return r;
+}
+
+// CTA-wide max / sum helpers over NT threads (every thread gets the result)
+template <int NT>
 __device__ float cta_max(float v, float* red) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -39,9 +53,10 @@ __device__ float cta_max(float v, float* red) {
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
     float t = -INFINITY;
-    for (int w = 0; w < kShThreads / 32; ++w) t = fmaxf(t, red[w]);
+    for (int w = 0; w < NT / 32; ++w) t = fmaxf(t, red[w]);
     return t;
 }
+template <int NT>
 __device__ float cta_sumf(float v, float* red) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -49,9 +64,10 @@ __device__ float cta_sumf(float v, float* red) {
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
     float t = 0.f;
-    for (int w = 0; w < kShThreads / 32; ++w) t += red[w];
+    for (int w = 0; w < NT / 32; ++w) t += red[w];
     return t;
 }
+template <int NT>
 __device__ int cta_min_i(int v, int* red) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -59,19 +75,7 @@ __device__ int cta_min_i(int v, int* red) {
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
     int t = 0x7FFFFFFF;
-    for (int w = 0; w < kShThreads / 32; ++w) t = min(t, red[w]);
-    return t;
-}
-// float-float sum over the CTA (every thread gets the total; summed in warp then warp-index order)
-__device__ ff cta_sum_ff(ff v, ff* red) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1)
-        v = ff_add(v, ff{__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)});
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    ff t{0.f, 0.f};
-    for (int w = 0; w < kShThreads / 32; ++w) t = ff_add(t, red[w]);
+    for (int w = 0; w < NT / 32; ++w) t = min(t, red[w]);
     return t;
 }
 
@@ -99,15 +103,18 @@ __device__ RowRef row_ref(const ShardArgs& A, int32_t r) {
     return R;
 }
 
-// 1. Partial statistics of every row's slice, one CTA per row.
+// 1. Partial statistics of every row's slice, one CTA of kShStatThreads per row (all rows of a headline
+// batch resident in one wave). Each thread keeps its running maximum, its first argmax and its sum of
+// 2^((l - m) K) relative to that maximum, taking its columns in batches (rescaled when a batch raises it).
+constexpr int kShStatThreads = 256;
 template <int DT>
-__global__ void __launch_bounds__(kShThreads) k_shard_stats(const __grid_constant__ ShardArgs A, ShardPartial* out) {
-    __shared__ float redf[kShThreads / 32];
-    __shared__ int redi[kShThreads / 32];
+__global__ void __launch_bounds__(kShStatThreads, 5) k_shard_stats(const __grid_constant__ ShardArgs A, ShardPartial* out) {
+    __shared__ float redf[kShStatThreads / 32];
+    __shared__ int redi[kShStatThreads / 32];
     const int32_t r = (int32_t)blockIdx.x;
     {  // every CTA checks the whole CSR structure before it reads a row (the decisions then fail the batch)
         int bad = threadIdx.x == 0 && __ldg(A.offs) != 0;
-        for (int32_t b = threadIdx.x; b < A.B; b += kShThreads) {
+        for (int32_t b = threadIdx.x; b < A.B; b += kShStatThreads) {
             const int32_t o0 = __ldg(A.offs + b), g = __ldg(A.offs + b + 1) - o0;
             bad |= o0 < 0 || g < 0 || g > A.max_gamma || g != __ldg(A.gammas + b);
         }
@@ -122,21 +129,104 @@ __global__ void __launch_bounds__(kShThreads) k_shard_stats(const __grid_constan
     const RowRef R = row_ref(A, r);
     const void* base = R.draft ? A.draft : A.target;
     const size_t row = (size_t)(R.draft ? r - R_t : r) * (size_t)A.Vs;
-    float m = -INFINITY;
+    float m = -INFINITY, s = 0.f;
     int arg = 0x7FFFFFFF;
-    uint32_t bad = 0;
-    for (int32_t k = threadIdx.x; k < A.Vs; k += kShThreads) {
-        const float l = lg<DT>(base, row + k);
-        bad |= l != l || l == INFINITY;
-        if (l > m) { m = l; arg = k; }
+    bool bad = false;
+    const float K = A.K_hi;
+    // n values x of columns col(i), increasing with i: the batch's maximum (fmax ignores NaN), the first
+    // column attaining it only when it raises the running maximum, and NaN / +inf flagged by one compare
+    auto take = [&](const float* x, int n, auto col) {
+        float bm = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+            bad |= !(x[i] <= FLT_MAX);
+            bm = fmaxf(bm, x[i]);
+        }
+        if (bm > m) {
+            int bi = 0;
+            for (int i = n - 1; i >= 0; --i)
+                if (x[i] == bm) bi = i;
+            if (!A.greedy && m != -INFINITY) s *= ex2_approx((m - bm) * K);
+            m = bm;
+            arg = col(bi);
+        }
+        if (!A.greedy && m != -INFINITY) {
+            const float nmK = -m * K;
+            float s0 = 0.f, s1 = 0.f;
+            for (int i = 0; i + 1 < n; i += 2) {
+                s0 += ex2_approx(__fmaf_rn(x[i], K, nmK));
+                s1 += ex2_approx(__fmaf_rn(x[i + 1], K, nmK));
+            }
+            if (n & 1) s0 += ex2_approx(__fmaf_rn(x[n - 1], K, nmK));
+            s += s0 + s1;
+        }
+    };
+    constexpr int PK = DT == SV_BF16 ? 8 : 4;  // values per 16-byte pack
+    constexpr int NB = 4;                      // packs per batch: p, p + NT, p + 2 NT, p + 3 NT (coalesced)
+    constexpr int NW = 4 * NB;                 // 32-bit words per batch
+    const char* rp = (const char*)base + row * (DT == SV_BF16 ? 2 : 4);
+    const bool vec = (uintptr_t)rp % 16 == 0 && A.Vs % PK == 0;
+    if (vec) {
+        // per batch: a NaN-propagating maximum over the raw words (bf16x2: two values an instruction; a NaN
+        // or +inf anywhere shows in it), the first column attaining it only when it raises the running
+        // maximum, then the sum with packed FMA / ADD and one MUFU ex2 per value
+        const int32_t np = A.Vs / PK;
+        const uint32_t ninf = DT == SV_BF16 ? 0xFF80FF80u : 0xFF800000u;  // -inf fills packs past the row
+        const float2 K2 = f2(K);
+        for (int32_t p = threadIdx.x; p < np; p += NB * kShStatThreads) {
+            uint32_t w[NW];
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const uint4 v = p + u * kShStatThreads < np ? __ldg((const uint4*)rp + p + u * kShStatThreads)
+                                                            : make_uint4(ninf, ninf, ninf, ninf);
+                w[4 * u] = v.x; w[4 * u + 1] = v.y; w[4 * u + 2] = v.z; w[4 * u + 3] = v.w;
+            }
+            float bm;
+            if (DT == SV_BF16) {
+                __nv_bfloat162 mx = bits_bf162(w[0]);
+#pragma unroll
+                for (int i = 1; i < NW; ++i) mx = __hmax2_nan(mx, bits_bf162(w[i]));
+                bm = fmax_nan(__low2float(mx), __high2float(mx));
+            } else {
+                bm = __uint_as_float(w[0]);
+#pragma unroll
+                for (int i = 1; i < NW; ++i) bm = fmax_nan(bm, __uint_as_float(w[i]));
+            }
+            bad |= !(bm <= FLT_MAX);  // NaN or +inf
+            auto val = [&](int i) {
+                return DT == SV_BF16 ? (i & 1 ? bf16hi_to_f32(w[i >> 1]) : bf16lo_to_f32(w[i >> 1]))
+                                     : __uint_as_float(w[i]);
+            };
+            if (bm > m) {
+                int bi = 0;
+#pragma unroll
+                for (int i = NB * PK - 1; i >= 0; --i)
+                    if (val(i) == bm) bi = i;
+                if (!A.greedy && m != -INFINITY) s *= ex2_approx((m - bm) * K);
+                m = bm;
+                arg = (p + (bi / PK) * kShStatThreads) * PK + bi % PK;
+            }
+            if (!A.greedy && m != -INFINITY) {
+                const float2 nmK2 = f2(-m * K);
+                float2 acc = f2(0.f);
+#pragma unroll
+                for (int i = 0; i < NB * PK; i += 2) {
+                    const float2 t = fma2(make_float2(val(i), val(i + 1)), K2, nmK2);
+                    acc = add2(acc, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                }
+                s += acc.x + acc.y;
+            }
+        }
+    } else {
+        for (int32_t k = threadIdx.x; k < A.Vs; k += kShStatThreads) {
+            const float x = lg<DT>(base, row + k);
+            take(&x, 1, [&](int) { return k; });
+        }
     }
-    const float M = cta_max(m, redf);
-    const int A0 = cta_min_i(m == M ? arg : 0x7FFFFFFF, redi);
+    const float M = cta_max<kShStatThreads>(m, redf);
+    const int A0 = cta_min_i<kShStatThreads>(m == M ? arg : 0x7FFFFFFF, redi);
     bad = __syncthreads_or(bad);
-    float s = 0.f;
-    if (!A.greedy && M != -INFINITY && !bad)
-        for (int32_t k = threadIdx.x; k < A.Vs; k += kShThreads) s += exp2f((lg<DT>(base, row + k) - M) * A.K_hi);
-    s = cta_sumf(s, redf);
+    s = cta_sumf<kShStatThreads>(!A.greedy && m != -INFINITY && M != -INFINITY ? s * ex2_approx((m - M) * K) : 0.f,
+                                 redf);
     if (threadIdx.x == 0) {
         ShardPartial p;
         p.m = bad ? __int_as_float(0x7FC00000) : M;
@@ -283,49 +373,128 @@ __device__ __forceinline__ void draw_weights(const ShardArgs& A, const ShardDraw
     sel = resid ? e.hi.x > dw.rho * e.hi.y : !(dw.mode == kModeResidualPM && A.v0 + k == dw.xcl);
 }
 
-// 2b. The draw's sums over this shard's slice, one CTA per sequence: all p weights, all q weights, and those
-// of the selected columns (bonus: every column; point-mass residual: all but the draft token), float-float.
-template <int DT>
-__global__ void __launch_bounds__(kShThreads) k_shard_sums(const __grid_constant__ ShardArgs A, const ShardDraw* draws,
-                                                           ff* sums) {
-    __shared__ float tab[2 * kExpTab];
-    __shared__ ff red[kShThreads / 32];
-    if (threadIdx.x < kExpTab) {
-        tab[threadIdx.x] = A.exp2_tab[threadIdx.x].x;
-        tab[kExpTab + threadIdx.x] = A.exp2_tab[threadIdx.x].y;
+// 2b. The draw's sums over this shard's slice, per 8192-column chunk: one CTA of kShSumThreads per (chunk,
+// sequence), all p weights, all q weights, and those of the selected columns (bonus: every column;
+// point-mass residual: all but the draft token). Thread t takes the column pairs t, t + 256, ... of the
+// chunk (16 pairs): weights <= 1 (relative to the merged maxima) split on the 2^-20 grid, summed exactly
+// (see grid_hi), then float-float across the CTA. Chunks past the slice hold zeros. bf16 rows on 16-byte
+// boundaries are first copied into shared memory (cp.async), so that every load of the chunk is in flight
+// at once; the rest read global memory directly.
+constexpr int kShSumThreads = 256;
+constexpr int kShRecSmem = 256;  // gathered sums records a finishing CTA stages in shared memory (8 KB)
+static_assert(kShChunk == 2 * 16 * kShSumThreads, "16 column pairs per thread and chunk");
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// The accumulation over the thread's column pairs; LOAD(k) gives the logits of columns k, k + 1 of the p
+// and q rows (q: -inf when unused).
+template <bool TWOSUM, typename Load>
+__device__ __forceinline__ void sums_pairs(const ShardArgs& A, const ShardDraw& dw, int32_t c0, int32_t c1,
+                                           const float* tab, Load load, ff (&v)[4]) {
+    const ExpConst EC{A.K_hi, A.K_lo, A.d_min};
+    const bool resid = dw.mode == kModeResidual;
+    float2 Ph = f2(0.f), Pl = f2(0.f), Qh = f2(0.f), Ql = f2(0.f), Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
+    constexpr int NP = kShChunk / (2 * kShSumThreads);
+#pragma unroll 4
+    for (int i = 0; i < NP; ++i) {
+        const int32_t k = c0 + 2 * (int32_t)threadIdx.x + i * 2 * kShSumThreads;
+        if (k >= c1) break;
+        float2 lp, lq;
+        load(k, lp, lq);
+        const ff2 ep = exp2_ff2<TWOSUM>(lp, f2(dw.m_p), EC, tab);
+        const ff2 eq = resid ? exp2_ff2<TWOSUM>(lq, f2(dw.m_q), EC, tab) : ff2{f2(0.f), f2(0.f)};
+        float2 mk;
+        if (resid) mk = make_float2(gt_mask(ep.hi.x, dw.rho * eq.hi.x), gt_mask(ep.hi.y, dw.rho * eq.hi.y));
+        else mk = make_float2(A.v0 + k == dw.xcl ? 0.f : 1.f, A.v0 + k + 1 == dw.xcl ? 0.f : 1.f);
+        const float2 hp = grid_hi(ep.hi), lpw = add2(sub2(ep.hi, hp), ep.lo);
+        const float2 hq = grid_hi(eq.hi), lqw = add2(sub2(eq.hi, hq), eq.lo);
+        Ph = add2(Ph, hp); Pl = add2(Pl, lpw); Qh = add2(Qh, hq); Ql = add2(Ql, lqw);
+        Ah = fma2(mk, hp, Ah); Al = fma2(mk, lpw, Al); Bh = fma2(mk, hq, Bh); Bl = fma2(mk, lqw, Bl);
     }
-    __syncthreads();
-    const int32_t b = (int32_t)blockIdx.x;
+    v[0] = ff_add(ff{Ph.x, Pl.x}, ff{Ph.y, Pl.y});
+    v[1] = ff_add(ff{Qh.x, Ql.x}, ff{Qh.y, Ql.y});
+    v[2] = ff_add(ff{Ah.x, Al.x}, ff{Ah.y, Al.y});
+    v[3] = ff_add(ff{Bh.x, Bl.x}, ff{Bh.y, Bl.y});
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kShSumThreads, 3) k_shard_sums(const __grid_constant__ ShardArgs A,
+                                                                 const ShardDraw* draws, ff* sums) {
+    __shared__ float tab[2 * kExpTab];
+    __shared__ ff red[4][kShSumThreads / 32];
+    __shared__ __align__(16) uint32_t stage[2][kShChunk / 2];  // the chunk's p and q rows as bf16 pairs
+    const int32_t b = (int32_t)(blockIdx.x / (uint32_t)A.nc), c = (int32_t)(blockIdx.x % (uint32_t)A.nc);
     const ShardDraw dw = draws[b];
-    ff* out = sums + (size_t)b * 4;
-    if (dw.mode == kModeNone) {
+    ff* out = sums + ((size_t)b * A.nc + c) * 4;
+    const int32_t c0 = c * kShChunk, c1 = min(A.Vs, c0 + kShChunk);
+    if (dw.mode == kModeNone || c0 >= c1) {
         if (threadIdx.x < 4) out[threadIdx.x] = ff{0.f, 0.f};
         return;
     }
     const int32_t o0 = __ldg(A.offs + b);
     const size_t prow = (size_t)(o0 + b + dw.n) * (size_t)A.Vs, qrow = (size_t)(o0 + dw.n) * (size_t)A.Vs;
-    const ExpConst EC{A.K_hi, A.K_lo, A.d_min};
-    ff P{0.f, 0.f}, Q{0.f, 0.f}, Sa{0.f, 0.f}, Sb{0.f, 0.f};
-    for (int32_t k = threadIdx.x; k < A.Vs; k += kShThreads) {
-        ff ep, eq;
-        bool sel;
-        draw_weights<DT>(A, dw, prow, qrow, k, EC, tab, ep, eq, sel);
-        P = ff_add(P, ep);
-        Q = ff_add(Q, eq);
-        if (sel) {
-            Sa = ff_add(Sa, ep);
-            Sb = ff_add(Sb, eq);
+    const bool resid = dw.mode == kModeResidual;
+    const bool staged = DT == SV_BF16 && A.Vs % 8 == 0 && (uintptr_t)A.target % 16 == 0 &&
+                        (!resid || (uintptr_t)A.draft % 16 == 0);
+    if (staged) {  // 16-byte packs of both rows (the chunk's width is a multiple of 8 columns)
+        const int32_t npk = (c1 - c0) / 8;
+        const char* gp = (const char*)A.target + (prow + c0) * 2;
+        const char* gq = (const char*)A.draft + (qrow + c0) * 2;
+        for (int32_t i = threadIdx.x; i < npk; i += kShSumThreads) {
+            cp_async16(&stage[0][4 * i], gp + 16 * (size_t)i);
+            if (resid) cp_async16(&stage[1][4 * i], gq + 16 * (size_t)i);
         }
     }
-    P = cta_sum_ff(P, red);
-    Q = cta_sum_ff(Q, red);
-    Sa = cta_sum_ff(Sa, red);
-    Sb = cta_sum_ff(Sb, red);
-    if (threadIdx.x == 0) {
-        out[0] = P;
-        out[1] = Q;
-        out[2] = Sa;
-        out[3] = Sb;
+    if (threadIdx.x < kExpTab) {
+        tab[threadIdx.x] = A.exp2_tab[threadIdx.x].x;
+        tab[kExpTab + threadIdx.x] = A.exp2_tab[threadIdx.x].y;
+    }
+    if (staged) cp_async_wait_all();
+    __syncthreads();
+    ff v[4];
+    auto run = [&](auto load) {
+        // bf16 rows whose maxima are not near zero need no rounding correction of l - m (see exp2_ff2)
+        if (DT == SV_BF16 && fabsf(dw.m_p) >= kNeedTwoSum && (!resid || fabsf(dw.m_q) >= kNeedTwoSum))
+            sums_pairs<false>(A, dw, c0, c1, tab, load, v);
+        else
+            sums_pairs<true>(A, dw, c0, c1, tab, load, v);
+    };
+    if (staged) {
+        run([&](int32_t k, float2& lp, float2& lq) {
+            const uint32_t wp = stage[0][(k - c0) >> 1];
+            lp = make_float2(bf16lo_to_f32(wp), bf16hi_to_f32(wp));
+            if (resid) {
+                const uint32_t wq = stage[1][(k - c0) >> 1];
+                lq = make_float2(bf16lo_to_f32(wq), bf16hi_to_f32(wq));
+            } else {
+                lq = f2(-INFINITY);
+            }
+        });
+    } else {
+        run([&](int32_t k, float2& lp, float2& lq) {
+            const bool two = k + 1 < c1;
+            lp = make_float2(lg<DT>(A.target, prow + k), two ? lg<DT>(A.target, prow + k + 1) : -INFINITY);
+            lq = resid ? make_float2(lg<DT>(A.draft, qrow + k), two ? lg<DT>(A.draft, qrow + k + 1) : -INFINITY)
+                       : f2(-INFINITY);
+        });
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            v[i] = ff_add(v[i], ff{__shfl_xor_sync(0xFFFFFFFFu, v[i].hi, o), __shfl_xor_sync(0xFFFFFFFFu, v[i].lo, o)});
+        if ((threadIdx.x & 31) == 0) red[i][threadIdx.x >> 5] = v[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < 4) {
+        ff t{0.f, 0.f};
+        for (int w = 0; w < kShSumThreads / 32; ++w) t = ff_add(t, red[threadIdx.x][w]);  // in warp order
+        out[threadIdx.x] = t;
     }
 }
 
@@ -339,124 +508,214 @@ __device__ __forceinline__ ff col_weight(const ShardDraw& dw, bool by_p, ff ep, 
     return w.hi > 0.f ? w : ff{0.f, 0.f};
 }
 
-// 3. The owner of the draw's target and, on the owning shard, the drawn column: one CTA per sequence.
+// Warp-wide float-float helpers (all 32 lanes take part).
+__device__ __forceinline__ ff shfl_ff(ff v, int src) {
+    return ff{__shfl_sync(0xFFFFFFFFu, v.hi, src), __shfl_sync(0xFFFFFFFFu, v.lo, src)};
+}
+// the sum over the warp, the same on every lane (each butterfly stage adds the same pair on both lanes)
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        v = ff_add(v, ff{__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)});
+    return v;
+}
+// inclusive prefix over lanes 0..lane
+__device__ __forceinline__ ff warp_scan_ff(ff v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff y{__shfl_up_sync(0xFFFFFFFFu, v.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.lo, o)};
+        if (lane >= o) v = ff_add(y, v);
+    }
+    return v;
+}
+
+// 3. The (shard, chunk) that holds the draw's target and, on the owning shard, the drawn column: one CTA per
+// sequence. Warp 0 of every shard finds the owner from the gathered chunk sums (records in shard, then chunk
+// order: ratio, masses, total, prefix; the same arithmetic on every shard). The owner scans that chunk:
+// thread t takes 16 contiguous columns, exact sums of their selected weights (A - rho B for a residual), a
+// CTA-wide prefix, then the crossing thread's warp weighs its 16 columns one a lane and scans them.
 template <int DT>
 __global__ void __launch_bounds__(kShThreads) k_shard_finish(const __grid_constant__ ShardArgs A, const ShardDraw* draws,
                                                              const ff* all_sums) {
     __shared__ float tab[2 * kExpTab];
     __shared__ ff red[kShThreads / 32];
     __shared__ int redi[kShThreads / 32];
+    __shared__ ff s_rec[kShRecSmem][4];
+    __shared__ ff s_rho, s_rem;
+    __shared__ int s_owner, s_byp, s_tail, s_col;
     if (threadIdx.x < kExpTab) {
         tab[threadIdx.x] = A.exp2_tab[threadIdx.x].x;
         tab[kExpTab + threadIdx.x] = A.exp2_tab[threadIdx.x].y;
     }
-    __syncthreads();
     const int32_t b = (int32_t)blockIdx.x;
     const ShardDraw dw = draws[b];
     if (dw.mode == kModeNone) return;  // greedy or failed: written by the decision
     const int32_t o0 = __ldg(A.offs + b), t0 = o0 + b;
-    // every shard: the exact ratio and each shard's mass, summed in shard order
-    ff sp{0.f, 0.f}, sq{0.f, 0.f};
-    for (int j = 0; j < A.S; ++j) {
-        sp = ff_add(sp, all_sums[((size_t)j * A.B + b) * 4]);
-        sq = ff_add(sq, all_sums[((size_t)j * A.B + b) * 4 + 1]);
-    }
     const bool resid = dw.mode == kModeResidual;
-    const ff rho = resid ? ff_div(sp, sq) : ff{0.f, 0.f};
-    auto mass = [&](int j, bool by_p) {
-        const ff* s = all_sums + ((size_t)j * A.B + b) * 4;
-        if (by_p) return s[0];
-        ff w = s[2];
-        if (resid) w = ff_sub(w, ff_mul(rho, s[3]));
-        return w.hi > 0.f ? w : ff{0.f, 0.f};
-    };
-    ff S{0.f, 0.f};
-    for (int j = 0; j < A.S; ++j) S = ff_add(S, mass(j, false));
-    const bool by_p = !(S.hi > 0.f);  // a residual of mass 0: draw from p
-    if (by_p) {
-        S = ff{0.f, 0.f};
-        for (int j = 0; j < A.S; ++j) S = ff_add(S, mass(j, true));
-    }
-    const ff target = ff_mul(ff{dw.u, 0.f}, S);
-    int jo = -1, jlast = -1;
-    ff before{0.f, 0.f}, c{0.f, 0.f}, before_last{0.f, 0.f};
-    for (int j = 0; j < A.S; ++j) {
-        const ff w = mass(j, by_p);
-        if (!(w.hi > 0.f)) continue;
-        const ff c2 = ff_add(c, w);
-        if (jo < 0 && ff_gt(c2, target)) {
-            jo = j;
-            before = c;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the sequence's gathered records, staged in shared memory when they fit
+    const int32_t nrec = A.S * A.nc;
+    const bool staged = nrec <= kShRecSmem;
+    if (staged)
+        for (int32_t i = threadIdx.x; i < nrec * 4; i += kShThreads) {
+            const int32_t j = i / (A.nc * 4), r = i % (A.nc * 4);
+            s_rec[i / 4][i % 4] = all_sums[((size_t)j * A.B + b) * A.nc * 4 + r];
         }
-        jlast = j;
-        before_last = c;
-        c = c2;
+    if (threadIdx.x == 0) s_col = -1;
+    __syncthreads();
+    if (warp == 0) {
+        auto rec = [&](int32_t r) {
+            return staged ? &s_rec[r][0] : all_sums + (((size_t)(r / A.nc) * A.B + b) * A.nc + r % A.nc) * 4;
+        };
+        ff sp{0.f, 0.f}, sq{0.f, 0.f};
+        for (int32_t r = lane; r < nrec; r += 32) {
+            sp = ff_add(sp, rec(r)[0]);
+            sq = ff_add(sq, rec(r)[1]);
+        }
+        sp = warp_sum_ff(sp);
+        sq = warp_sum_ff(sq);
+        const ff rho = resid ? ff_div(sp, sq) : ff{0.f, 0.f};
+        auto mass = [&](int32_t r, bool by_p) {
+            if (r >= nrec) return ff{0.f, 0.f};
+            const ff* x = rec(r);
+            if (by_p) return x[0];
+            ff w = x[2];
+            if (resid) w = ff_sub(w, ff_mul(rho, x[3]));
+            return w.hi > 0.f ? w : ff{0.f, 0.f};
+        };
+        ff S{0.f, 0.f};
+        for (int32_t r = lane; r < nrec; r += 32) S = ff_add(S, mass(r, false));
+        S = warp_sum_ff(S);
+        const bool by_p = !(S.hi > 0.f);  // a residual of mass 0: draw from p
+        if (by_p) {
+            S = ff{0.f, 0.f};
+            for (int32_t r = lane; r < nrec; r += 32) S = ff_add(S, mass(r, true));
+            S = warp_sum_ff(S);
+        }
+        const ff target = ff_mul(ff{dw.u, 0.f}, S);
+        // the first record of positive mass whose inclusive prefix exceeds the target; else (rounding) the
+        // last record of positive mass
+        int32_t owner = -1, lastr = -1;
+        ff before{0.f, 0.f}, before_last{0.f, 0.f}, carry{0.f, 0.f};
+        for (int32_t g = 0; g < nrec; g += 32) {
+            const ff w = mass(g + lane, by_p);
+            const ff inc = ff_add(carry, warp_scan_ff(w, lane));
+            const ff up = shfl_ff(inc, lane ? lane - 1 : 0);
+            const ff exc = lane ? up : carry;
+            const bool pos = w.hi > 0.f;
+            const uint32_t cross = __ballot_sync(0xFFFFFFFFu, pos && ff_gt(inc, target));
+            if (cross) {
+                const int f = __ffs(cross) - 1;
+                owner = g + f;
+                before = shfl_ff(exc, f);
+                break;
+            }
+            const uint32_t pb = __ballot_sync(0xFFFFFFFFu, pos);
+            if (pb) {
+                const int l = 31 - __clz(pb);
+                lastr = g + l;
+                before_last = shfl_ff(exc, l);
+            }
+            carry = shfl_ff(inc, 31);
+        }
+        if (lane == 0) {
+            s_tail = owner < 0;
+            if (owner < 0) {
+                owner = lastr;
+                before = before_last;
+            }
+            s_owner = owner;
+            s_byp = by_p;
+            s_rho = rho;
+            s_rem = ff_sub(target, before);
+        }
     }
-    const bool tail_rule = jo < 0;  // rounding lost the crossing: the last positive column overall
-    if (tail_rule) {
-        jo = jlast;
-        before = before_last;
-    }
-    if (jo != A.shard) {
+    __syncthreads();
+    const int32_t owner = s_owner;
+    const bool by_p = s_byp, tail_rule = s_tail;
+    if (owner < 0 || owner / A.nc != A.shard) {
         if (threadIdx.x == 0) A.out_tokens[t0 + dw.n] = -1;  // another shard's column
         return;
     }
-    // the owning shard: thread t scans the columns [t C, t C + C) of its slice
-    const ff rem = ff_sub(target, before);
-    const int32_t C = (A.Vs + kShThreads - 1) / kShThreads, k0 = threadIdx.x * C, k1 = min(A.Vs, k0 + C);
+    const ff rho = s_rho, rem = s_rem;
+    const int32_t kc0 = (owner % A.nc) * kShChunk, kc1 = min(A.Vs, kc0 + kShChunk);
+    constexpr int C = kShChunk / kShThreads;  // 16 columns per thread
+    const int32_t k0 = kc0 + (int32_t)threadIdx.x * C, k1 = min(kc1, k0 + C);
     const size_t prow = (size_t)(o0 + b + dw.n) * (size_t)A.Vs, qrow = (size_t)(o0 + dw.n) * (size_t)A.Vs;
     const ExpConst EC{A.K_hi, A.K_lo, A.d_min};
-    ff tot{0.f, 0.f};
-    int lastpos = -1;
-    for (int32_t k = k0; k < k1; ++k) {
-        ff ep, eq;
-        bool sel;
-        draw_weights<DT>(A, dw, prow, qrow, k, EC, tab, ep, eq, sel);
-        const ff w = col_weight(dw, by_p, ep, eq, sel, rho);
-        if (w.hi > 0.f) {
-            tot = ff_add(tot, w);
-            lastpos = k;
-        }
-    }
-    // exclusive prefix of the threads' totals (warp scan, then the warps' totals in order)
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    ff incl = tot;
+    // the thread's total: exact sums of its selected p (and q) weights, A - rho B for a residual
+    float2 Ah = f2(0.f), Al = f2(0.f), Bh = f2(0.f), Bl = f2(0.f);
+    float2 LP[C / 2], LQ[C / 2];  // the thread's columns, loaded before use
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const ff y{__shfl_up_sync(0xFFFFFFFFu, incl.hi, o), __shfl_up_sync(0xFFFFFFFFu, incl.lo, o)};
-        if (lane >= o) incl = ff_add(y, incl);
+    for (int i = 0; i < C / 2; ++i) {
+        const int32_t k = k0 + 2 * i;
+        LP[i] = make_float2(k < k1 ? lg<DT>(A.target, prow + k) : -INFINITY,
+                            k + 1 < k1 ? lg<DT>(A.target, prow + k + 1) : -INFINITY);
+        LQ[i] = make_float2(resid && k < k1 ? lg<DT>(A.draft, qrow + k) : -INFINITY,
+                            resid && k + 1 < k1 ? lg<DT>(A.draft, qrow + k + 1) : -INFINITY);
     }
+#pragma unroll
+    for (int i = 0; i < C / 2; ++i) {
+        const int32_t k = k0 + 2 * i;
+        if (k >= k1) break;
+        const float2 lp = LP[i], lq = LQ[i];
+        const ff2 ep = exp2_ff2(lp, f2(dw.m_p), EC, tab);
+        const ff2 eq = resid ? exp2_ff2(lq, f2(dw.m_q), EC, tab) : ff2{f2(0.f), f2(0.f)};
+        float2 mk;
+        if (by_p) mk = f2(1.f);
+        else if (resid) mk = make_float2(gt_mask(ep.hi.x, dw.rho * eq.hi.x), gt_mask(ep.hi.y, dw.rho * eq.hi.y));
+        else mk = make_float2(A.v0 + k == dw.xcl ? 0.f : 1.f, A.v0 + k + 1 == dw.xcl ? 0.f : 1.f);
+        const float2 hp = grid_hi(ep.hi), lpw = add2(sub2(ep.hi, hp), ep.lo);
+        const float2 hq = grid_hi(eq.hi), lqw = add2(sub2(eq.hi, hq), eq.lo);
+        Ah = fma2(mk, hp, Ah); Al = fma2(mk, lpw, Al);
+        Bh = fma2(mk, hq, Bh); Bl = fma2(mk, lqw, Bl);
+    }
+    ff tot = ff_add(ff{Ah.x, Al.x}, ff{Ah.y, Al.y});
+    if (resid && !by_p) tot = ff_sub(tot, ff_mul(rho, ff_add(ff{Bh.x, Bl.x}, ff{Bh.y, Bl.y})));
+    if (!(tot.hi > 0.f)) tot = ff{0.f, 0.f};
+    // exclusive prefix of the threads' totals (warp scan, then the warps' totals in order)
+    const ff incl = warp_scan_ff(tot, lane);
     if (lane == 31) red[warp] = incl;
     __syncthreads();
     ff wbefore{0.f, 0.f};
     for (int w = 0; w < warp; ++w) wbefore = ff_add(wbefore, red[w]);
-    const ff ex_lane{__shfl_up_sync(0xFFFFFFFFu, incl.hi, 1), __shfl_up_sync(0xFFFFFFFFu, incl.lo, 1)};
+    const ff ex_lane = shfl_ff(incl, lane ? lane - 1 : 0);
     const ff excl = ff_add(wbefore, lane ? ex_lane : ff{0.f, 0.f});
     const ff inc = ff_add(excl, tot);
     // the first thread whose inclusive prefix exceeds rem holds the crossing (lowest thread index)
     const bool holds = !tail_rule && tot.hi > 0.f && ff_gt(inc, rem) && !ff_gt(excl, rem);
-    const int first = cta_min_i(holds ? (int)threadIdx.x : 0x7FFFFFFF, redi);
-    const int lastp = -cta_min_i(-lastpos, redi);  // the slice's last column of positive weight
-    if (first != 0x7FFFFFFF) {
-        if ((int)threadIdx.x == first) {
-            ff cc = excl;
-            int32_t col = -1, lastc = -1;
-            for (int32_t k = k0; k < k1 && col < 0; ++k) {
-                ff ep, eq;
-                bool sel;
-                draw_weights<DT>(A, dw, prow, qrow, k, EC, tab, ep, eq, sel);
-                const ff w = col_weight(dw, by_p, ep, eq, sel, rho);
-                if (!(w.hi > 0.f)) continue;
-                cc = ff_add(cc, w);
-                lastc = k;
-                if (ff_gt(cc, rem)) col = k;
-            }
-            if (col < 0) col = lastc;  // the thread's sum crossed, its running sum fell short by rounding
-            A.out_tokens[t0 + dw.n] = A.v0 + col;
+    const int first = cta_min_i<kShThreads>(holds ? (int)threadIdx.x : 0x7FFFFFFF, redi);
+    if (first != 0x7FFFFFFF && warp == first / 32) {
+        // the crossing thread's columns, one a lane: weights, their prefix from the thread's exclusive
+        // prefix, the first positive column past rem (else, rounding, its last positive column)
+        const int32_t f0 = kc0 + first * C, f1 = min(kc1, f0 + C);
+        const ff base = shfl_ff(excl, first & 31);
+        ff w{0.f, 0.f};
+        if (lane < C && f0 + lane < f1) {
+            ff ep, eq;
+            bool sel;
+            draw_weights<DT>(A, dw, prow, qrow, f0 + lane, EC, tab, ep, eq, sel);
+            w = col_weight(dw, by_p, ep, eq, sel, rho);
         }
-    } else if (threadIdx.x == 0) {
-        A.out_tokens[t0 + dw.n] = lastp >= 0 ? A.v0 + lastp : -1;
+        const ff cc = ff_add(base, warp_scan_ff(w, lane));
+        const bool pos = w.hi > 0.f;
+        const uint32_t cross = __ballot_sync(0xFFFFFFFFu, pos && ff_gt(cc, rem));
+        const uint32_t pb = __ballot_sync(0xFFFFFFFFu, pos);
+        if (lane == 0 && pb) s_col = f0 + (cross ? __ffs(cross) - 1 : 31 - __clz(pb));
     }
+    __syncthreads();
+    int32_t col = s_col;
+    if (col < 0) {  // no crossing (the tail rule, or rounding): the chunk's last column of positive weight
+        int lastpos = -1;
+        for (int32_t k = k0; k < k1; ++k) {
+            ff ep, eq;
+            bool sel;
+            draw_weights<DT>(A, dw, prow, qrow, k, EC, tab, ep, eq, sel);
+            if (col_weight(dw, by_p, ep, eq, sel, rho).hi > 0.f) lastpos = k;
+        }
+        col = -cta_min_i<kShThreads>(-lastpos, redi);
+    }
+    if (threadIdx.x == 0) A.out_tokens[t0 + dw.n] = col >= 0 ? A.v0 + col : -1;
 }
 
 }  // namespace
@@ -467,8 +726,8 @@ cudaError_t launch_shard(int stage, const ShardArgs& A, void* a, void* b, void* 
     switch (stage) {
         case 0:
             if (nrows > 0) {
-                if (A.dtype == SV_BF16) k_shard_stats<SV_BF16><<<nrows, kShThreads, 0, st>>>(A, (ShardPartial*)a);
-                else k_shard_stats<SV_F32><<<nrows, kShThreads, 0, st>>>(A, (ShardPartial*)a);
+                if (A.dtype == SV_BF16) k_shard_stats<SV_BF16><<<nrows, kShStatThreads, 0, st>>>(A, (ShardPartial*)a);
+                else k_shard_stats<SV_F32><<<nrows, kShStatThreads, 0, st>>>(A, (ShardPartial*)a);
             }
             break;
         case 1:
@@ -476,8 +735,8 @@ cudaError_t launch_shard(int stage, const ShardArgs& A, void* a, void* b, void* 
             else k_shard_decide<SV_F32><<<(A.B + 7) / 8, 256, 0, st>>>(A, (const ShardPartial*)a, (ShardDraw*)b);
             break;
         case 2:
-            if (A.dtype == SV_BF16) k_shard_sums<SV_BF16><<<A.B, kShThreads, 0, st>>>(A, (const ShardDraw*)a, (ff*)b);
-            else k_shard_sums<SV_F32><<<A.B, kShThreads, 0, st>>>(A, (const ShardDraw*)a, (ff*)b);
+            if (A.dtype == SV_BF16) k_shard_sums<SV_BF16><<<A.nc * A.B, kShSumThreads, 0, st>>>(A, (const ShardDraw*)a, (ff*)b);
+            else k_shard_sums<SV_F32><<<A.nc * A.B, kShSumThreads, 0, st>>>(A, (const ShardDraw*)a, (ff*)b);
             break;
         default:
             if (A.dtype == SV_BF16) k_shard_finish<SV_BF16><<<A.B, kShThreads, 0, st>>>(A, (const ShardDraw*)a, (const ff*)b);
@@ -525,6 +784,9 @@ int shard_bounds(sv::ShardArgs& A, int32_t S, const int32_t* bounds, int32_t V) 
     }
     A.bounds[S] = V;
     A.S = S;
+    int32_t w = 0;
+    for (int j = 0; j < S; ++j) w = std::max(w, bounds[j + 1] - bounds[j]);
+    A.nc = (w + sv::kShChunk - 1) / sv::kShChunk;
     return SV_OK;
 }
 bool aligned4(const void* p) { return p && (uintptr_t)p % 4 == 0; }
@@ -583,21 +845,30 @@ int spec_shard_decide(const void* all_partials, int32_t S, const int32_t* shard_
     return sv::launch_shard(1, A, const_cast<void*>(all_partials), draws, nullptr) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-int spec_shard_sums(const void* shard_target, const void* shard_draft, sv_dtype dtype, int32_t v0, int32_t Vs,
-                    const void* draws, const int32_t* seq_offsets, int32_t B, int32_t V, float temperature, void* sums,
-                    void* cuda_stream) {
+int32_t spec_shard_chunks(int32_t S, const int32_t* shard_bounds_host) {
+    sv::ShardArgs A{};
+    if (S < 1 || S > sv::kMaxShards || !shard_bounds_host) return 0;
+    return shard_bounds(A, S, shard_bounds_host, shard_bounds_host[S]) == SV_OK ? A.nc : 0;
+}
+
+int spec_shard_sums(int32_t shard, int32_t S, const int32_t* shard_bounds_host, const void* shard_target,
+                    const void* shard_draft, sv_dtype dtype, const void* draws, const int32_t* seq_offsets, int32_t B,
+                    int32_t V, float temperature, void* sums, void* cuda_stream) {
     sv::ShardArgs A;
     int rc = shard_args(A, dtype, B, V, 0, temperature, cuda_stream);
     if (rc != SV_OK) return rc;
-    if (v0 < 0 || Vs < 1 || (int64_t)v0 + Vs > V || !shard_target || !draws || (uintptr_t)draws % 16 ||
-        !aligned4(seq_offsets) || !sums || (uintptr_t)sums % 16)
+    if ((rc = shard_bounds(A, S, shard_bounds_host, V)) != SV_OK) return rc;
+    if (shard < 0 || shard >= S || !shard_target || !draws || (uintptr_t)draws % 16 || !aligned4(seq_offsets) ||
+        !sums || (uintptr_t)sums % 16)
         return SV_ERR_INVALID_ARG;
     if (B == 0 || A.greedy) return SV_OK;
+    if ((int64_t)A.nc * B >= (1ll << 31)) return SV_ERR_INVALID_ARG;  // one CTA per (sequence, chunk)
+    A.shard = shard;
+    A.v0 = A.bounds[shard];
+    A.Vs = A.bounds[shard + 1] - A.bounds[shard];
     A.target = shard_target;
     A.draft = shard_draft;
     A.offs = seq_offsets;
-    A.v0 = v0;
-    A.Vs = Vs;
     return sv::launch_shard(2, A, const_cast<void*>(draws), sums, nullptr) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
@@ -628,3 +899,4 @@ int spec_shard_finish(int32_t shard, int32_t S, const int32_t* shard_bounds_host
 
 static_assert(sizeof(sv::ShardPartial) == sizeof(sv_shard_partial), "the C ABI's partial record");
 static_assert(sizeof(sv::ShardDraw) == sizeof(sv_shard_draw), "the C ABI's draw record");
+static_assert(sv::kShChunk == SV_SHARD_CHUNK, "the C ABI's sums chunk");

@@ -15,7 +15,7 @@ from . import specverify as sv
 
 PARTIAL_WORDS = 4  # sv_shard_partial: 16 bytes
 DRAW_WORDS = 8     # sv_shard_draw: 32 bytes
-SUM_WORDS = 8      # four float pairs per sequence
+SUM_WORDS = 8      # four float pairs per sequence and chunk
 
 
 class CudaShard:
@@ -39,7 +39,10 @@ class CudaShard:
         i32 = torch.int32
         self.partials = torch.zeros((self.rows, PARTIAL_WORDS), dtype=i32, device=dev)
         self.draws = torch.zeros((B, DRAW_WORDS), dtype=i32, device=dev)
-        self.sums = torch.zeros((B, SUM_WORDS), dtype=torch.float32, device=dev)
+        self.nc = sv.spec_shard_chunks(self.S, self.bounds)
+        if self.nc < 1:
+            raise ValueError(f"invalid shard bounds {self.bounds}")
+        self.sums = torch.zeros((B, self.nc * SUM_WORDS), dtype=torch.float32, device=dev)
         self.out_tokens = torch.full((R_t,), -1, dtype=i32, device=dev)
         self.out_n = torch.full((B,), -1, dtype=i32, device=dev)
         self.status = torch.zeros(1, dtype=i32, device=dev)
@@ -67,8 +70,8 @@ class CudaShard:
 
     def draw_sums(self, stream=None):
         p = sv._ptr
-        rc = sv.spec_shard_sums(p(self.target), p(self.draft), self.dtype, self.v0, self.Vs, p(self.draws), p(self.offs),
-                                self.B, self.V, self.T, p(self.sums), self._st(stream))
+        rc = sv.spec_shard_sums(self.shard, self.S, self.bounds, p(self.target), p(self.draft), self.dtype,
+                                p(self.draws), p(self.offs), self.B, self.V, self.T, p(self.sums), self._st(stream))
         if rc != sv.SV_OK:
             raise RuntimeError(sv.spec_verify_status_string(rc))
         return self.sums

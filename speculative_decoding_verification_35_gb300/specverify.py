@@ -20,7 +20,7 @@ SV_MAX_GAMMA = 31
 # every exported symbol of the C ABI, in header order
 EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
            "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
-           "spec_shard_stats", "spec_shard_decide", "spec_shard_sums", "spec_shard_finish",
+           "spec_shard_stats", "spec_shard_decide", "spec_shard_chunks", "spec_shard_sums", "spec_shard_finish",
            "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host")
 
 
@@ -69,7 +69,9 @@ def _load():
     L.spec_shard_stats.restype = ctypes.c_int
     L.spec_shard_decide.argtypes = [vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, i32, u64, u64, vp, vp, vp, vp, vp]
     L.spec_shard_decide.restype = ctypes.c_int
-    L.spec_shard_sums.argtypes = [vp, vp, ctypes.c_int, i32, i32, vp, vp, i32, i32, f32, vp, vp]
+    L.spec_shard_chunks.argtypes = [i32, vp]
+    L.spec_shard_chunks.restype = i32
+    L.spec_shard_sums.argtypes = [i32, i32, vp, vp, vp, ctypes.c_int, vp, vp, i32, i32, f32, vp, vp]
     L.spec_shard_sums.restype = ctypes.c_int
     L.spec_shard_finish.argtypes = [i32, i32, vp, vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, f32, vp, vp]
     L.spec_shard_finish.restype = ctypes.c_int
@@ -174,11 +176,18 @@ def spec_shard_decide(all_partials, S, bounds, draft_tokens, seq_offsets, gammas
                                  device_status, cuda_stream)
 
 
-def spec_shard_sums(shard_target, shard_draft, dtype, v0, Vs, draws, seq_offsets, B, V, temperature, sums,
+def spec_shard_chunks(S, bounds) -> int:
+    """Sums records per sequence and shard (chunks of the widest shard), 0 for invalid bounds."""
+    hb = (ctypes.c_int32 * (S + 1))(*[int(v) for v in bounds])
+    return lib.spec_shard_chunks(S, hb)
+
+
+def spec_shard_sums(shard, S, bounds, shard_target, shard_draft, dtype, draws, seq_offsets, B, V, temperature, sums,
                     cuda_stream) -> int:
-    """The draws' exact sums over one shard's slice."""
-    return lib.spec_shard_sums(shard_target, shard_draft, dtype, v0, Vs, draws, seq_offsets, B, V, float(temperature),
-                               sums, cuda_stream)
+    """The draws' exact sums over one shard's slice, per chunk of SV_SHARD_CHUNK columns."""
+    hb = (ctypes.c_int32 * (S + 1))(*[int(v) for v in bounds])
+    return lib.spec_shard_sums(shard, S, hb, shard_target, shard_draft, dtype, draws, seq_offsets, B, V,
+                               float(temperature), sums, cuda_stream)
 
 
 def spec_shard_finish(shard, S, bounds, shard_target, shard_draft, dtype, draws, all_sums, seq_offsets, B, V,

@@ -31,7 +31,8 @@ def test_header_declares_the_api():
     assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
                           "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
                           "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host",
-                          "spec_shard_stats", "spec_shard_decide", "spec_shard_sums", "spec_shard_finish"}
+                          "spec_shard_stats", "spec_shard_decide", "spec_shard_chunks", "spec_shard_sums",
+                          "spec_shard_finish"}
 
 
 def test_library_exports_every_declared_symbol(libpath):
@@ -206,8 +207,21 @@ def test_shard_host_side_checks_without_gpu(libpath):
     assert decide(S=9, bounds=list(range(0, 99, 11)) + [100]) == sv.SV_ERR_INVALID_ARG  # at most 8 shards
     assert decide(draws=fake + 4) == sv.SV_ERR_INVALID_ARG
     assert decide(B=0) == sv.SV_OK
-    assert sv.spec_shard_sums(fake, fake, sv.SV_BF16, 90, 20, fake, fake, 4, 100, 1.0, fake, None) == \
-        sv.SV_ERR_INVALID_ARG
+    assert sv.spec_shard_sums(2, 2, [0, 50, 100], fake, fake, sv.SV_BF16, fake, fake, 4, 100, 1.0, fake, None) == \
+        sv.SV_ERR_INVALID_ARG  # shard index past S
+    assert sv.spec_shard_sums(0, 2, [0, 50, 100], fake, fake, sv.SV_BF16, fake, fake, 4, 100, 1.0, fake + 8, None) == \
+        sv.SV_ERR_INVALID_ARG  # records 16-byte aligned
+    assert sv.spec_shard_sums(0, 2, [0, 50, 100], fake, fake, sv.SV_BF16, fake, fake, 4, 100, 0.0, fake, None) == \
+        sv.SV_OK  # greedy: no draws
+    # records per sequence: chunks of the widest shard
+    assert sv.spec_shard_chunks(2, [0, 50, 100]) == 1
+    assert sv.spec_shard_chunks(2, [0, 8192, 8193]) == 1
+    assert sv.spec_shard_chunks(2, [0, 1, 8194]) == 2
+    assert sv.spec_shard_chunks(2, [0, 64128, 128256]) == 8
+    assert sv.spec_shard_chunks(4, [0, 32064, 64128, 96192, 128256]) == 4
+    assert sv.spec_shard_chunks(2, [0, 60, 50]) == 0
+    assert sv.spec_shard_chunks(2, [1, 60, 100]) == 0
+    assert sv.spec_shard_chunks(9, list(range(0, 99, 11)) + [100]) == 0
     assert sv.spec_shard_finish(2, 2, [0, 50, 100], fake, fake, sv.SV_BF16, fake, fake, fake, 4, 100, 1.0, fake,
                                 None) == sv.SV_ERR_INVALID_ARG  # shard index past S
     assert sv.spec_shard_finish(0, 2, [0, 50, 100], fake, fake, sv.SV_BF16, fake, fake, fake, 4, 100, 0.0, fake,

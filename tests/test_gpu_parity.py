@@ -280,3 +280,38 @@ def test_point_mass_gamma_zero_and_max():
     b = synth.make_batch("pointmass_b64_g5_v128256", B=5, V=4000, gammas=[0, 31, 3, 0, 31])
     for step in range(3):
         parity.assert_parity(b, 9, step)
+
+
+@pytest.mark.parametrize("T", [0.3, 0.6, 1.7, 3.0])
+def test_value_table_across_temperatures(T):
+    """Batches large enough that the call builds the value table (>= 2048 sampler tasks), at temperatures
+    that move its range (the largest row maximum it serves is min(63.75, 96 / K), K = log2(e) / T)."""
+    w = synth.WORKLOADS["b64_g5_v128256"]
+    wt = synth.Workload("b20_g5_v128256_t", 20, w.V, w.dtype, T, w.gamma, w.target_sigma, w.zipf_s, w.draft_scale,
+                        w.draft_sigmas, seed=w.seed)
+    b = synth.make_batch(wt)
+    assert b.B * ((b.V + 1023) // 1024) >= 2048
+    for step in range(3):
+        parity.assert_parity(b, 42, step)
+
+
+def test_value_table_and_exponential_draws_in_one_call():
+    """Rows shifted so that some sequences' maxima lie above the value table's range (63.75) or below its
+    floor (-63.75 + 60 / K): those draws take the precise exponential, the others the table, in one call."""
+    b0 = synth.make_batch("b64_g5_v128256", B=24)
+
+    def shifted(bits, shift):
+        x = synth.bf16_bits_to_f32(bits) + np.float32(shift)
+        return synth.to_bf16_bits(x.astype(np.float32))
+
+    tgt, dft = b0.target.copy(), b0.draft.copy()
+    for s in range(b0.B):
+        shift = (70.0, -40.0, 0.0, 50.0)[s % 4]  # above the range, below the floor, inside, near the top
+        t0, d0, g = int(b0.seq_offsets[s]) + s, int(b0.seq_offsets[s]), int(b0.gammas[s])
+        tgt[t0:t0 + g + 1] = shifted(b0.target[t0:t0 + g + 1], shift)
+        dft[d0:d0 + g] = shifted(b0.draft[d0:d0 + g], shift)
+    b = synth.Batch(b0.workload, tgt, dft, b0.draft_tokens, b0.seq_offsets, b0.gammas)
+    m = synth.bf16_bits_to_f32(b.target).max(1)
+    assert m.max() > 63.75 and m.min() < -63.75 + 60 / 1.4426950408889634
+    for step in range(3):
+        parity.assert_parity(b, 8, step)
