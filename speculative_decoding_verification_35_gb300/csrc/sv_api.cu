@@ -108,6 +108,11 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.use_tab = !greedy && (int64_t)B * P.nS >= kTabMinTasks;
     P.tab_mlo = greedy ? 1.f : (float)(-63.75 + 60.0 / (double)K_hi);
     P.tab_mhi = greedy ? 0.f : (float)std::min(63.75, 96.0 / (double)K_hi);
+    {
+        const bool row_dbg = debug && (debug->row_lse || debug->row_argmax || debug->p_x || debug->q_x || debug->beta);
+        P.prog = !greedy && dtype == SV_BF16 && vec && !parents && !row_dbg && B < kBaseCache &&
+                 (int64_t)B * ((P.pm ? 1 : 2) * (int64_t)max_gamma + 1) <= kRowCache;
+    }
     P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;
     P.seed = seed;
     P.step = step;
@@ -128,6 +133,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.remw = (Word*)(ws + L.remw);
     P.pathw = (Word*)(ws + L.pathw);
     P.seqstate = (uint32_t*)(ws + L.seqstate);
+    P.order = (uint32_t*)(ws + L.order);
     P.ctr = (Counters*)(ws + L.counters);
     P.parents = parents;
     P.out_path = out_path;

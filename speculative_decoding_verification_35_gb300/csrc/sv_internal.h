@@ -90,9 +90,11 @@ constexpr int kGroupCols = kSTask / kGroups;         // 128 columns
 constexpr int kGroupWords = 2;
 
 // Counters of one call (zeroed before the kernel by the launch sequence).
+constexpr uint32_t kOrderLost = 0xFFFFFFFFu;
 struct Counters {
-    uint32_t claim;  // sampler tasks claimed, in sequence-major order
-    uint32_t pad[31];
+    uint32_t claim;    // sampler tasks claimed: in sequence-major order, or (slot order) in decision order
+    uint32_t decided;  // slot order: decisions published (positions in the decision-order queue)
+    uint32_t pad[30];
 };
 
 struct Params {
@@ -110,6 +112,9 @@ struct Params {
     float d_min;       // clamp of l - m in the precise exponential (about -126.5 / K)
     int32_t use_tab;         // the CTAs build the value table (batches with enough sampler work, bf16 rows)
     float tab_mlo, tab_mhi;  // a draw uses the value table when its rows' raw maxima lie in [tab_mlo, tab_mhi]
+    int32_t prog;      // slot order: statistics streamed slot by slot, each decision made at its first
+                       // rejection, the rows after it checked by the sequence's find (bf16 bulk-copy path,
+                       // linear sampled drafts, no per-row debug output, row bases and map in shared memory)
     uint32_t spin;     // polls before a wait on another warp's word gives up (kSpinLimit unless a caller
                        // testing the time-out path asks for fewer)
     double invT64;     // 1 / T (debug output of the row log-normalisers only)
@@ -127,6 +132,8 @@ struct Params {
     Word* pathw;            // [B * kMaxRemoved] accepted path of a sampled tree: (0x80000000 | node) << 32 | token
     uint32_t* seqstate;     // [B] who writes a sampled sequence's outputs: 0 open, 1 its find, 2 failed (a wait
                             // on the sequence gave up); claimed by compare-and-swap
+    uint32_t* order;        // [B] slot order: the decision-order queue, entry p = b + 1 of the p-th decided
+                            // sequence (0: not yet; kOrderLost: a claimer gave up waiting for it)
     const int32_t* parents; // token trees: parent node of each non-root node (nullptr: linear drafts)
     int32_t* out_path;      // token trees: the accepted nodes (nullable)
     Counters* ctr;
@@ -181,7 +188,7 @@ struct ShardArgs {
 cudaError_t launch_shard(int stage, const ShardArgs& A, void* a, void* b, void* c);
 
 struct Layout {
-    size_t counters, partials, taskw, recw, groupw, remw, pathw, seqstate, status;
+    size_t counters, partials, taskw, recw, groupw, remw, pathw, seqstate, order, status;
     size_t zero_begin, zero_end;  // byte range the launch sequence clears
     size_t total;
 };

@@ -58,6 +58,11 @@ __device__ __forceinline__ Word ld_word(const Word* p) {
 __device__ __forceinline__ void st_word(Word* p, Word v) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ uint32_t ld_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ Word pack_words(uint32_t hi32, uint32_t lo32) { return ((Word)hi32 << 32) | lo32; }
 // a non-negative float-float value with the marker bit in its high part's sign
 __device__ __forceinline__ Word pack_ff(ff v) { return pack_words(__float_as_uint(v.lo), __float_as_uint(v.hi) | kWordMark); }
@@ -895,6 +900,208 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     }
 }
 
+// Slot order (P.prog): the statistics rows are numbered by slot, q = s * per + k with per = B (point-mass
+// drafts) or 2 B: k = b for the target row of slot s of sequence b, k = B + b for its draft row; the last
+// slot (s = max_gamma) holds target rows only. A q that sequence b does not have (s > gamma_b, or the draft
+// row of slot gamma_b) is a hole. The partial words are indexed by q; the CTA's row map holds, per q, the
+// logits row (bits 0-11), the sequence (bits 12-21), the slot (bits 22-26) and the draft flag (bit 31),
+// or kProgHole.
+constexpr uint32_t kProgHole = 0x7FFFFFFFu;
+__device__ __forceinline__ uint32_t prog_per(const Params& P) { return P.pm ? (uint32_t)P.B : 2u * (uint32_t)P.B; }
+__device__ __forceinline__ uint32_t prog_rows(const Params& P) {
+    return prog_per(P) * (uint32_t)P.max_gamma + (uint32_t)P.B;
+}
+__device__ __forceinline__ int32_t prog_q(const Params& P, int32_t b, int32_t s, bool draft) {
+    return s * (int32_t)prog_per(P) + (draft ? P.B : 0) + b;
+}
+
+// Slot order: a published decision takes the next position of the decision-order queue, from which the
+// sampler tasks are claimed (so that no warp waits on a sequence decided late while decided ones wait).
+// A position a claimer gave up waiting for (kOrderLost, SV_ERR_TIMEOUT set) fails its sequence here.
+__device__ __noinline__ void enqueue_decided(const Params& P, int32_t b, int lane) {
+    uint32_t lost = 0;
+    if (lane == 0) {
+        const uint32_t p = atomicAdd(&P.ctr->decided, 1u);
+        lost = atomicCAS(P.order + p, 0u, (uint32_t)b + 1u) != 0u;
+    }
+    if (__shfl_sync(0xFFFFFFFFu, lost, 0)) give_up_seq(P, b, lane);
+}
+
+// Decision in slot order (P.prog, linear sampled drafts; one warp): slot s is tested as soon as its rows'
+// statistics are in (target row s and draft row s, which the slot-order stream delivers together), and
+// the first rejection ends the decision: the rows of later slots are not waited for. Errors follow the
+// order of the rule: a bad draft token first, then the rows slot by slot (target before draft); a row of a
+// later slot is checked by the sequence's find. The draw's words are those of decide().
+template <int DT, bool VEC>
+__device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, int32_t o0, int lane, const float* tab) {
+    const int32_t t0 = o0 + b;
+    const int nch = P.nchA;
+    const float K = P.K_hi;
+    const bool pm = P.pm;
+    int32_t x = 0;
+    uint32_t err = 0;
+    float lt = 0.f, ld = 0.f, u_acc = 0.f, u_draw = 0.f;
+    if (lane < g) {
+        x = __ldg(P.tokens + o0 + lane);
+        if (x < 0 || x >= P.V) {
+            err = 1u << SV_ERR_BAD_TOKEN;
+        } else {
+            lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
+            if (!pm) ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
+        }
+        u_acc = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);
+    }
+    if (lane <= g) u_draw = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 1);
+    err = warp_or(err);
+    // rows (max, sum) of the current slot; the loads of slot s + 1 are issued once slot s's words are in
+    float Mt = -INFINITY, St = 0.f, Md = 0.f, Sd = 1.f;
+    int n = g;
+    auto word_at = [&](int32_t r, int c) { return ld_word(P.partials + (size_t)r * nch + c); };
+    for (int s = 0; s <= g && !err; ++s) {
+        const bool hd = !pm && s < g;
+        const int32_t rt = prog_q(P, b, s, false), rd = prog_q(P, b, s, true);
+        float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int c = c0 + lane;
+            const bool in = c < nch;
+            PartialWord wt = in ? word_at(rt, c) : 1ull, wd = in && hd ? word_at(rd, c) : 1ull;
+            uint32_t spins = 0, nsl = 64;
+            while (__any_sync(0xFFFFFFFFu, wt == 0 || wd == 0)) {
+                if (++spins > P.spin) {
+                    if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+                    err = 1u << SV_ERR_TIMEOUT;
+                    break;
+                }
+                __nanosleep(nsl);
+                nsl = nsl < 256 ? 2 * nsl : 256;
+                if (wt == 0) wt = word_at(rt, c);
+                if (wd == 0) wd = word_at(rd, c);
+            }
+            if (err) break;
+            if (in) {  // merge the lane's chunks (online rescaling; a NaN sum stays NaN)
+                const float qm = __uint_as_float((uint32_t)wt), qs = __uint_as_float((uint32_t)(wt >> 32));
+                if (c0 == 0) { mt = qm; st = qs; }
+                else if (qs != qs) { st = qs; mt = fmaxf(mt, qm); }
+                else if (st == st) merge_ms<true>(mt, st, qm, qs, K);
+                if (hd) {
+                    const float rm = __uint_as_float((uint32_t)wd), rs = __uint_as_float((uint32_t)(wd >> 32));
+                    if (c0 == 0) { md = rm; sd = rs; }
+                    else if (rs != rs) { sd = rs; md = fmaxf(md, rm); }
+                    else if (sd == sd) merge_ms<true>(md, sd, rm, rs, K);
+                }
+            }
+        }
+        if (err) break;
+        // the two rows' reductions, interleaved
+        float MT = mt, MD = md;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            MT = fmaxf(MT, __shfl_xor_sync(0xFFFFFFFFu, MT, o));
+            MD = fmaxf(MD, __shfl_xor_sync(0xFFFFFFFFu, MD, o));
+        }
+        float ST = st != st ? st : (mt == -INFINITY ? 0.f : st * exp2_fma((mt - MT) * K));
+        float SD = sd != sd ? sd : (md == -INFINITY ? 0.f : sd * exp2_fma((md - MD) * K));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            ST += __shfl_xor_sync(0xFFFFFFFFu, ST, o);
+            SD += __shfl_xor_sync(0xFFFFFFFFu, SD, o);
+        }
+        // the first failing row in order: target before draft (a NaN or +inf row is reported as such)
+        if (ST != ST) err = 1u << SV_ERR_NONFINITE;
+        else if (MT == -INFINITY) err = 1u << SV_ERR_EMPTY_ROW;
+        else if (hd && SD != SD) err = 1u << SV_ERR_NONFINITE;
+        else if (hd && MD == -INFINITY) err = 1u << SV_ERR_EMPTY_ROW;
+        if (err) break;
+        Mt = MT;
+        St = ST;
+        if (hd) {
+            Md = MD;
+            Sd = SD;
+        }
+        if (s == g) break;  // every draft accepted: the bonus draw from target row g
+        // the accept test of slot s: p(x) and q(x) from the precise exponential of the exact logit gaps
+        const float lts = __shfl_sync(0xFFFFFFFFu, lt, s), lds = __shfl_sync(0xFFFFFFFFu, ld, s);
+        const float us = __shfl_sync(0xFFFFFFFFu, u_acc, s);
+        const ff2 e = exp2_ff2(make_float2(lts, lds), make_float2(Mt, pm ? 0.f : Md), exp_const(P), tab);
+        const float px = div_fma(e.hi.x + e.lo.x, St);
+        const float qx = pm ? 1.f : div_fma(e.hi.y + e.lo.y, Sd);
+        if (!(us * qx < px)) {
+            n = s;
+            break;
+        }
+    }
+    if (err) {
+        if (lane == 0) {
+            atomicOr(P.status, err);
+            P.out_n[b] = -1;
+        }
+        put_task(P, b, lane, kModeNone, 0, 0.f, 0.f, 1.f, 0.f, 0);
+        for (int32_t j = lane; j <= g; j += 32) P.out_tokens[t0 + j] = -1;
+        commit_seq(P, b, -1, -1, -1, lane);
+        enqueue_decided(P, b, lane);
+        return;
+    }
+    const float un = __shfl_sync(0xFFFFFFFFu, u_draw, n);
+    const int32_t xn = __shfl_sync(0xFFFFFFFFu, x, n < g ? n : 0);
+    if (pm) {
+        put_task(P, b, lane, n < g ? kModeResidualPM : kModeBonus, n, Mt, 0.f, n < g ? __int_as_float(xn + 1) : 1.f,
+                 un, n);
+    } else {
+        float rho = 1.f;
+        if (n < g) {
+            rho = div_fma(St, Sd);
+            if (draw_uses_table<DT, VEC>(P, kModeResidual, Mt, Md)) rho *= exp2_fma((Mt - Md) * K);
+        }
+        put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, Mt, n < g ? Md : 0.f, rho, un, n);
+    }
+    enqueue_decided(P, b, lane);
+}
+
+// The check of a sequence's rows after its emitting slot n (P.prog), in the rule's order (target row
+// s, then draft row s, for s = n + 1 .. g): polled until written (the streamers never wait), then the first
+// row with a NaN / +inf chunk (SV_ERR_NONFINITE) or without a value above -inf (SV_ERR_EMPTY_ROW). Returns
+// that error's bit, 0 when every row is clean, or the time-out bit.
+__device__ __noinline__ uint32_t check_dead_rows(const Params& P, int32_t b, int32_t g, int32_t n, int lane) {
+    const int nd = P.pm ? g - n : (n < g ? 2 * (g - n) - 1 : 0);  // at most 61 rows
+    if (nd <= 0) return 0u;
+    const int nch = P.nchA;
+    unsigned long long nan = 0ull, live = 0ull;
+    const int total = nd * nch;
+    for (int w0 = 0; w0 < total; w0 += 32) {
+        const int w = w0 + lane;
+        const bool in = w < total;
+        const int i = in ? w / nch : 0, c = in ? w - i * nch : 0;
+        const int32_t s = n + 1 + (P.pm ? i : i >> 1);
+        const int32_t r = prog_q(P, b, s, !P.pm && (i & 1));
+        PartialWord q = in ? ld_word(P.partials + (size_t)r * nch + c) : 1ull;
+        uint32_t spins = 0, nsl = 64;
+        while (__any_sync(0xFFFFFFFFu, q == 0)) {
+            if (++spins > P.spin) {
+                if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+                return 1u << SV_ERR_TIMEOUT;
+            }
+            __nanosleep(nsl);
+            nsl = nsl < 256 ? 2 * nsl : 256;
+            if (q == 0) q = ld_word(P.partials + (size_t)r * nch + c);
+        }
+        if (in) {
+            const float m = __uint_as_float((uint32_t)q), sm = __uint_as_float((uint32_t)(q >> 32));
+            if (sm != sm) nan |= 1ull << i;
+            if (m > -INFINITY) live |= 1ull << i;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        nan |= __shfl_xor_sync(0xFFFFFFFFu, nan, o);
+        live |= __shfl_xor_sync(0xFFFFFFFFu, live, o);
+    }
+    const unsigned long long all = nd == 64 ? ~0ull : (1ull << nd) - 1ull;
+    const unsigned long long bad = (nan | ~live) & all;
+    if (!bad) return 0u;
+    const int i = __ffsll((long long)bad) - 1;
+    return (nan >> i) & 1ull ? 1u << SV_ERR_NONFINITE : 1u << SV_ERR_EMPTY_ROW;
+}
+
 // ------------------------------------------------------------------------------------------------
 // Sampler weights
 // ------------------------------------------------------------------------------------------------
@@ -1376,6 +1583,14 @@ __device__ __noinline__ void find(const Params& P, int32_t b, const TaskInfo tk,
     }
     // every output of the sequence: the accepted tokens, the drawn one, -1 after it
     const int32_t g = __ldg(P.offs + b + 1) - o0, npos = tk.npos;
+    if (P.prog) {  // slot order: the rows after the emitting slot pass their check first
+        const uint32_t e = check_dead_rows(P, b, g, tk.n, lane);
+        if (e) {
+            if (lane == 0) atomicOr(P.status, e);
+            fail_outputs(P, b, lane);
+            return;
+        }
+    }
     if (lane <= g) P.out_tokens[o0 + b + lane] = lane < npos ? acc_tok : (lane == npos ? token : -1);
     if (P.out_path && lane < g) P.out_path[o0 + lane] = lane < npos ? acc_node : -1;
     if (lane == 0) {
@@ -1569,8 +1784,28 @@ __device__ __noinline__ void s_accumulate(const Params& P, int32_t b, int i, con
 template <int DT, bool VEC>
 __device__ void s_task(const Params& P, uint32_t c, const float* tab, const char* vt, int lane) {
     // c / nS by a multiply-high with floor(2^64 / nS) + 1: exact for c, nS < 2^32 (no MUFU reciprocal)
-    const int32_t b = P.nS == 1 ? (int32_t)c : (int32_t)__umul64hi((unsigned long long)c, P.nS_recip);
+    int32_t b = P.nS == 1 ? (int32_t)c : (int32_t)__umul64hi((unsigned long long)c, P.nS_recip);
     const int i = (int)(c - (uint32_t)b * (uint32_t)P.nS);
+    if (P.prog) {  // slot order: c / nS is a position of the decision-order queue
+        const uint32_t p = (uint32_t)b;
+        uint32_t e = ld_u32(P.order + p);
+        uint32_t spins = 0, ns = 32;
+        while (__any_sync(0xFFFFFFFFu, e == 0u)) {
+            if (++spins > P.spin) {  // give the position up (its decision fails its sequence) unless it came
+                if (lane == 0) {
+                    e = atomicCAS(P.order + p, 0u, kOrderLost);
+                    if (e == 0u) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
+                }
+                e = __shfl_sync(0xFFFFFFFFu, e, 0);
+                break;
+            }
+            __nanosleep(ns);
+            ns = ns < 256 ? 2 * ns : 256;
+            e = ld_u32(P.order + p);
+        }
+        if (e == 0u || e == kOrderLost) return;
+        b = (int32_t)(e - 1u);
+    }
     const int32_t o0 = __ldg(P.offs + b);
     TaskInfo tk;
     if (!get_task(P, b, lane, tk)) {
@@ -1653,6 +1888,13 @@ __device__ __forceinline__ const char* stat_row_src(const Params& P, int32_t r, 
     return (const char*)(draft ? P.draft : P.target) + (row * (size_t)P.V + (size_t)ch * kAChunk) * esz;
 }
 
+// Source of slot-order row q (see prog_q): from the row map entry.
+__device__ __forceinline__ const char* prog_row_src(const Params& P, int32_t q, int32_t ch, const int32_t* rows) {
+    const uint32_t v = (uint32_t)rows[q];
+    const size_t row = v & 0xFFFu;
+    return (const char*)(v >> 31 ? P.draft : P.target) + (row * (size_t)P.V + (size_t)ch * kAChunk) * 2;
+}
+
 template <int DT, bool GREEDY>
 __device__ __forceinline__ ATask a_task_at(const Params& P, uint32_t t, int32_t& cur, const int32_t* bases,
                                            const int32_t* rows) {
@@ -1698,9 +1940,10 @@ __device__ void lead_decide(const Params& P, int32_t b, const int32_t* bases, co
 
 // A streamer warp on the bulk-copy path: its statistics tasks (statically strided over all streamers)
 // arrive through a ring of kStages shared-memory stages filled by 1-D bulk copies, so up to
-// kStages - 1 tasks stay in flight while one is reduced, without holding registers. The (row, chunk)
-// of the task being reduced and of the task that refills its stage advance incrementally; the refill's
-// source is resolved before waiting on the stage, so its lookups overlap the wait and the reduction.
+// kStages - 1 tasks stay in flight while one is reduced, without holding registers. The position (row or
+// slot-order index, chunk) of the task being reduced and of the task that refills its stage advance
+// incrementally; the refill's source is resolved before waiting on the stage, so its lookups overlap the
+// wait and the reduction. In slot order (P.prog) the positions skip holes.
 __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, const int32_t* bases,
                             const int32_t* rows, int warp, int lane) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(dsmem + kStreamWarps * kStages * kStageBytes) + warp * kStages;
@@ -1709,13 +1952,28 @@ __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, 
     const uint32_t sw = blockIdx.x * kStreamWarps + warp;
     const uint32_t nch = (uint32_t)P.nchA;
     const uint32_t dr = SW / nch, dc = SW % nch;
-    auto advance = [&](uint32_t& r, uint32_t& c) {
-        r += dr;
-        c += dc;
-        if (c >= nch) {
-            c -= nch;
-            ++r;
+    const bool prog = P.prog;
+    struct Pos {
+        uint32_t t, q, c;  // task index, row (slot-order index in slot order), chunk
+    };
+    auto advance = [&](Pos& p) {
+        p.t += SW;
+        p.q += dr;
+        p.c += dc;
+        if (p.c >= nch) {
+            p.c -= nch;
+            ++p.q;
         }
+    };
+    // the statistics row of p (slot order: skipping holes)
+    auto settle = [&](Pos& p) -> int32_t {
+        if (!prog) return (int32_t)p.q;
+        for (; p.t < nA; advance(p))
+            if ((uint32_t)rows[p.q] != kProgHole) return (int32_t)p.q;
+        return -1;
+    };
+    auto src_of = [&](int32_t r, uint32_t c, int32_t& cur) {
+        return prog ? prog_row_src(P, r, (int32_t)c, rows) : stat_row_src<SV_BF16, false>(P, r, (int32_t)c, cur, bases, rows);
     };
     auto len_of = [&](uint32_t c) { return min(kAChunk, P.V - (int)c * kAChunk); };
     if (lane == 0) {
@@ -1728,27 +1986,29 @@ __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, 
         mbar_arrive_expect_tx(&bars[s], bytes);
         bulk_g2s(bufs + (size_t)s * kStageBytes, src, bytes, &bars[s]);
     };
-    uint32_t rp = sw / nch, cp = sw % nch;  // task being reduced
-    uint32_t ri = rp, ci = cp;              // next task to issue
+    Pos rp{sw, sw / nch, sw % nch};  // task being reduced
+    int32_t rr = settle(rp);
+    Pos ip = rp;                     // next task to issue
     for (int s = 0; s < kStages; ++s) {
-        if (sw + s * SW < nA) {
-            const char* src = stat_row_src<SV_BF16, false>(P, (int32_t)ri, (int32_t)ci, cur, bases, rows);
-            if (lane == 0) issue(src, (uint32_t)len_of(ci) * 2u, s);
+        const int32_t ir = settle(ip);
+        if (ip.t < nA) {
+            const char* src = src_of(ir, ip.c, cur);
+            if (lane == 0) issue(src, (uint32_t)len_of(ip.c) * 2u, s);
+            advance(ip);
         }
-        advance(ri, ci);
     }
     uint32_t parity = 0;  // bit s: parity of stage s's next completion
     int k = 0;
-    for (uint32_t t = sw; t < nA; t += SW, ++k) {
+    for (; rp.t < nA; ++k) {
         const int s = k % kStages;
-        const uint32_t tn = t + kStages * SW;
+        const int32_t nr = settle(ip);
+        const bool more = ip.t < nA;
         const char* nsrc = nullptr;
         uint32_t nbytes = 0;
-        if (tn < nA) {
-            nsrc = stat_row_src<SV_BF16, false>(P, (int32_t)ri, (int32_t)ci, cur, bases, rows);
-            nbytes = (uint32_t)len_of(ci) * 2u;
+        if (more) {
+            nsrc = src_of(nr, ip.c, cur);
+            nbytes = (uint32_t)len_of(ip.c) * 2u;
         }
-        advance(ri, ci);
         // one verdict for the whole warp: a time-out seen by some lanes only must not split it (a copy
         // always lands: this bound is the library's, never a caller's)
         const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bars[s], (parity >> s) & 1u, kSpinLimit));
@@ -1756,17 +2016,21 @@ __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, 
             // a copy that does not land: report, give every copy in flight (this stage's included) its
             // own bound to land before the shared memory is left, stop streaming
             if (lane == 0) atomicOr(P.status, 1u << SV_ERR_TIMEOUT);
-            for (int q = 0; q < kStages; ++q) {
-                const int s2 = (k + q) % kStages;
-                if (t + q * SW < nA) mbar_wait(&bars[s2], (parity >> s2) & 1u, kSpinLimit);
+            Pos q = rp;
+            for (int i = 0; i < kStages; ++i) {
+                settle(q);
+                if (q.t >= nA) break;
+                const int s2 = (k + i) % kStages;
+                mbar_wait(&bars[s2], (parity >> s2) & 1u, kSpinLimit);
+                advance(q);
             }
             return;
         }
         parity ^= 1u << s;
         ATask at;
-        at.r = (int32_t)rp;
-        at.ch = (int32_t)cp;
-        at.len = len_of(cp);
+        at.r = rr;
+        at.ch = (int32_t)rp.c;
+        at.len = len_of(rp.c);
         // the stage is refilled only once its task is reduced: with one copy per streamer in flight during
         // the reduction the stream keeps HBM busy without queueing the handoff loads of the decisions and
         // finds behind it (refilling right after the stage is read into registers measured slower)
@@ -1774,12 +2038,14 @@ __device__ void stream_bulk(const Params& P, uint32_t nA, unsigned char* dsmem, 
         load_stage(bufs + (size_t)s * kStageBytes, at.len, lane, v);
         const SegStats st = stats_bf16(v, P.K_hi);
         __syncwarp();
-        if (lane == 0 && tn < nA) {
+        if (lane == 0 && more) {
             fence_proxy_async_smem();  // this stage's reads come before the copy that overwrites it
             issue(nsrc, nbytes, s);
         }
+        if (more) advance(ip);
         a_finish<false>(P, at, st, lane);
-        advance(rp, cp);
+        advance(rp);
+        rr = settle(rp);
     }
 }
 
@@ -1816,9 +2082,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_verify(const __grid_constant__ 
         bad |= !ok;
         const int32_t sb = GREEDY || P.pm ? o0 + b : 2 * o0 + b;
         if (cache) s_base[b] = sb;
-        if (!GREEDY && !P.pm && ok)  // row map entries that fit (it is used only when every row fits)
+        if (kBulk && P.prog) {  // slot-order map (its size is checked by the host): every q of sequence b
+            if (ok)
+                for (int32_t sl = 0; sl <= P.max_gamma; ++sl) {
+                    const uint32_t id = (uint32_t)b << 12 | (uint32_t)sl << 22;
+                    s_row[prog_q(P, b, sl, false)] = (int32_t)(sl <= g ? id | (uint32_t)(o0 + b + sl) : kProgHole);
+                    if (!P.pm && sl < P.max_gamma)
+                        s_row[prog_q(P, b, sl, true)] =
+                            (int32_t)(sl < g ? 0x80000000u | id | (uint32_t)(o0 + sl) : kProgHole);
+                }
+        } else if (!GREEDY && !P.pm && ok) {  // row map entries that fit (used only when every row fits)
             for (int32_t j = 0; j <= 2 * g && sb + j < kRowCache; ++j)
                 s_row[sb + j] = j <= g ? o0 + b + j : (int32_t)(0x80000000u | (uint32_t)(o0 + j - g - 1));
+        }
     }
     const int32_t* bases = cache ? s_base : nullptr;
     if (__syncthreads_or(bad) || s_bad) {
@@ -1833,9 +2109,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_verify(const __grid_constant__ 
     }
     const int32_t oB = __ldg(P.offs + P.B);
     // the host bounds rows * nchA and B * nS below 2^31
-    const uint32_t nA = (uint32_t)(GREEDY || P.pm ? oB + P.B : 2 * oB + P.B) * (uint32_t)P.nchA;
+    const uint32_t nA = (kBulk && P.prog ? prog_rows(P) : (uint32_t)(GREEDY || P.pm ? oB + P.B : 2 * oB + P.B)) *
+                        (uint32_t)P.nchA;
     const uint32_t nStot = GREEDY ? 0u : (uint32_t)P.B * (uint32_t)P.nS;
-    const int32_t* rows = !GREEDY && !P.pm && 2 * oB + P.B <= kRowCache ? s_row : nullptr;
+    const int32_t* rows = (kBulk && P.prog) || (!GREEDY && !P.pm && 2 * oB + P.B <= kRowCache) ? s_row : nullptr;
 
     // Statistics. Bulk-copy path: the upper kStreamWarps warps of the CTA stream while the lower ones
     // build the sampler's value table, then decide and take sampler tasks. Other paths: every warp streams
@@ -1881,7 +2158,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_verify(const __grid_constant__ 
     // Cooperative decisions when every CTA holds at most one: the non-streaming warps of CTA c share the
     // rows of sequence c (the decision's latency, not its throughput, is what the step waits for)
     const bool coop = kBulk && (uint32_t)P.B <= gridDim.x;
-    if (coop) {
+    if (kBulk && P.prog) {  // slot order: one warp decides a sequence, slot by slot
+        const uint32_t d = coop ? (warp == 0 ? blockIdx.x : (uint32_t)P.B) : did;
+        if (!streamer)
+            for (uint32_t b = d; b < (uint32_t)P.B; b += coop ? (uint32_t)P.B : ND) {
+                const int32_t s0 = bases[b], s1 = bases[b + 1];
+                const int32_t o0 = P.pm ? s0 - (int32_t)b : (s0 - (int32_t)b) >> 1;
+                const int32_t g = P.pm ? s1 - s0 - 1 : (s1 - s0 - 1) >> 1;
+                decide_prog<DT, VEC>(P, (int32_t)b, g, o0, lane, tab);
+            }
+    } else if (coop) {
         if (!streamer && blockIdx.x < (uint32_t)P.B)
             lead_decide<DT, VEC, GREEDY>(P, (int32_t)blockIdx.x, bases, tab, lane, warp, kWarps - kStreamWarps, &s_coop, 0);
     } else if (!streamer) {
@@ -2034,7 +2320,8 @@ Layout workspace_layout(int32_t B, int32_t V, int32_t max_gamma) {
     L.remw = up(L.groupw + (size_t)B * nS * kGroups * kGroupWords * sizeof(Word));
     L.pathw = up(L.remw + (size_t)B * kMaxRemoved * sizeof(Word));
     L.seqstate = up(L.pathw + (size_t)B * kMaxRemoved * sizeof(Word));
-    L.status = up(L.seqstate + (size_t)B * sizeof(uint32_t));
+    L.order = up(L.seqstate + (size_t)B * sizeof(uint32_t));
+    L.status = up(L.order + (size_t)B * sizeof(uint32_t));
     L.zero_begin = 0;
     L.zero_end = L.status;
     L.total = up(L.status + sizeof(uint32_t));

@@ -384,11 +384,9 @@ constexpr int kShSumThreads = 256;
 constexpr int kShRecSmem = 256;  // gathered sums records a finishing CTA stages in shared memory (8 KB)
 static_assert(kShChunk == 2 * 16 * kShSumThreads, "16 column pairs per thread and chunk");
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
-}
 __device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    cp_async_commit();
+    cp_async_wait<0>();
 }
 
 // The accumulation over the thread's column pairs; LOAD(k) gives the logits of columns k, k + 1 of the p
