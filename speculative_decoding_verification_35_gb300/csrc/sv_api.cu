@@ -109,9 +109,12 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.tab_mlo = greedy ? 1.f : (float)(-63.75 + 60.0 / (double)K_hi);
     P.tab_mhi = greedy ? 0.f : (float)std::min(63.75, 96.0 / (double)K_hi);
     {
+        // Slot order pays where drafts have their own rows (their acceptance varies); point-mass batches,
+        // whose planted drafts are mostly accepted, measured faster in sequence order (37.6 against 39.2 us
+        // per step at B = 64, gamma = 5, V = 128256), so they keep it.
         const bool row_dbg = debug && (debug->row_lse || debug->row_argmax || debug->p_x || debug->q_x || debug->beta);
-        P.prog = !greedy && dtype == SV_BF16 && vec && !parents && !row_dbg && B < kBaseCache &&
-                 (int64_t)B * ((P.pm ? 1 : 2) * (int64_t)max_gamma + 1) <= kRowCache;
+        P.prog = !greedy && !P.pm && dtype == SV_BF16 && vec && !parents && !row_dbg && B < kBaseCache &&
+                 (int64_t)B * (2 * (int64_t)max_gamma + 1) <= kRowCache;
     }
     P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;
     P.seed = seed;

@@ -900,19 +900,18 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     }
 }
 
-// Slot order (P.prog): the statistics rows are numbered by slot, q = s * per + k with per = B (point-mass
-// drafts) or 2 B: k = b for the target row of slot s of sequence b, k = B + b for its draft row; the last
-// slot (s = max_gamma) holds target rows only. A q that sequence b does not have (s > gamma_b, or the draft
-// row of slot gamma_b) is a hole. The partial words are indexed by q; the CTA's row map holds, per q, the
+// Slot order (P.prog, batches with draft rows): the statistics rows are numbered by slot, q = 2 B s + k:
+// k = b for the target row of slot s of sequence b, k = B + b for its draft row; the last slot
+// (s = max_gamma) holds target rows only. A q that sequence b does not have (s > gamma_b, or the draft row
+// of slot gamma_b) is a hole. The partial words are indexed by q; the CTA's row map holds, per q, the
 // logits row (bits 0-11), the sequence (bits 12-21), the slot (bits 22-26) and the draft flag (bit 31),
 // or kProgHole.
 constexpr uint32_t kProgHole = 0x7FFFFFFFu;
-__device__ __forceinline__ uint32_t prog_per(const Params& P) { return P.pm ? (uint32_t)P.B : 2u * (uint32_t)P.B; }
 __device__ __forceinline__ uint32_t prog_rows(const Params& P) {
-    return prog_per(P) * (uint32_t)P.max_gamma + (uint32_t)P.B;
+    return (2u * (uint32_t)P.max_gamma + 1u) * (uint32_t)P.B;
 }
 __device__ __forceinline__ int32_t prog_q(const Params& P, int32_t b, int32_t s, bool draft) {
-    return s * (int32_t)prog_per(P) + (draft ? P.B : 0) + b;
+    return (2 * s + (draft ? 1 : 0)) * P.B + b;
 }
 
 // Slot order: a published decision takes the next position of the decision-order queue, from which the
@@ -927,7 +926,7 @@ __device__ __noinline__ void enqueue_decided(const Params& P, int32_t b, int lan
     if (__shfl_sync(0xFFFFFFFFu, lost, 0)) give_up_seq(P, b, lane);
 }
 
-// Decision in slot order (P.prog, linear sampled drafts; one warp): slot s is tested as soon as its rows'
+// Decision in slot order (P.prog, linear sampled drafts with draft rows; one warp): slot s is tested as soon as its rows'
 // statistics are in (target row s and draft row s, which the slot-order stream delivers together), and
 // the first rejection ends the decision: the rows of later slots are not waited for. Errors follow the
 // order of the rule: a bad draft token first, then the rows slot by slot (target before draft); a row of a
@@ -937,7 +936,6 @@ __device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, 
     const int32_t t0 = o0 + b;
     const int nch = P.nchA;
     const float K = P.K_hi;
-    const bool pm = P.pm;
     int32_t x = 0;
     uint32_t err = 0;
     float lt = 0.f, ld = 0.f, u_acc = 0.f, u_draw = 0.f;
@@ -947,7 +945,7 @@ __device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, 
             err = 1u << SV_ERR_BAD_TOKEN;
         } else {
             lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
-            if (!pm) ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
+            ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
         }
         u_acc = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);
     }
@@ -958,7 +956,7 @@ __device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, 
     int n = g;
     auto word_at = [&](int32_t r, int c) { return ld_word(P.partials + (size_t)r * nch + c); };
     for (int s = 0; s <= g && !err; ++s) {
-        const bool hd = !pm && s < g;
+        const bool hd = s < g;
         const int32_t rt = prog_q(P, b, s, false), rd = prog_q(P, b, s, true);
         float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
         for (int c0 = 0; c0 < nch; c0 += 32) {
@@ -1022,9 +1020,9 @@ __device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, 
         // the accept test of slot s: p(x) and q(x) from the precise exponential of the exact logit gaps
         const float lts = __shfl_sync(0xFFFFFFFFu, lt, s), lds = __shfl_sync(0xFFFFFFFFu, ld, s);
         const float us = __shfl_sync(0xFFFFFFFFu, u_acc, s);
-        const ff2 e = exp2_ff2(make_float2(lts, lds), make_float2(Mt, pm ? 0.f : Md), exp_const(P), tab);
+        const ff2 e = exp2_ff2(make_float2(lts, lds), make_float2(Mt, Md), exp_const(P), tab);
         const float px = div_fma(e.hi.x + e.lo.x, St);
-        const float qx = pm ? 1.f : div_fma(e.hi.y + e.lo.y, Sd);
+        const float qx = div_fma(e.hi.y + e.lo.y, Sd);
         if (!(us * qx < px)) {
             n = s;
             break;
@@ -1042,18 +1040,12 @@ __device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, 
         return;
     }
     const float un = __shfl_sync(0xFFFFFFFFu, u_draw, n);
-    const int32_t xn = __shfl_sync(0xFFFFFFFFu, x, n < g ? n : 0);
-    if (pm) {
-        put_task(P, b, lane, n < g ? kModeResidualPM : kModeBonus, n, Mt, 0.f, n < g ? __int_as_float(xn + 1) : 1.f,
-                 un, n);
-    } else {
-        float rho = 1.f;
-        if (n < g) {
-            rho = div_fma(St, Sd);
-            if (draw_uses_table<DT, VEC>(P, kModeResidual, Mt, Md)) rho *= exp2_fma((Mt - Md) * K);
-        }
-        put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, Mt, n < g ? Md : 0.f, rho, un, n);
+    float rho = 1.f;
+    if (n < g) {
+        rho = div_fma(St, Sd);
+        if (draw_uses_table<DT, VEC>(P, kModeResidual, Mt, Md)) rho *= exp2_fma((Mt - Md) * K);
     }
+    put_task(P, b, lane, n < g ? kModeResidual : kModeBonus, n, Mt, n < g ? Md : 0.f, rho, un, n);
     enqueue_decided(P, b, lane);
 }
 
@@ -1062,7 +1054,7 @@ __device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, 
 // row with a NaN / +inf chunk (SV_ERR_NONFINITE) or without a value above -inf (SV_ERR_EMPTY_ROW). Returns
 // that error's bit, 0 when every row is clean, or the time-out bit.
 __device__ __noinline__ uint32_t check_dead_rows(const Params& P, int32_t b, int32_t g, int32_t n, int lane) {
-    const int nd = P.pm ? g - n : (n < g ? 2 * (g - n) - 1 : 0);  // at most 61 rows
+    const int nd = n < g ? 2 * (g - n) - 1 : 0;  // at most 61 rows
     if (nd <= 0) return 0u;
     const int nch = P.nchA;
     unsigned long long nan = 0ull, live = 0ull;
@@ -1071,8 +1063,8 @@ __device__ __noinline__ uint32_t check_dead_rows(const Params& P, int32_t b, int
         const int w = w0 + lane;
         const bool in = w < total;
         const int i = in ? w / nch : 0, c = in ? w - i * nch : 0;
-        const int32_t s = n + 1 + (P.pm ? i : i >> 1);
-        const int32_t r = prog_q(P, b, s, !P.pm && (i & 1));
+        const int32_t s = n + 1 + (i >> 1);
+        const int32_t r = prog_q(P, b, s, i & 1);
         PartialWord q = in ? ld_word(P.partials + (size_t)r * nch + c) : 1ull;
         uint32_t spins = 0, nsl = 64;
         while (__any_sync(0xFFFFFFFFu, q == 0)) {
@@ -2087,7 +2079,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_verify(const __grid_constant__ 
                 for (int32_t sl = 0; sl <= P.max_gamma; ++sl) {
                     const uint32_t id = (uint32_t)b << 12 | (uint32_t)sl << 22;
                     s_row[prog_q(P, b, sl, false)] = (int32_t)(sl <= g ? id | (uint32_t)(o0 + b + sl) : kProgHole);
-                    if (!P.pm && sl < P.max_gamma)
+                    if (sl < P.max_gamma)
                         s_row[prog_q(P, b, sl, true)] =
                             (int32_t)(sl < g ? 0x80000000u | id | (uint32_t)(o0 + sl) : kProgHole);
                 }

@@ -1,11 +1,12 @@
 """GPU parity of the slot-order verify path against the fp64 oracle, through the C ABI.
 
-Calls without per-row debug outputs on bf16 rows with 16-byte alignment (sampled, linear drafts, row map in
-shared memory) stream the statistics slot by slot and decide each sequence at its first rejection; the rows
-after it are only checked for NaN / +inf / empty, by the sequence's find. These tests run that path (no debug
-arrays) on full-size and reduced batches, ragged gammas and gamma = 0, more sequences than CTAs, a
-max_gamma above the batch's (empty slots), errors planted in rows before and after the first rejection,
-and waits that run out. Outputs and status must equal the oracle's under the usual rule.
+Calls without per-row debug outputs on bf16 rows with 16-byte alignment (sampled, linear drafts with draft
+rows, row map in shared memory) stream the statistics slot by slot and decide each sequence at its first
+rejection; the rows after it are checked for NaN / +inf / empty by the sequence's find. These tests run that
+path (no debug arrays) on full-size and reduced batches, ragged gammas and gamma = 0, more sequences than
+CTAs, a max_gamma above the batch's (empty slots), errors planted in rows before and after the first
+rejection, and waits that run out. Point-mass batches keep sequence order; their cases here run that path
+without debug arrays. Outputs and status must equal the oracle's under the usual rule.
 """
 import numpy as np
 import pytest
