@@ -634,11 +634,19 @@ __device__ __noinline__ void tree_sampled(const Params& P, int32_t b, int32_t g,
 // both uniforms of every slot) is fetched before the partials are polled. Rows are reduced 8 at a
 // time without control flow between them, so their shuffle trees overlap.
 // ------------------------------------------------------------------------------------------------
+// Order key of a failing statistics row jr of a sequence with g drafts (code in the low 4 bits): the rule
+// reads target row i, then draft row i (rows 0..g are the target rows, g + 1 + i draft row i)
+__device__ __forceinline__ uint32_t row_key(int jr, int g, uint32_t code) {
+    const uint32_t ord = jr <= g ? 2u * (uint32_t)jr : 2u * (uint32_t)(jr - g - 1) + 1u;
+    return ord << 4 | code;
+}
+
 // Row statistics shared by the warps of a cooperative decision: (max, sum) per statistics row, and
 // the error bits of the rows; two sets, used by alternate decisions of the CTA.
 struct CoopRows {
     float2 rs[2][2 * 32];
-    uint32_t err[2];
+    uint32_t err[2];  // time-outs (OR)
+    uint32_t key[2];  // the first failing row (minimum of row_key; ~0: none)
 };
 
 // nsub > 1: a cooperative decision. Warp wsub of the nsub deciding warps of the CTA reduces the rows
@@ -668,7 +676,9 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
     PartialWord qn[8];
     load_block(0, 0, qn);
     int32_t x = 0;
-    uint32_t err = 0;
+    uint32_t err = 0;    // time-outs
+    uint32_t tcode = 0;  // this slot's draft error: a bad token, else (token tree) a bad parent
+    uint32_t rkey = ~0u; // the first failing row of this warp's rows, as row_key
     float lt = 0.f, ld = 0.f, u_acc = 0.f, u_draw = 0.f;
     // the node whose target row tests slot `lane`: its parent in a token tree, the slot itself otherwise
     int32_t par = lane;
@@ -677,11 +687,11 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         if (P.parents) {
             par = __ldg(P.parents + o0 + lane);
             if (par < 0 || par > lane) {
-                err |= 1u << SV_ERR_BAD_OFFSETS;
+                tcode = SV_ERR_BAD_OFFSETS;
                 par = lane;
             }
         }
-        if (x < 0 || x >= P.V) err |= 1u << SV_ERR_BAD_TOKEN;
+        if (x < 0 || x >= P.V) tcode = SV_ERR_BAD_TOKEN;
         else if (!GREEDY) {
             lt = logit_at<DT>(P.target, (size_t)(t0 + par) * P.V + x);
             if (!P.pm) ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
@@ -789,7 +799,8 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
             // a row with a NaN or +inf is reported as such, not as empty (both fail the sequence)
             const uint32_t rf = GREEDY ? (F[k] | (M[k] == INFINITY ? 1u << SV_ERR_NONFINITE : 0u))
                                        : (S[k] != S[k] ? 1u << SV_ERR_NONFINITE : 0u);
-            if (in) err |= rf | (M[k] == -INFINITY && !rf ? 1u << SV_ERR_EMPTY_ROW : 0u);
+            const uint32_t rc = rf ? SV_ERR_NONFINITE : (M[k] == -INFINITY ? SV_ERR_EMPTY_ROW : 0u);
+            if (in && rc) rkey = min(rkey, row_key(jr, g, rc));
             if (nsub > 1) {
                 if (in && lane == 0) co->rs[set][jr] = make_float2(M[k], GREEDY ? 0.f : S[k]);
             } else {
@@ -799,11 +810,14 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         }
     }
     err = warp_or(err);
+    rkey = __reduce_min_sync(0xFFFFFFFFu, rkey);
     if (nsub > 1) {  // meet the other deciding warps; warp 0 continues with every row's statistics
         if (lane == 0 && err) atomicOr(&co->err[set], err);
+        if (lane == 0 && rkey != ~0u) atomicMin(&co->key[set], rkey);
         asm volatile("bar.sync 1, %0;" ::"r"(32 * nsub) : "memory");
         if (wsub != 0) return;
         err = co->err[set];
+        rkey = co->key[set];
         if (lane < nrows_all) {
             const float2 r0 = co->rs[set][lane];
             my_m0 = r0.x;
@@ -815,7 +829,17 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
             my_s1 = r1.y;
         }
         __syncwarp();
-        if (lane == 0) co->err[set] = 0u;  // read by every lane above; cleared for the set's next use
+        if (lane == 0) {  // read by every lane above; cleared for the set's next use
+            co->err[set] = 0u;
+            co->key[set] = ~0u;
+        }
+    }
+    // the failing sequence's code, in the rule's order: the first slot with a bad draft token (a token tree:
+    // or a bad parent), else the first failing row (target row i, then draft row i); time-outs added
+    {
+        const uint32_t tb = __ballot_sync(0xFFFFFFFFu, tcode != 0u);
+        const uint32_t tc = tb ? __shfl_sync(0xFFFFFFFFu, tcode, __ffs(tb) - 1) : 0u;
+        err |= tc ? 1u << tc : (rkey != ~0u ? 1u << (rkey & 15u) : 0u);
     }
     if (err) {
         if (lane == 0) {
@@ -2058,6 +2082,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_verify(const __grid_constant__ 
     if (tid == 0) {
         s_bad = __ldg(P.offs) != 0;
         s_coop.err[0] = s_coop.err[1] = 0u;
+        s_coop.key[0] = s_coop.key[1] = ~0u;
     }
     __syncthreads();
     // every CTA checks the whole CSR structure before any row is read (and caches small batches' row

@@ -91,7 +91,7 @@ def _rows(b, s):
 
 
 @pytest.mark.parametrize("pm", [False, True])
-def test_slot_order_errors_before_and_after_the_rejection(pm):
+def test_errors_report_the_first_failure_in_order(pm):
     name = "pointmass_b64_g5_v128256" if pm else "b64_g5_v128256"
     cases = []
     # NaN in the last target row of sequence 2 (after most first rejections: the find's check)
@@ -125,13 +125,21 @@ def test_slot_order_errors_before_and_after_the_rejection(pm):
         bb.draft[d1, :] = NEG_INF_BF16
         bb.target[t1 + 4, 9] = NAN_BF16
         cases.append(bb)
+    # a bad draft token with a NaN row in the same sequence: the token is reported, not the row
+    bb = synth.make_batch(name, B=5, V=704)
+    t4, _ = _rows(bb, 4)
+    bb.draft_tokens[int(bb.seq_offsets[4]) + 1] = 704
+    bb.target[t4, 0] = NAN_BF16
+    cases.append(bb)
     for bb in cases:
         for step in range(3):
-            g = run_plain(bb, 1, step)
             r = parity.run_oracle(bb, 1, step)
-            assert g["status"] == r.status and r.status != 0, (g["status"], r.status)
-            assert np.array_equal(g["n"], r.num_accepted), (g["n"], r.num_accepted)
-            parity.assert_parity(bb, 1, step, g=g, r=r, check_debug=False)
+            # both paths: without debug arrays (slot order for batches with draft rows) and with them
+            # (sequence order); each reports the first failure in the rule's order, as the oracle does
+            for g in (run_plain(bb, 1, step), parity.run_gpu(bb, 1, step)):
+                assert g["status"] == r.status and r.status != 0, (g["status"], r.status)
+                assert np.array_equal(g["n"], r.num_accepted), (g["n"], r.num_accepted)
+                parity.assert_parity(bb, 1, step, g=g, r=r, check_debug=False)
 
 
 @pytest.mark.parametrize("name,B,V", [("b64_g5_v128256", None, None), ("pointmass_b64_g5_v128256", None, None),
