@@ -703,7 +703,7 @@ def main():
     cfg.update({"l2_policy": rig.l2_policy(),
                 "launch": f"CUDA graph of {G} steps; per step one memset node (handoff regions) and "
                           f"{kernels_per_step} verify kernel",
-                "parallelism": f"{world} independent replica(s), sequences sharded by rank"})
+                "parallelism": f"{world} independent replica(s): each rank verifies its own batch"})
     line = None
     if rank == 0:
         line = {

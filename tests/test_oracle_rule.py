@@ -182,8 +182,9 @@ def test_deterministic_and_thread_count_independent():
     np.testing.assert_array_equal(r1.num_accepted, r2.num_accepted)
 
 
-def test_sharding_by_sequence_ranges_is_exact():
-    """Verifying contiguous sequence ranges separately (global seq index kept) equals the batch."""
+def test_a_sequences_outputs_depend_only_on_its_own_rows():
+    """A sequence's outputs depend only on its own rows (with the same uniforms): zeroing another
+    sequence's target rows leaves every other sequence's outputs unchanged."""
     b = synth.make_batch("ragged_b128_v129280", B=12, V=300)
     full = oracle.verify(b.target, b.draft, b.draft_tokens, b.seq_offsets, b.gammas, b.V, 1.0, 11, 2)
     assert full.status == 0
