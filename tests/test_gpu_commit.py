@@ -142,3 +142,33 @@ def test_fused_update_overflow_and_failed_sequences():
     assert np.array_equal(hist.cpu().numpy(), rh)
     assert np.array_equal(lens.cpu().numpy(), rl)
     assert np.array_equal(nxt.cpu().numpy(), rn)
+
+
+def test_fused_update_with_a_failure_in_rows_after_the_rejection():
+    """Slot-order batches (bf16 rows with draft rows, no debug arrays): a NaN in a sequence's last target
+    row, which most first rejections leave out of the draw, is found by the sequence's find before it writes;
+    the sequence fails (n = -1, history and length kept, next token -1) like the oracle's."""
+    from speculative_decoding_verification_35_gb300 import specverify as sv
+    b = synth.make_batch("b64_g5_v128256", B=9, V=3000)
+    t2 = int(b.seq_offsets[2]) + 2
+    b.target[t2 + int(b.gammas[2]), 11] = 0x7FC0  # sequence 2: NaN in its last target row
+    d = parity.to_device(b)
+    cap = 40
+    call = sv.Call(b.B, b.V, int(b.gammas.max()), b.R_t, b.R_d)
+    lens0 = np.arange(b.B, dtype=np.int32)
+    hist = torch.full((b.B, cap), 55, dtype=torch.int32, device="cuda")
+    lens = torch.from_numpy(lens0.copy()).cuda()
+    nxt = torch.zeros(b.B, dtype=torch.int32, device="cuda")
+    for step in range(3):
+        r = parity.run_oracle(b, 9, step)
+        rh, rl, rn, rs = commit(r.tokens, r.num_accepted, b.seq_offsets, hist.cpu().numpy(), cap, lens.cpu().numpy())
+        assert call.run_fused(d["target"], d["draft"], d["draft_tokens"], d["seq_offsets"], d["gammas"],
+                              b.temperature, 9, step, hist, cap, lens, nxt) == sv.SV_OK
+        torch.cuda.synchronize()
+        assert r.num_accepted[2] == -1 and r.status == 1 << sv.SV_ERR_NONFINITE
+        assert np.array_equal(call.out_n.cpu().numpy(), r.num_accepted)
+        assert np.array_equal(call.out_tokens.cpu().numpy(), r.tokens)
+        assert call.status_bits() == rs | r.status
+        assert np.array_equal(hist.cpu().numpy(), rh)
+        assert np.array_equal(lens.cpu().numpy(), rl)
+        assert np.array_equal(nxt.cpu().numpy(), rn)
