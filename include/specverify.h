@@ -86,6 +86,10 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  *   spin_limit polls after which a wait of one warp on another warp's word gives up (SV_ERR_TIMEOUT);
  *              0 keeps the library's bound (about a second). A small value exists to exercise the
  *              time-out path in tests: a sequence whose wait gave up reports n = -1 and tokens -1.
+ *   order      the order of the statistics stream, for tests of both paths (the outputs are the same):
+ *              0 the library's choice; 1 sequence order; 2 slot order wherever the call allows it (bf16
+ *              rows on 16-byte boundaries, sampling with draft rows, linear drafts, none of the per-row
+ *              fields above, B < 1024 and B (2 max_gamma + 1) <= 2048), whatever the batch's size.
  */
 typedef struct {
     double* row_lse;
@@ -95,6 +99,7 @@ typedef struct {
     double* seq_mass;
     double* beta;
     uint32_t spin_limit;
+    uint32_t order;
 } sv_debug;
 
 /*

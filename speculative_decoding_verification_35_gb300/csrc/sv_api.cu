@@ -109,12 +109,17 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.tab_mlo = greedy ? 1.f : (float)(-63.75 + 60.0 / (double)K_hi);
     P.tab_mhi = greedy ? 0.f : (float)std::min(63.75, 96.0 / (double)K_hi);
     {
-        // Slot order pays where drafts have their own rows (their acceptance varies); point-mass batches,
-        // whose planted drafts are mostly accepted, measured faster in sequence order (37.6 against 39.2 us
-        // per step at B = 64, gamma = 5, V = 128256), so they keep it.
+        // Slot order pays where drafts have their own rows (their acceptance varies) and the statistics
+        // stream is long enough for early decisions to overlap it. Measured per step: B = 64, gamma = 5,
+        // V = 128256 (22528 statistics tasks): 54.3 against 55.2 us; B = 8, V = 32000 (576 tasks, streamed
+        // in ~3 us): 24.6 against 23.1 us, so small batches keep sequence order (kProgMinTasks); point-mass
+        // batches, whose planted drafts are mostly accepted, also measured faster in sequence order (37.6
+        // against 39.2 us at the headline size).
         const bool row_dbg = debug && (debug->row_lse || debug->row_argmax || debug->p_x || debug->q_x || debug->beta);
+        const int64_t rows = (int64_t)B * (2 * (int64_t)max_gamma + 1);
+        const uint32_t order = debug ? debug->order : 0u;
         P.prog = !greedy && !P.pm && dtype == SV_BF16 && vec && !parents && !row_dbg && B < kBaseCache &&
-                 (int64_t)B * (2 * (int64_t)max_gamma + 1) <= kRowCache;
+                 rows <= kRowCache && order != 1u && (order == 2u || rows * P.nchA >= kProgMinTasks);
     }
     P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;
     P.seed = seed;

@@ -36,6 +36,7 @@ constexpr uint32_t kTabCodeHi = 0x427Fu;    // bf16 code of 63.75
 constexpr int kTabHalf = 4096;              // entries per sign
 constexpr int kTabBytes = 2 * kTabHalf * 8; // 64 KB
 constexpr int kTabSmemOffset = (kTmaSmemBytes + 15) & ~15;  // after the stages and their barriers
+constexpr int kProgMinTasks = 4096;  // statistics tasks (bound) from which a sampled call streams in slot order
 constexpr int kTabMinTasks = 2048;  // sampler tasks (sequences x 1024-column tasks) from which a call builds
                                     // the table: below, its build (~4 us at the launch's start) would sit on
                                     // the step's critical path instead of under the stream

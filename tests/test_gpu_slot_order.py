@@ -1,9 +1,9 @@
 """GPU parity of the slot-order verify path against the fp64 oracle, through the C ABI.
 
 Calls without per-row debug outputs on bf16 rows with 16-byte alignment (sampled, linear drafts with draft
-rows, row map in shared memory) stream the statistics slot by slot and decide each sequence at its first
-rejection; the rows after it are checked for NaN / +inf / empty by the sequence's find. These tests run that
-path (no debug arrays) on full-size and reduced batches, ragged gammas and gamma = 0, more sequences than
+rows, row map in shared memory, enough statistics tasks) stream the statistics slot by slot and decide each
+sequence at its first rejection; the rows after it are checked for NaN / +inf / empty by the sequence's find.
+These tests force that path (sv_debug.order = 2, no debug arrays) on full-size and reduced batches, ragged gammas and gamma = 0, more sequences than
 CTAs, a max_gamma above the batch's (empty slots), errors planted in rows before and after the first
 rejection, and waits that run out. Point-mass batches keep sequence order; their cases here run that path
 without debug arrays. Outputs and status must equal the oracle's under the usual rule.
@@ -31,15 +31,15 @@ def built():
     oracle.build()
 
 
-def run_plain(b, seed, step, d=None, max_gamma=None, spin=0):
-    """One call without debug arrays (the slot-order path where it applies); spin > 0 bounds every wait to
-    that many polls through a debug struct that carries no arrays."""
+def run_plain(b, seed, step, d=None, max_gamma=None, spin=0, order=2):
+    """One call without debug arrays, through a debug struct that carries no arrays: the statistics in slot
+    order wherever the call allows it (order 2; 0: the library's choice by size, 1: sequence order); spin > 0
+    bounds every wait to that many polls."""
     from speculative_decoding_verification_35_gb300 import specverify as sv
     d = d or parity.to_device(b)
     mg = int(b.gammas.max()) if max_gamma is None else max_gamma
     call = sv.Call(b.B, b.V, mg, b.R_t, b.R_d)
-    if spin:
-        call.dbg_struct = sv.SvDebug(0, 0, 0, 0, 0, 0, spin)
+    call.dbg_struct = sv.SvDebug(0, 0, 0, 0, 0, 0, spin, order)
     call.out_tokens.fill_(-9)
     call.out_n.fill_(-9)
     rc = call.run(d["target"], d["draft"], d["draft_tokens"], d["seq_offsets"], d["gammas"], b.temperature, seed, step)
@@ -48,13 +48,15 @@ def run_plain(b, seed, step, d=None, max_gamma=None, spin=0):
     return dict(tokens=call.out_tokens.cpu().numpy(), n=call.out_n.cpu().numpy(), status=call.status_bits())
 
 
-@pytest.mark.parametrize("name", ["b64_g5_v128256", "b256_g3_v152064_t0.8", "pointmass_b64_g5_v128256"])
-def test_slot_order_full_size(name):
+@pytest.mark.parametrize("name", ["b64_g5_v128256", "b256_g3_v152064_t0.8", "pointmass_b64_g5_v128256",
+                                  "b8_g4_v32000_t0.7"])
+@pytest.mark.parametrize("order", [0, 1, 2])
+def test_slot_order_full_size(name, order):
     b = synth.make_batch(name)
     d = parity.to_device(b)
     tot = dict(draws=0, band=0)
     for step in range(4):
-        g = run_plain(b, 1234, step, d=d)
+        g = run_plain(b, 1234, step, d=d, order=order)
         assert g["status"] == 0
         rep = parity.assert_parity(b, 1234, step, g=g, check_debug=False)
         tot["draws"] += rep["draws"]
