@@ -66,6 +66,12 @@ def lib():
                                         ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.POINTER(_Debug), ctypes.c_int]
             L.oracle_verify.restype = ctypes.c_uint32
+            L.oracle_verify_range.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                              ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.POINTER(_Debug), ctypes.c_int]
+            L.oracle_verify_range.restype = ctypes.c_uint32
             L.oracle_verify_steps.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
@@ -140,12 +146,14 @@ class Result:
 
 
 def verify(target, draft, draft_tokens, seq_offsets, gammas, V, temperature, seed, step,
-           nthreads: int | None = None) -> Result:
+           nthreads: int | None = None, seq_base: int = 0) -> Result:
     """Verify a CSR-packed batch on host arrays.
 
     target/draft: numpy arrays of float32 logits, or uint16 arrays holding raw bf16 bits, with
     shapes [R_t, V] / [R_d, V]. draft None with temperature > 0: the drafts are point masses (an
-    n-gram drafter's). Returns a ``Result`` with tokens, counts and debug values.
+    n-gram drafter's). seq_base: the global index of sequence 0 when the batch is a contiguous range
+    of a larger one (its uniforms are then the larger batch's). Returns a ``Result`` with tokens,
+    counts and debug values.
     """
     target = np.ascontiguousarray(target)
     dtype = BF16 if target.dtype == np.uint16 else F32
@@ -165,10 +173,10 @@ def verify(target, draft, draft_tokens, seq_offsets, gammas, V, temperature, see
                  _ptr(res.seq_mass), _ptr(res.seq_fallback), _ptr(res.beta))
     if nthreads is None:
         nthreads = len(os.sched_getaffinity(0))
-    res.status = lib().oracle_verify(_ptr(target), _ptr(draft), dtype, _ptr(tok), _ptr(offs),
-                                     _ptr(gam), B, V, float(temperature), seed, step,
-                                     _ptr(res.tokens), _ptr(res.num_accepted), ctypes.byref(dbg),
-                                     int(nthreads))
+    res.status = lib().oracle_verify_range(_ptr(target), _ptr(draft), dtype, _ptr(tok), _ptr(offs),
+                                           _ptr(gam), B, V, float(temperature), seed, step, int(seq_base),
+                                           _ptr(res.tokens), _ptr(res.num_accepted), ctypes.byref(dbg),
+                                           int(nthreads))
     return res
 
 

@@ -241,6 +241,7 @@ typedef struct {
     oracle_debug* dbg;
     int32_t b0, b1;
     int32_t nsteps;   /* sampling mode: draws for steps step .. step + nsteps - 1 (outputs step-major) */
+    uint32_t seq_base;/* global index of sequence 0: sequence b's uniforms are keyed by seq_base + b */
     uint32_t status;
 } job_t;
 
@@ -317,8 +318,8 @@ static void verify_one(job_t* J, int32_t b, double* prow, double* qrow, double* 
     for (int32_t s = 0; s < J->nsteps; ++s) {
         const uint64_t step = J->step + (uint64_t)s;
         for (int32_t i = 0; i <= g; ++i) {
-            u_acc[i] = oracle_uniform(J->seed, step, (uint32_t)b, (uint32_t)i, 0);
-            u_smp[i] = oracle_uniform(J->seed, step, (uint32_t)b, (uint32_t)i, 1);
+            u_acc[i] = oracle_uniform(J->seed, step, J->seq_base + (uint32_t)b, (uint32_t)i, 0);
+            u_smp[i] = oracle_uniform(J->seed, step, J->seq_base + (uint32_t)b, (uint32_t)i, 1);
         }
         double S = 0.0;
         int32_t fb = 0;
@@ -353,7 +354,7 @@ static void* run_job(void* arg) {
  */
 static uint32_t verify_batch(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
                              const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V,
-                             double temperature, uint64_t seed, uint64_t step, int32_t nsteps,
+                             double temperature, uint64_t seed, uint64_t step, uint32_t seq_base, int32_t nsteps,
                              int32_t* out_tokens, int32_t* out_num_accepted, oracle_debug* dbg, int nthreads) {
     if (B < 0 || V <= 0 || !(temperature >= 0.0) || isinf(temperature) || !target || !seq_offsets ||
         !gammas || !out_tokens || !out_num_accepted || nsteps < 1)
@@ -375,6 +376,7 @@ static uint32_t verify_batch(const void* target, const void* draft, int dtype, c
         J->seed = seed; J->step = step; J->out_tok = out_tokens; J->out_n = out_num_accepted;
         J->dbg = dbg;
         J->nsteps = nsteps;
+        J->seq_base = seq_base;
         J->b0 = (int32_t)((int64_t)B * t / nthreads);
         J->b1 = (int32_t)((int64_t)B * (t + 1) / nthreads);
     }
@@ -394,7 +396,20 @@ uint32_t oracle_verify(const void* target, const void* draft, int dtype, const i
                        double temperature, uint64_t seed, uint64_t step, int32_t* out_tokens,
                        int32_t* out_num_accepted, oracle_debug* dbg, int nthreads) {
     return verify_batch(target, draft, dtype, draft_tokens, seq_offsets, gammas, B, V, temperature, seed, step,
-                        1, out_tokens, out_num_accepted, dbg, nthreads);
+                        0u, 1, out_tokens, out_num_accepted, dbg, nthreads);
+}
+
+/*
+ * oracle_verify on a contiguous range of a larger batch whose sequence 0 is the batch's sequence
+ * seq_base: the uniforms of sequence b are those of the batch's sequence seq_base + b, so verifying the
+ * ranges of a batch separately and concatenating their outputs gives the whole batch's outputs.
+ */
+uint32_t oracle_verify_range(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                             const int32_t* seq_offsets, const int32_t* gammas, int32_t B, int32_t V,
+                             double temperature, uint64_t seed, uint64_t step, uint32_t seq_base,
+                             int32_t* out_tokens, int32_t* out_num_accepted, oracle_debug* dbg, int nthreads) {
+    return verify_batch(target, draft, dtype, draft_tokens, seq_offsets, gammas, B, V, temperature, seed, step,
+                        seq_base, 1, out_tokens, out_num_accepted, dbg, nthreads);
 }
 
 /*
@@ -409,7 +424,7 @@ uint32_t oracle_verify_steps(const void* target, const void* draft, int dtype, c
                              int32_t* out_tokens, int32_t* out_num_accepted, int nthreads) {
     if (!(temperature > 0.0)) return 1u << OR_ERR_INVALID_ARG;
     return verify_batch(target, draft, dtype, draft_tokens, seq_offsets, gammas, B, V, temperature, seed, step,
-                        nsteps, out_tokens, out_num_accepted, NULL, nthreads);
+                        0u, nsteps, out_tokens, out_num_accepted, NULL, nthreads);
 }
 
 /*
