@@ -137,6 +137,20 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
                    const sv_debug* debug, void* cuda_stream);
 
 /*
+ * One contiguous range of a larger batch (a batch split over GPUs by sequence, or over calls): exactly
+ * spec_verify_ex, with seq_base the index in the whole batch of this call's sequence 0. The uniforms of
+ * sequence b are keyed by seq_base + b (mod 2^32), so verifying the ranges [s0, s1) of a batch, each with
+ * seq_base = s0, and concatenating their outputs gives the whole batch's outputs (the draws of a sequence
+ * depend only on its own rows and its global index). spec_verify_ex is this call with seq_base = 0.
+ */
+int spec_verify_range(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                      int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
+                      uint64_t step, uint32_t seq_base, int32_t* out_tokens, int32_t* out_num_accepted,
+                      uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                      const sv_debug* debug, void* cuda_stream);
+
+/*
  * Device staging buffers of spec_verify_host, sized by the caller for the batch: target_logits
  * R_t x V elements, draft_logits R_d x V (may be NULL when the host call passes no draft logits),
  * draft_tokens R_d, seq_offsets B + 1, gammas B, out_tokens R_t, out_num_accepted B (R_d =

@@ -57,7 +57,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
                 float temperature, uint64_t seed, uint64_t step, int32_t* out_tokens, int32_t* out_num_accepted,
                 uint32_t* device_status, void* workspace, size_t workspace_bytes, const sv_debug* debug,
                 const CommitBufs* commit, const int32_t* parents, int32_t* out_path, void* cuda_stream,
-                bool validate_only = false) {
+                bool validate_only = false, uint32_t seq_base = 0) {
     if (B < 0 || V < 1 || max_gamma < 0 || max_gamma > SV_MAX_GAMMA) return SV_ERR_INVALID_ARG;
     if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
     if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
@@ -124,6 +124,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, sv_dtype dt
     P.invT64 = greedy ? 0.0 : 1.0 / (double)temperature;
     P.seed = seed;
     P.step = step;
+    P.seq_base = seq_base;
     P.out_tokens = out_tokens;
     P.out_n = out_num_accepted;
     P.status = device_status ? device_status : (uint32_t*)(ws + L.status);
@@ -167,6 +168,17 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype
     return verify_impl(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
                        temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
                        workspace_bytes, debug, nullptr, nullptr, nullptr, cuda_stream);
+}
+
+int spec_verify_range(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_tokens, const int32_t* seq_offsets, const int32_t* gammas,
+                      int32_t B, int32_t V, int32_t max_gamma, float temperature, uint64_t seed,
+                      uint64_t step, uint32_t seq_base, int32_t* out_tokens, int32_t* out_num_accepted,
+                      uint32_t* device_status, void* workspace, size_t workspace_bytes,
+                      const sv_debug* debug, void* cuda_stream) {
+    return verify_impl(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                       temperature, seed, step, out_tokens, out_num_accepted, device_status, workspace,
+                       workspace_bytes, debug, nullptr, nullptr, nullptr, cuda_stream, false, seq_base);
 }
 
 int spec_verify_fused(const void* target_logits, const void* draft_logits, sv_dtype dtype,

@@ -120,6 +120,7 @@ struct Params {
                        // testing the time-out path asks for fewer)
     double invT64;     // 1 / T (debug output of the row log-normalisers only)
     uint64_t seed, step;
+    uint32_t seq_base;  // global index of sequence 0: sequence b's uniforms are keyed by seq_base + b
     int32_t* out_tokens;
     int32_t* out_n;
     uint32_t* status;

@@ -698,8 +698,8 @@ __device__ __noinline__ void decide(const Params& P, int32_t b, int32_t g, int32
         }
     }
     if (!GREEDY && wsub == 0) {
-        if (lane < g) u_acc = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);
-        if (lane <= g) u_draw = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 1);
+        if (lane < g) u_acc = philox_uniform(P.seed, P.step, P.seq_base + (uint32_t)b, (uint32_t)lane, 0);
+        if (lane <= g) u_draw = philox_uniform(P.seed, P.step, P.seq_base + (uint32_t)b, (uint32_t)lane, 1);
     }
     // row statistics: row jr's (max, sum) or (max, argmax) ends on lane jr & 31, register jr >> 5
     float my_m0 = -INFINITY, my_m1 = -INFINITY, my_s0 = 0.f, my_s1 = 0.f;
@@ -971,9 +971,9 @@ __device__ __noinline__ void decide_prog(const Params& P, int32_t b, int32_t g, 
             lt = logit_at<DT>(P.target, (size_t)(t0 + lane) * P.V + x);
             ld = logit_at<DT>(P.draft, (size_t)(o0 + lane) * P.V + x);
         }
-        u_acc = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 0);
+        u_acc = philox_uniform(P.seed, P.step, P.seq_base + (uint32_t)b, (uint32_t)lane, 0);
     }
-    if (lane <= g) u_draw = philox_uniform(P.seed, P.step, (uint32_t)b, (uint32_t)lane, 1);
+    if (lane <= g) u_draw = philox_uniform(P.seed, P.step, P.seq_base + (uint32_t)b, (uint32_t)lane, 1);
     err = warp_or(err);
     // rows (max, sum) of the current slot; the loads of slot s + 1 are issued once slot s's words are in
     float Mt = -INFINITY, St = 0.f, Md = 0.f, Sd = 1.f;

@@ -18,7 +18,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_MAX_GAMMA = 31
 
 # every exported symbol of the C ABI, in header order
-EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
+EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_range", "spec_verify_noalloc",
            "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
            "spec_shard_stats", "spec_shard_decide", "spec_shard_chunks", "spec_shard_sums", "spec_shard_finish",
            "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host")
@@ -49,6 +49,9 @@ def _load():
     L.spec_verify_ex.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
                                  vp, vp, sz, ctypes.POINTER(SvDebug), vp]
     L.spec_verify_ex.restype = ctypes.c_int
+    L.spec_verify_range.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, ctypes.c_uint32,
+                                    vp, vp, vp, vp, sz, ctypes.POINTER(SvDebug), vp]
+    L.spec_verify_range.restype = ctypes.c_int
     L.spec_verify_noalloc.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, i32, i32, i32, f32, u64, u64, vp, vp,
                                       vp, ctypes.POINTER(SvDebug), vp]
     L.spec_verify_noalloc.restype = ctypes.c_int
@@ -104,6 +107,16 @@ def spec_verify_ex(target_logits, draft_logits, dtype, draft_tokens, seq_offsets
                               max_gamma, float(temperature), seed, step, out_tokens, out_num_accepted,
                               device_status, workspace, workspace_bytes,
                               ctypes.byref(debug) if debug is not None else None, cuda_stream)
+
+
+def spec_verify_range(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
+                      temperature, seed, step, seq_base, out_tokens, out_num_accepted, device_status, workspace,
+                      workspace_bytes, debug: SvDebug | None, cuda_stream) -> int:
+    """spec_verify_ex on a contiguous range of a larger batch whose sequence 0 is the batch's seq_base."""
+    return lib.spec_verify_range(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V,
+                                 max_gamma, float(temperature), seed, step, seq_base, out_tokens, out_num_accepted,
+                                 device_status, workspace, workspace_bytes,
+                                 ctypes.byref(debug) if debug is not None else None, cuda_stream)
 
 
 def spec_verify_noalloc(target_logits, draft_logits, dtype, draft_tokens, seq_offsets, gammas, B, V, max_gamma,
@@ -249,15 +262,15 @@ class Call:
                                         ("row_lse", "row_argmax", "p_x", "q_x", "seq_mass", "beta")), 0)
 
     def run(self, target, draft, draft_tokens, seq_offsets, gammas, temperature, seed, step, stream=None,
-            clear_status=True) -> int:
+            clear_status=True, seq_base=0) -> int:
         import torch
         if clear_status:
             self.status.zero_()
         st = stream if stream is not None else torch.cuda.current_stream()
-        return spec_verify_ex(_ptr(target), _ptr(draft), dtype_code(target), _ptr(draft_tokens),
-                              _ptr(seq_offsets), _ptr(gammas), self.B, self.V, self.max_gamma, temperature,
-                              seed, step, _ptr(self.out_tokens), _ptr(self.out_n), _ptr(self.status),
-                              _ptr(self.workspace), self.ws_bytes, self.dbg_struct, st.cuda_stream)
+        return spec_verify_range(_ptr(target), _ptr(draft), dtype_code(target), _ptr(draft_tokens),
+                                 _ptr(seq_offsets), _ptr(gammas), self.B, self.V, self.max_gamma, temperature,
+                                 seed, step, seq_base, _ptr(self.out_tokens), _ptr(self.out_n), _ptr(self.status),
+                                 _ptr(self.workspace), self.ws_bytes, self.dbg_struct, st.cuda_stream)
 
     def run_host(self, target, draft, draft_tokens, seq_offsets, gammas, temperature, seed, step, out_tokens,
                  out_num_accepted, staging, stream=None, clear_status=True) -> int:

@@ -28,7 +28,8 @@ def declared_functions():
 
 def test_header_declares_the_api():
     names = declared_functions()
-    assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_noalloc",
+    assert set(names) == {"spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_verify_range",
+                          "spec_verify_noalloc",
                           "spec_verify_commit", "spec_verify_fused", "spec_draft_ngram", "spec_verify_tree",
                           "spec_verify_status_from_bits", "spec_verify_status_string", "spec_verify_host",
                           "spec_shard_stats", "spec_shard_decide", "spec_shard_chunks", "spec_shard_sums",
