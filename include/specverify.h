@@ -90,6 +90,11 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
  *              0 the library's choice; 1 sequence order; 2 slot order wherever the call allows it (bf16
  *              rows on 16-byte boundaries, sampling with draft rows, linear drafts, none of the per-row
  *              fields above, B < 1024 and B (2 max_gamma + 1) <= 2048), whatever the batch's size.
+ *   cluster    the small-batch form, for tests (the outputs are the same): 0 the library's choice (sampled
+ *              batches small enough that the persistent launch would give each streaming warp at most one
+ *              statistics task run one CTA cluster of up to 8 CTAs per sequence; greedy batches keep the
+ *              persistent launch); 1 never; 2 wherever the call allows it, greedy included (linear drafts,
+ *              none of the array fields above, V <= 131072, B clusters fit the SMs).
  */
 typedef struct {
     double* row_lse;
@@ -100,6 +105,7 @@ typedef struct {
     double* beta;
     uint32_t spin_limit;
     uint32_t order;
+    uint32_t cluster;
 } sv_debug;
 
 /*

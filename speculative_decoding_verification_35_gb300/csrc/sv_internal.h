@@ -185,6 +185,11 @@ struct ShardArgs {
     cudaStream_t stream;
     float2 exp2_tab[128];
 };
+// Small batches: one CTA cluster per sequence (sv_small.cu). small_eligible: the call can take that path
+// (sets the cluster size); launch_small: the launch.
+bool small_eligible(const Params& P, int sms, int32_t* clusters);
+cudaError_t launch_small(const Params& P, int dtype, int32_t clusters, cudaStream_t st);
+
 // stage 0: statistics (a = partials of this shard); 1: decisions (a = all partials, b = draws);
 // 2: sums (a = draws, b = this shard's per-chunk sums); 3: finish (a = draws, b = all shards' sums)
 cudaError_t launch_shard(int stage, const ShardArgs& A, void* a, void* b, void* c);

@@ -2306,6 +2306,19 @@ static cudaError_t launch_typed(const Params& P, cudaStream_t st) {
 cudaError_t launch_verify(const Params& P, const Layout& L, void* ws, int dtype, bool vec, bool greedy,
                           cudaStream_t st) {
     if (P.B == 0) return cudaSuccess;
+    {  // small sampled batches (at most one statistics task per streaming warp of the persistent launch): one
+       // CTA cluster per sequence (sv_debug.cluster: 1 never, 2 whenever the call allows it, greedy included;
+       // a greedy step, a decision without a draw, is shorter as the persistent launch)
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        int32_t C = 0;
+        const int64_t rows = (int64_t)P.B * (greedy || P.pm ? P.max_gamma + 1 : 2 * P.max_gamma + 1);
+        const bool small = P.dbg.cluster == 2u ||
+                           (P.dbg.cluster == 0u && !greedy && rows * P.nchA <= (int64_t)sms * kStreamWarps);
+        if (small && P.dbg.cluster != 1u && small_eligible(P, sms, &C)) return launch_small(P, dtype, C, st);
+    }
     cudaError_t e = cudaMemsetAsync((char*)ws + L.zero_begin, 0, L.zero_end - L.zero_begin, st);
     if (e != cudaSuccess) return e;
     if (dtype == SV_BF16) {

@@ -27,7 +27,8 @@ EXPORTS = ("spec_verify", "spec_verify_workspace_size", "spec_verify_ex", "spec_
 class SvDebug(ctypes.Structure):
     _fields_ = [("row_lse", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p),
                 ("p_x", ctypes.c_void_p), ("q_x", ctypes.c_void_p), ("seq_mass", ctypes.c_void_p),
-                ("beta", ctypes.c_void_p), ("spin_limit", ctypes.c_uint32), ("order", ctypes.c_uint32)]
+                ("beta", ctypes.c_void_p), ("spin_limit", ctypes.c_uint32), ("order", ctypes.c_uint32),
+                ("cluster", ctypes.c_uint32)]
 
 
 class SvDeviceBuffers(ctypes.Structure):

@@ -39,7 +39,7 @@ def run_plain(b, seed, step, d=None, max_gamma=None, spin=0, order=2):
     d = d or parity.to_device(b)
     mg = int(b.gammas.max()) if max_gamma is None else max_gamma
     call = sv.Call(b.B, b.V, mg, b.R_t, b.R_d)
-    call.dbg_struct = sv.SvDebug(0, 0, 0, 0, 0, 0, spin, order)
+    call.dbg_struct = sv.SvDebug(0, 0, 0, 0, 0, 0, spin, order, 1)  # the persistent launch (no cluster form)
     call.out_tokens.fill_(-9)
     call.out_n.fill_(-9)
     rc = call.run(d["target"], d["draft"], d["draft_tokens"], d["seq_offsets"], d["gammas"], b.temperature, seed, step)
