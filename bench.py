@@ -57,14 +57,23 @@ def code_only(src: str) -> str:
     return " ".join(src.split())
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources' code (comments and layout excluded), keying profiled figures to the
-    code they were measured on."""
+# the sources a profiled kernel's launch is built from: its kernel file, the device helpers, the shared
+# declarations, the host code that fills its parameters and picks its launch, and the public header
+KERNEL_SOURCES = {
+    "k_verify": ("speculative_decoding_verification_35_gb300/csrc/sv_api.cu",
+                 "speculative_decoding_verification_35_gb300/csrc/sv_kernels.cu",
+                 "speculative_decoding_verification_35_gb300/csrc/sv_device.cuh",
+                 "speculative_decoding_verification_35_gb300/csrc/sv_internal.h",
+                 "include/specverify.h"),
+}
+
+
+def kernel_source_hash(kernel: str = "k_verify") -> str:
+    """Hash of the code (comments and layout excluded) of the sources a kernel is built from, keying
+    profiled figures to the code they were measured on."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "speculative_decoding_verification_35_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode() + b"\0" + code_only(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(f.encode() + b"\0" + code_only(open(os.path.join(ROOT, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,3 +32,10 @@ def test_hash_is_stable_and_short():
     b = _bench()
     h = b.kernel_source_hash()
     assert h == b.kernel_source_hash() and len(h) == 16
+
+
+def test_hash_covers_existing_sources_of_the_kernel():
+    b = _bench()
+    for f in b.KERNEL_SOURCES["k_verify"]:
+        assert os.path.exists(os.path.join(ROOT, f)), f
+    assert any(f.endswith("sv_kernels.cu") for f in b.KERNEL_SOURCES["k_verify"])
