@@ -115,6 +115,8 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_small(const __grid_constant__
     __shared__ int redi[kSmWarps];
     __shared__ ff s_rho, s_rem;
     __shared__ int s_owner, s_byp, s_tail, s_col;
+    __shared__ int32_t s_tok[32];   // CTA 0: the draft tokens of slots 0 .. g - 1
+    __shared__ float s_u[2][32];    // CTA 0: the accept and draw uniforms of every slot
     if (tid < kExpTab) {
         tab[tid] = P.exp2_tab[tid].x;
         tab[kExpTab + tid] = P.exp2_tab[tid].y;
@@ -143,6 +145,14 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_small(const __grid_constant__
     const int32_t v0 = (int32_t)((int64_t)V * j / C), v1 = (int32_t)((int64_t)V * (j + 1) / C);
     const float K = P.K_hi;
     const ExpConst EC{P.K_hi, P.K_lo, P.d_min};
+    if (j == 0 && warp == kSmWarps - 1) {  // the decision's inputs that need no statistics, under phase 1
+        s_tok[lane] = lane < g ? __ldg(P.tokens + o0 + lane) : -1;
+        if (!greedy) {
+            const uint32_t seq = P.seq_base + (uint32_t)b;
+            s_u[0][lane] = philox_uniform(P.seed, P.step, seq, (uint32_t)lane, 0);
+            s_u[1][lane] = philox_uniform(P.seed, P.step, seq, (uint32_t)lane, 1);
+        }
+    }
 
     // 1. partial statistics of every row over the slice. The slice of a row is cut into np pieces so that
     // every warp has an item (row r, piece p); a warp reads its piece with 16-byte loads (scalar elements
@@ -339,7 +349,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_small(const __grid_constant__
         int32_t x = -1;
         uint32_t tcode = 0;
         if (lane < g) {
-            x = __ldg(P.tokens + o0 + lane);
+            x = s_tok[lane];
             if (x < 0 || x >= V) tcode = SV_ERR_BAD_TOKEN;
         }
         float Tm = -INFINITY, Ts = 0.f, Dm = 0.f, Ds = 1.f;
@@ -385,15 +395,12 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_small(const __grid_constant__
             drawn = __shfl_sync(0xFFFFFFFFu, Ta, n);
         } else {
             bool ok = true;
-            // every lane: the draw's uniform if the draw falls on its slot (taken by slot once n is known)
-            const float u_draw = philox_uniform(P.seed, P.step, P.seq_base + (uint32_t)b, (uint32_t)lane, 1);
             if (lane < g) {
                 const float lt = gval(lane, x), ld = P.pm ? 0.f : gval(g + 1 + lane, x);
                 const ff2 e = exp2_ff2(make_float2(lt, ld), make_float2(Tm, P.pm ? 0.f : Dm), EC, tab);
                 const float px = div_fma(e.hi.x + e.lo.x, Ts);
                 const float qx = P.pm ? 1.f : div_fma(e.hi.y + e.lo.y, Ds);
-                const float u = philox_uniform(P.seed, P.step, P.seq_base + (uint32_t)b, (uint32_t)lane, 0);
-                ok = u * qx < px;
+                ok = s_u[0][lane] * qx < px;
             }
             const uint32_t rej = __ballot_sync(0xFFFFFFFFu, lane < g && !ok);
             n = rej ? __ffs(rej) - 1 : g;
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_small(const __grid_constant__
             const float qm = __shfl_sync(0xFFFFFFFFu, Dm, n), qs = __shfl_sync(0xFFFFFFFFu, Ds, n);
             dw.m_q = n < g && !P.pm ? qm : 0.f;
             dw.rho = n < g && !P.pm ? div_fma(ps, qs) : 1.f;
-            dw.u = __shfl_sync(0xFFFFFFFFu, u_draw, n);
+            dw.u = s_u[1][n];
             dw.xcl = n < g && P.pm ? __shfl_sync(0xFFFFFFFFu, x, n) : -1;
         }
         if (lane < C) *cl.map_shared_rank(&draw, (unsigned)lane) = dw;
