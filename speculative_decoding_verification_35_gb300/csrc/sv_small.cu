@@ -29,6 +29,7 @@ namespace {
 constexpr int kSmThreads = 512;
 constexpr int kSmWarps = kSmThreads / 32;
 constexpr int kSmRows = 2 * SV_MAX_GAMMA + 1;
+constexpr int kSmBatch = 8;    // 16-byte loads a lane issues together in phase 1
 constexpr int kSmParts = 128;  // piece records of a CTA (rows x pieces; one piece a row always fits)
 
 struct SmRec {  // one row's partial statistics over a CTA's slice
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_small(const __grid_constant__
     // before the first aligned address and after the last whole vector); a tie in the maximum goes to the
     // lower column, whatever order a lane takes its columns in.
     const int32_t Ls = v1 - v0;
-    const int32_t np = max(1, min((kSmWarps + nrows - 1) / nrows, Ls / 256));  // pieces a row
+    const int32_t np = max(1, min(kSmWarps / nrows, Ls / 256));  // pieces a row: at most one item a warp
     auto piece_lo = [&](int32_t p) {  // interior boundaries on 64-column multiples (aligned vectors)
         if (p == 0 || p == np) return p == 0 ? v0 : v1;
         return max(v0, (v0 + (int32_t)((int64_t)Ls * p / np)) & ~63);
@@ -218,15 +219,15 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_small(const __grid_constant__
             if (lane < e - tail) xt = lgs<DT>(base, row + tail + lane);
         }
         const uint4* vp = (const uint4*)((const char*)base + (row + (size_t)body) * ES);
-        for (int32_t v0b = 0; v0b < nvec; v0b += 32 * 4) {
-            uint4 u[4];
+        for (int32_t v0b = 0; v0b < nvec; v0b += 32 * kSmBatch) {
+            uint4 u[kSmBatch];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kSmBatch; ++i) {
                 const int32_t v = v0b + lane + 32 * i;
                 if (v < nvec) u[i] = __ldg(vp + v);
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kSmBatch; ++i) {
                 const int32_t v = v0b + lane + 32 * i;
                 if (v < nvec) {
                     float x[VE];
