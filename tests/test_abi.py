@@ -59,18 +59,24 @@ def test_header_compiles_as_c(tmp_path):
 
 
 def test_binding_structs_match_the_header(tmp_path):
-    """The ctypes structures of the binding have the C structures' sizes and field offsets."""
+    """The ctypes structures of the binding have the C structures' sizes and every field's offset."""
     from speculative_decoding_verification_35_gb300 import specverify as sv
+    structs = (("sv_debug", sv.SvDebug), ("sv_device_buffers", sv.SvDeviceBuffers))
+    lines = []
+    for cname, py in structs:
+        lines.append(f'printf("%zu\\n", sizeof({cname}));')
+        for field, _ in py._fields_:
+            lines.append(f'printf("%zu\\n", offsetof({cname}, {field}));')
     c = tmp_path / "sizes.c"
     c.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "specverify.h"\n'
-                 'int main(void){ printf("%zu %zu %zu %zu\\n", sizeof(sv_debug), offsetof(sv_debug, spin_limit),'
-                 ' offsetof(sv_debug, order), sizeof(sv_device_buffers)); return 0; }\n')
+                 'int main(void){ ' + " ".join(lines) + ' return 0; }\n')
     exe = tmp_path / "sizes"
     subprocess.check_call(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(c), "-o", str(exe)])
-    size, spin_off, order_off, dev_size = map(int, subprocess.check_output([str(exe)]).split())
-    assert ctypes.sizeof(sv.SvDebug) == size
-    assert sv.SvDebug.spin_limit.offset == spin_off and sv.SvDebug.order.offset == order_off
-    assert ctypes.sizeof(sv.SvDeviceBuffers) == dev_size
+    got = iter(map(int, subprocess.check_output([str(exe)]).split()))
+    for cname, py in structs:
+        assert ctypes.sizeof(py) == next(got), cname
+        for field, _ in py._fields_:
+            assert getattr(py, field).offset == next(got), (cname, field)
 
 
 def test_host_side_checks_without_gpu(libpath):
