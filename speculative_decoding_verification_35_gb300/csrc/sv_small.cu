@@ -9,8 +9,10 @@
 //   3. each CTA: the draw's exact sums over its slice (float-float on the 2^-20 grid, see grid_hi);
 //   4. every CTA finds the slice holding the draw's target u S (the same arithmetic on each); that CTA
 //      scans its slice for the drawn column and writes it.
-// For a batch whose persistent launch would give each statistics warp at most one task, a step is then a
-// chain of four phases on shared memory instead of handoff words polled across the GPU.
+// For a sampled batch whose persistent launch would give each statistics warp at most one task, a step is
+// then a chain of four phases on shared memory instead of handoff words polled across the GPU (a greedy
+// step, one decision without a draw, stays shorter as the persistent launch unless forced here). Every
+// wait is a cluster barrier among CTAs that the hardware schedules together; nothing is polled.
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
