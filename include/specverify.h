@@ -111,7 +111,7 @@ typedef struct {
 /*
  * The plain form: bf16 logits, the legacy default stream, blocking. It allocates its own
  * workspace and device status word, waits for the step to finish and returns SV_OK or the first
- * device error code (priority BAD_OFFSETS, BAD_TOKEN, NONFINITE, EMPTY_ROW, TIMEOUT). Host sizes
+ * device error code (priority BAD_OFFSETS, BAD_TOKEN, NONFINITE, EMPTY_ROW, TIMEOUT, CAPACITY). Host sizes
  * are read from gammas (copied to the host once) to size the workspace. temperature == 0 selects
  * greedy, in which case draft_logits may be NULL and is never read.
  */
