@@ -279,3 +279,16 @@ def test_host_buffer_form_checks_without_gpu(libpath):
     assert call(temperature=float("nan")) == sv.SV_ERR_INVALID_ARG
     assert call(workspace=None) == sv.SV_ERR_WORKSPACE
     assert call(B=0) == sv.SV_OK
+
+
+def test_binding_raises_without_the_library(tmp_path):
+    """A copy of the package without its compiled library fails at import: there is no fallback path."""
+    import shutil
+    import sys
+    src = os.path.join(ROOT, "speculative_decoding_verification_35_gb300")
+    shutil.copytree(src, tmp_path / "speculative_decoding_verification_35_gb300",
+                    ignore=shutil.ignore_patterns("*.so", "*.o", "csrc", "__pycache__"))
+    r = subprocess.run([sys.executable, "-c", "import speculative_decoding_verification_35_gb300.specverify"],
+                       cwd=tmp_path, capture_output=True, text=True, env={**os.environ, "PYTHONPATH": str(tmp_path)})
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "is not built" in r.stderr, r.stderr[-500:]
